@@ -1,0 +1,489 @@
+#!/usr/bin/env python3
+"""Throughput of the GDN library on one GB300 (or N, one process per GPU).
+
+One step is one pass of the whole path on seeded synthetic inputs resident in HBM:
+  * a chunked prefill of one Qwen3.5-style GDN layer: B=1, Hk=16, Hv=32 (GQA 2),
+    S=8192, Dk=Dv=128, bf16 q/k/v, fp32 g_log/beta, zero initial state;
+  * one fused decode step over B=256 x 32 value heads (BH=8192), K=V=128, fp32 state
+    [8192,128,128] updated in place, bf16 output.
+Each kernel is timed with CUDA events on the stream it is launched on. The decode
+step streams 1 GiB through HBM between two prefills, so every prefill starts with a
+cold L2 (and the decode's own 1 GiB state is far larger than L2).
+
+The JSON line reports prefill tokens/s as `value` (the headline), the prefill kernel's
+roofline, the decode step's state GB/s and its roofline, an end-to-end prefill number
+through the binding with host buffers, and the fp64 oracle timed on the host cores.
+`--impl reference` times that oracle alone (the CPU reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN prefill tokens/s & % roofline; decode-step state HBM GB/s vs peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM traffic per launch of the dominant kernel from one ncu capture, keyed by the
+# sha256 of the kernel's source file at capture time (reported only while it matches).
+NCU_TRAFFIC = {}
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-batched", action="store_true",
+                   help="skip the extra B=8, S=4096 prefill measurement")
+    return p.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------- algorithmic counts
+
+
+def prefill_bytes(w) -> int:
+    """Compulsory HBM bytes of one prefill: q,k at the key heads (read once, shared by
+    the GQA group), v and out at the value heads, g_log and beta, the state written
+    (and read when supplied)."""
+    e = 4 if w.dtype == "f32" else 2
+    qk = 2 * w.B * w.Hk * w.S * w.Dk * e
+    vo = 2 * w.B * w.Hv * w.S * w.Dv * e
+    gb = 2 * w.B * w.Hv * w.S * 4
+    st = w.B * w.Hv * w.Dk * w.Dv * 4 * (2 if w.state_std is not None else 1)
+    return qk + vo + gb + st
+
+
+def prefill_flops(w, C: int = 64) -> float:
+    """FLOPs of the chunked form at C=64, products counted densely, the O(C^3) solve
+    ignored: per token per value head 2C(2Dk/G + Dk + 2Dv) + 6 Dk Dv (the Gram
+    products once per key head)."""
+    G = w.Hv // w.Hk
+    per = 2 * C * (2 * w.Dk / G + w.Dk + 2 * w.Dv) + 6 * w.Dk * w.Dv
+    return per * w.B * w.S * w.Hv
+
+
+def decode_bytes(w) -> tuple[int, int]:
+    """(state bytes, all bytes) of one decode step: the fp32 state in and out, the
+    q,k,v,z rows, b and a, out, and the per-head and per-column parameters."""
+    state = 2 * w.BH * w.K * w.V * 4
+    rows = w.BH * (2 * w.K + 2 * w.V) * 2 + 2 * w.BH * 2 + w.BH * w.V * 2
+    params = 2 * w.num_v_heads * 4 + w.V * 4
+    return state, state + rows + params
+
+
+# ----------------------------------------------------------------------- clock sampling
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks, power and throttle reasons every 200 ms."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        import torch
+        self.proc = None
+        self.path = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            ident = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+        except Exception:
+            ident = str(device_index)
+        self.ident = ident
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.ident, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 8:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    smax.append(float(parts[1]))
+                    power.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[4:8]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "power_w_max": max(power), "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------- distributed
+
+
+def dist_init():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return ws, rank, local
+
+
+def reduce_max(values, ws):
+    """Max over ranks of a list of floats (identity for one process)."""
+    if ws == 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" \
+        else torch.device("cpu")
+    t = torch.tensor(list(values), dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.cpu().tolist()
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------------- CPU oracle
+
+
+def cpu_oracle_prefill(w, x, nthreads):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.prefill(x["q"], x["k"], x["v"], x["g_log"], x["beta"], x["scale"], x["state"],
+                   nthreads=nthreads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(wp, xp, wd, xd):
+    import oracle
+    n = os.cpu_count() or 1
+    oracle.build()
+    dt = cpu_oracle_prefill(wp, xp, n)
+    rows = 2048
+    names = ("q", "k", "v", "b", "a", "A_log", "dt_bias", "z", "norm_weight", "state")
+    sub = {k: (xd[k][:rows] if k in ("q", "k", "v", "b", "a", "z", "state") else xd[k])
+           for k in names}
+    t0 = time.perf_counter()
+    oracle.decode_step(*(sub[k] for k in names), xd["num_v_heads"], nthreads=n)
+    dd = time.perf_counter() - t0
+    return {"value": wp.tokens / dt, "unit": "tokens/s", "cores": n, "kind": "oracle",
+            "sample": f"fp64 token recurrence over the whole prefill workload ({wp.name}, "
+                      f"all {wp.B * wp.Hv} value heads), {n} threads, {dt:.2f} s wall",
+            "decode": {"value": 2 * rows * wd.K * wd.V * 4 / dd / 1e9, "unit": "GB/s state",
+                       "sample": f"{rows} of {wd.BH} rows, {dd:.2f} s wall"}}
+
+
+# ------------------------------------------------------------------------- arms
+
+
+def run_reference(args):
+    ws, rank, _ = dist_init()
+    if rank != 0:
+        return 0
+    from linear_attention_recurrence_03_gb300 import synthetic as syn
+    import oracle
+    oracle.build()
+    wp = syn.PREFILL_BF16_LAYER
+    xp = syn.prefill_inputs(wp)
+    n = os.cpu_count() or 1
+    for _ in range(args.warmup):
+        cpu_oracle_prefill(wp, xp, n)
+    times = [cpu_oracle_prefill(wp, xp, n) for _ in range(args.steps)]
+    t = sum(times) / len(times)
+    value = wp.tokens / t
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; Qwen3.5-style GDN layer shapes, no weights)",
+        "config": {"workload": wp.name, "B": wp.B, "Hk": wp.Hk, "Hv": wp.Hv, "S": wp.S,
+                   "Dk": wp.Dk, "Dv": wp.Dv},
+        "impl": "reference",
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": n, "kind": "oracle",
+                         "sample": f"each step: the fp64 token recurrence over the whole "
+                                   f"prefill workload ({wp.B * wp.Hv} value heads x {wp.S} "
+                                   f"tokens) on {n} threads"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _kernel_source_sha(name):
+    p = os.path.join(ROOT, "linear_attention_recurrence_03_gb300", "csrc", name)
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def run_gdn(args):
+    import torch
+
+    ws, rank, local = dist_init()
+    if not torch.cuda.is_available():
+        print(json.dumps({"metric": METRIC, "error": "no CUDA device"}))
+        return 1
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from linear_attention_recurrence_03_gb300 import build as lib_build
+    lib_build.build()
+    import linear_attention_recurrence_03_gb300 as gdn
+    from linear_attention_recurrence_03_gb300 import synthetic as syn
+
+    peaks, peak_src = load_peaks()
+    wp, wd, wb = syn.PREFILL_BF16_LAYER, syn.DECODE_BH8192, syn.PREFILL_BF16_BATCHED
+
+    # inputs: drawn on the host (seeded), copied once to HBM
+    xp = syn.prefill_inputs(wp)
+    xd = syn.decode_inputs(wd)
+    P = {n: xp[n].to(dev) for n in ("q", "k", "v", "g_log", "beta")}
+    p_out = torch.empty((wp.B, wp.Hv, wp.S, wp.Dv), dtype=torch.bfloat16, device=dev)
+    p_state = torch.empty((wp.B, wp.Hv, wp.Dk, wp.Dv), dtype=torch.float32, device=dev)
+    dnames = ("q", "k", "v", "b", "a", "A_log", "dt_bias", "z", "norm_weight", "state")
+    D = {n: xd[n].to(dev) for n in dnames}
+    d_out = torch.empty((wd.BH, wd.V), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+    lib = gdn.load_library()
+
+    import ctypes
+    vp = ctypes.c_void_p
+    sptr = vp(stream.cuda_stream)
+    pargs = [vp(P[n].data_ptr()) for n in ("q", "k", "v", "g_log", "beta")]
+
+    def prefill():
+        rc = lib.gdn_prefill(*pargs, float(xp["scale"]), gdn.GDN_DTYPE_BF16, wp.B, wp.Hk, wp.Hv,
+                             wp.S, wp.Dk, wp.Dv, vp(p_state.data_ptr()), 0,
+                             vp(p_out.data_ptr()), None, 0, sptr)
+        if rc != 0:
+            raise RuntimeError(gdn.gdn_last_error())
+
+    dargs = [vp(D[n].data_ptr()) for n in dnames] + [vp(D["state"].data_ptr()),
+                                                     vp(d_out.data_ptr())]
+
+    def decode():
+        rc = lib.gdn_decode_step(*dargs, wd.BH, wd.num_v_heads, wd.K, wd.V, sptr)
+        if rc != 0:
+            raise RuntimeError(gdn.gdn_last_error())
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    # spin-up (untimed) so that the clock samples see the GPU under this load
+    t_end = time.perf_counter() + 1.0
+    while time.perf_counter() < t_end:
+        prefill()
+        decode()
+        torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        prefill()
+        decode()
+    torch.cuda.synchronize()
+    barrier(ws)
+    torch.cuda.synchronize()
+
+    K = args.steps
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    e2 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    launches0 = gdn.gdn_launch_count()
+    t_wall = time.perf_counter()
+    for i in range(K):
+        e0[i].record(stream)
+        prefill()
+        e1[i].record(stream)
+        decode()
+        e2[i].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    barrier(ws)
+    launches = gdn.gdn_launch_count() - launches0
+    clk = clocks.stop()
+    if gdn.gdn_get_device_status() != gdn.GDN_OK:
+        raise RuntimeError("device status: " + gdn.gdn_last_error())
+
+    p_ms = sum(a.elapsed_time(b) for a, b in zip(e0, e1)) / K
+    d_ms = sum(a.elapsed_time(b) for a, b in zip(e1, e2)) / K
+    step_ms = e0[0].elapsed_time(e2[-1]) / K
+    p_ms, d_ms, step_ms = reduce_max([p_ms, d_ms, step_ms], ws)
+
+    tokens_per_s = ws * wp.tokens / (p_ms * 1e-3)
+    pb, pf = prefill_bytes(wp), prefill_flops(wp)
+    p_gbs = pb / (p_ms * 1e-3) / 1e9
+    p_tfs = pf / (p_ms * 1e-3) / 1e12
+    hbm = float(peaks["hbm_gbs"])
+    bf16 = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+    t_bytes, t_flops = pb / (hbm * 1e9), pf / (bf16 * 1e12)
+    bound = "hbm" if t_bytes >= t_flops else "tensor"
+    src_name = "prefill_simt.cu"
+    sha = _kernel_source_sha(src_name)
+    traffic = NCU_TRAFFIC.get(f"{src_name}@{sha}")
+    roof = {"bound": bound, "achieved": p_gbs if bound == "hbm" else p_tfs,
+            "peak": hbm if bound == "hbm" else bf16,
+            "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
+            "frac": (p_gbs / hbm) if bound == "hbm" else (p_tfs / bf16),
+            "traffic": traffic, "kernel": src_name, "peak_source": peak_src,
+            "algorithmic_bytes": pb, "algorithmic_flops": pf,
+            "tensor_tflops": p_tfs, "tensor_frac": p_tfs / bf16,
+            "roofline_ms": max(t_bytes, t_flops) * 1e3,
+            "frac_of_roofline": max(t_bytes, t_flops) / (p_ms * 1e-3)}
+    sb, db = decode_bytes(wd)
+    decode_info = {"workload": wd.name, "ms": d_ms,
+                   "state_gbs": sb / (d_ms * 1e-3) / 1e9,
+                   "roofline": {"bound": "hbm", "achieved": db / (d_ms * 1e-3) / 1e9,
+                                "peak": hbm, "unit": "GB/s",
+                                "frac": db / (d_ms * 1e-3) / 1e9 / hbm,
+                                "algorithmic_bytes": db, "peak_source": peak_src,
+                                "kernel": "decode.cu"}}
+
+    result = {
+        "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": ws,
+        "steps": K, "warmup": args.warmup, "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; Qwen3.5-style GDN layer shapes, no weights)",
+        "config": {"workload": f"{wp.name} + {wd.name}", "B": wp.B, "Hk": wp.Hk, "Hv": wp.Hv,
+                   "S": wp.S, "Dk": wp.Dk, "Dv": wp.Dv, "decode_BH": wd.BH,
+                   "l2": "inputs larger than L2: the 1 GiB decode state streams between "
+                         "prefills", "parallelism": f"replicas{ws}" if ws > 1 else "1 GPU"},
+        "prefill_ms": p_ms, "roofline": roof, "decode": decode_info,
+        "gpu_launches": launches, "clocks": clk, "wall_s_timed": t_wall,
+    }
+
+    # extra prefill measurement: B=8, Hk=16, Hv=32, S=4096, state in place
+    if not args.no_batched:
+        xb = syn.prefill_inputs(wb)
+        PB = {n: xb[n].to(dev) for n in ("q", "k", "v", "g_log", "beta")}
+        b_state = xb["state"].to(dev)
+        b_out = torch.empty((wb.B, wb.Hv, wb.S, wb.Dv), dtype=torch.bfloat16, device=dev)
+        bargs = [vp(PB[n].data_ptr()) for n in ("q", "k", "v", "g_log", "beta")]
+
+        def prefill_b():
+            rc = lib.gdn_prefill(*bargs, float(xb["scale"]), gdn.GDN_DTYPE_BF16, wb.B, wb.Hk,
+                                 wb.Hv, wb.S, wb.Dk, wb.Dv, vp(b_state.data_ptr()), 1,
+                                 vp(b_out.data_ptr()), None, 0, sptr)
+            if rc != 0:
+                raise RuntimeError(gdn.gdn_last_error())
+
+        for _ in range(args.warmup):
+            prefill_b()
+        torch.cuda.synchronize()
+        eb0 = torch.cuda.Event(enable_timing=True)
+        eb1 = torch.cuda.Event(enable_timing=True)
+        eb0.record(stream)
+        for _ in range(K):
+            prefill_b()
+        eb1.record(stream)
+        torch.cuda.synchronize()
+        b_ms = reduce_max([eb0.elapsed_time(eb1) / K], ws)[0]
+        bb, bf_ = prefill_bytes(wb), prefill_flops(wb)
+        rb = max(bb / (hbm * 1e9), bf_ / (bf16 * 1e12))
+        result["prefill_batched"] = {
+            "workload": wb.name, "ms": b_ms, "tokens_per_s": ws * wb.tokens / (b_ms * 1e-3),
+            "achieved_gbs": bb / (b_ms * 1e-3) / 1e9, "frac_hbm": bb / (b_ms * 1e-3) / 1e9 / hbm,
+            "tensor_tflops": bf_ / (b_ms * 1e-3) / 1e12, "frac_of_roofline": rb / (b_ms * 1e-3),
+            "l2": "working set 0.85 GB > L2"}
+        del PB, b_state, b_out
+
+    # end to end through the binding, host buffers: H2D inputs, prefill, D2H out + state
+    if not args.no_e2e:
+        H = {n: xp[n].pin_memory() for n in ("q", "k", "v", "g_log", "beta")}
+        h_out = torch.empty(p_out.shape, dtype=p_out.dtype).pin_memory()
+        h_state = torch.empty(p_state.shape, dtype=p_state.dtype).pin_memory()
+        bi = sum(t.numel() * t.element_size() for t in H.values())
+        bo = h_out.numel() * h_out.element_size() + h_state.numel() * h_state.element_size()
+
+        def e2e_step():
+            for n in H:
+                P[n].copy_(H[n], non_blocking=True)
+            _, st = gdn.gdn_prefill(P["q"], P["k"], P["v"], P["g_log"], P["beta"],
+                                    xp["scale"], out=p_out, stream=stream)
+            h_out.copy_(p_out, non_blocking=True)
+            h_state.copy_(st, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(ws)
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(K):
+            e2e_step()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = reduce_max([s0.elapsed_time(s1) / K], ws)[0]
+        result["e2e"] = {"value": ws * wp.tokens / (e_ms * 1e-3), "unit": "tokens/s",
+                         "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms": e_ms,
+                         "api": "gdn_prefill (Python binding over the C ABI), pinned host "
+                                "buffers"}
+
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(wp, xp, wd, xd)
+
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gdn(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

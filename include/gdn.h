@@ -1,0 +1,147 @@
+/*
+ * gdn.h -- C ABI of the gated delta-rule (GDN) linear-attention library for one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The library computes, per (batch, value head), the recurrence over a state S laid
+ * out [Dk, Dv] in fp32:
+ *     S_t = exp(g_t) (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = scale * S_t^T q_t
+ * with value head h reading key/query head h / (Hv / Hk).
+ *
+ * Sources (AWS Neuron NKI library API pages):
+ *   "GDN CTE Kernel API Reference"  -- the chunked prefill (gdn_prefill).
+ *   "GDN TKG Kernel API Reference"  -- the fused single-token decode step
+ *                                      (gdn_decode_step).
+ *
+ * Conventions for every call:
+ *   - Pointers marked "device" are CUDA device pointers; the caller owns all memory.
+ *     The library allocates nothing and frees nothing.
+ *   - Tensors are dense, row-major, with the listed shapes. Every pointer must be
+ *     non-NULL and 16-byte aligned unless stated otherwise.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy default
+ *     stream). A GDN_OK return means the work was validated and enqueued.
+ *   - Errors are returned, never thrown. On a non-GDN_OK status nothing was enqueued
+ *     and gdn_last_error() returns a message for the calling thread.
+ *   - Outputs must not overlap inputs, except where aliasing is stated.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gdn_status {
+    GDN_OK = 0,
+    GDN_EINVAL = 1,        /* invalid argument: shape, pointer or alignment           */
+    GDN_EUNSUPPORTED = 2,  /* valid per the pages but not built here                  */
+    GDN_ECUDA = 3,         /* a CUDA runtime/driver call or kernel launch failed       */
+    GDN_ETIMEOUT = 4       /* a kernel gave up a bounded wait (gdn_get_device_status) */
+} gdn_status;
+
+typedef enum gdn_dtype {
+    GDN_DTYPE_F32 = 0,
+    GDN_DTYPE_BF16 = 1
+} gdn_dtype;
+
+/* Largest head dimension: "GDN CTE Kernel API Reference", Notes (Dk, Dv <= 128). */
+#define GDN_MAX_HEAD_DIM 128
+
+/*
+ * gdn_prefill_workspace_bytes -- scratch (device memory) gdn_prefill needs for this
+ * shape. Returns 0 when no workspace is needed, or (size_t)-1 if the shape is invalid.
+ */
+size_t gdn_prefill_workspace_bytes(int B, int Hk, int Hv, int S, int Dk, int Dv,
+                                   gdn_dtype dtype);
+
+/*
+ * gdn_prefill -- chunked GDN prefill ("GDN CTE Kernel API Reference": description,
+ * parameters, returns and Notes).
+ *
+ *   q, k       device, [B, Hk, S, Dk], token-major, dtype `dtype` (which sets the
+ *              compute dtype of the products and of `out`). Rows must be
+ *              L2-normalised (precondition, not checked).
+ *   v          device, [B, Hv, S, Dv], dtype `dtype`.
+ *   g_log      device, [B, Hv, S] fp32, per-token log decay (<= 0, not checked).
+ *   beta       device, [B, Hv, S] fp32, update strength in (0, 1) (not checked).
+ *   scale      query scale, applied on the device (typically 1/sqrt(Dk)).
+ *   B, Hk, Hv, S, Dk, Dv
+ *              B >= 1, Hk >= 1, Hv % Hk == 0, S >= 0, 1 <= Dk, Dv <= 128.
+ *              S needs no particular multiple: a ragged last chunk is handled.
+ *   state      device, [B, Hv, Dk, Dv] fp32. If state_is_input != 0 its contents are
+ *              the initial state and it is overwritten IN PLACE with the final state;
+ *              if 0 the initial state is zero, nothing is read from it, and the final
+ *              state is written to it.
+ *   out        device, [B, Hv, S, Dv], dtype `dtype`, head-major, un-normalised.
+ *   workspace  device scratch of gdn_prefill_workspace_bytes(...) bytes (may be NULL
+ *              when that is 0). Its contents on entry do not matter.
+ *   stream     cudaStream_t to enqueue on.
+ *
+ * Errors: GDN_EINVAL for a bad shape, a NULL or misaligned pointer, or too little
+ * workspace; GDN_ECUDA if a launch fails.
+ */
+gdn_status gdn_prefill(const void* q, const void* k, const void* v,
+                       const float* g_log, const float* beta, float scale,
+                       gdn_dtype dtype, int B, int Hk, int Hv, int S, int Dk, int Dv,
+                       float* state, int state_is_input, void* out,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * gdn_decode_step -- one fused decode token ("GDN TKG Kernel API Reference":
+ * Background, parameters, returns, Notes and Dimensions).
+ *
+ *   q, k         device, [BH, K] bf16, RAW (not l2-normalised), already expanded to
+ *                the value heads; BH = batch * num_v_heads with heads cycling fastest
+ *                (bh = b * num_v_heads + h).
+ *   v, z         device, [BH, V] bf16 (z is the RMSNormGated gate input).
+ *   b, a         device, [BH] bf16: raw pre-sigmoid beta input and raw gate input.
+ *   A_log        device, [num_v_heads] fp32.
+ *   dt_bias      device, [num_v_heads] fp32.
+ *   norm_weight  device, [V] fp32 (RMSNormGated gamma).
+ *   state_in     device, [BH, K, V] fp32, incoming state.
+ *   state_out    device, [BH, K, V] fp32, updated state. May equal state_in (in place);
+ *                must not otherwise overlap it.
+ *   out          device, [BH, V] bf16, the RMSNormGated output.
+ *   1 <= K, V <= 128; BH % num_v_heads == 0. BH == 0 enqueues nothing.
+ *
+ * The step computes, per row: q^ = q/sqrt(|q|^2 + 1e-6), k^ likewise;
+ * beta = sigmoid(b); g = -exp(A_log[h]) * softplus(a + dt_bias[h]); alpha = exp(g);
+ * S' = alpha (I - beta k^ k^^T) S + beta k^ v^T; o = S'^T q^ / sqrt(K);
+ * out = bf16( o / sqrt(mean_V(o^2) + 1e-6) * norm_weight * z * sigmoid(z) ).
+ * exp(g) and the 1/sqrt(K) scale are applied inside (Notes). The two eps values and
+ * the norm-then-gate order are readings: the pages do not state them.
+ *
+ * Errors: GDN_EINVAL for a bad shape or a NULL/misaligned pointer; GDN_ECUDA if the
+ * launch fails.
+ */
+gdn_status gdn_decode_step(const void* q, const void* k, const void* v, const void* b,
+                           const void* a, const float* A_log, const float* dt_bias,
+                           const void* z, const float* norm_weight, const float* state_in,
+                           float* state_out, void* out, int BH, int num_v_heads, int K,
+                           int V, void* stream);
+
+/* Message describing the calling thread's last non-GDN_OK status ("" if none). The
+ * pointer stays valid until the thread's next call into the library. */
+const char* gdn_last_error(void);
+
+/*
+ * gdn_get_device_status -- synchronises `stream`, then reports and clears the
+ * device-side status word the kernels set when a bounded wait runs out.
+ * Returns GDN_OK, GDN_ETIMEOUT, or GDN_ECUDA if the synchronisation itself failed.
+ */
+gdn_status gdn_get_device_status(void* stream);
+
+/*
+ * gdn_launch_count -- number of CUDA kernels this library has enqueued in this
+ * process since it was loaded (diagnostics: lets a caller count the kernels of a
+ * timed region). Thread-safe.
+ */
+unsigned long long gdn_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

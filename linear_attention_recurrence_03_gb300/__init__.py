@@ -1,0 +1,26 @@
+"""Gated delta-rule (GDN) linear-attention recurrence for one NVIDIA GB300 (sm_103a).
+
+A C-ABI CUDA library (include/gdn.h, built into ``libgdn.so`` by ``build.py``) with a
+thin Python binding of the same names:
+
+* ``gdn_prefill``      -- chunked prefill ("GDN CTE Kernel API Reference").
+* ``gdn_decode_step``  -- fused single-token decode step ("GDN TKG Kernel API Reference").
+"""
+from .gdn import (  # noqa: F401
+    EXPORTS,
+    GDN_DTYPE_BF16,
+    GDN_DTYPE_F32,
+    GDN_ECUDA,
+    GDN_EINVAL,
+    GDN_ETIMEOUT,
+    GDN_EUNSUPPORTED,
+    GDN_OK,
+    GDNError,
+    gdn_decode_step,
+    gdn_get_device_status,
+    gdn_last_error,
+    gdn_launch_count,
+    gdn_prefill,
+    gdn_prefill_workspace_bytes,
+    load_library,
+)

@@ -1,0 +1,139 @@
+// gdn_api.cu -- the extern "C" entry points declared in include/gdn.h: argument
+// validation, kernel selection and error reporting. No arithmetic of the method lives
+// here; every step runs in the kernels.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdint>
+#include <string>
+
+#include "gdn.h"
+#include "internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+std::atomic<unsigned long long> g_launches{0};
+
+gdn_status fail(gdn_status st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Checks that p is non-NULL and 16-byte aligned (or NULL allowed when unused).
+bool ptr_ok(const void* p, bool required) {
+    if (p == nullptr) return !required;
+    return aligned16(p);
+}
+
+gdn_status check_prefill_shape(int B, int Hk, int Hv, int S, int Dk, int Dv, gdn_dtype dt) {
+    if (B < 1 || Hk < 1 || Hv < 1 || S < 0)
+        return fail(GDN_EINVAL, "gdn_prefill: need B >= 1, Hk >= 1, Hv >= 1, S >= 0 "
+                    "(got B=%d Hk=%d Hv=%d S=%d)", B, Hk, Hv, S);
+    if (Hv % Hk != 0)
+        return fail(GDN_EINVAL, "gdn_prefill: Hv (%d) must be a multiple of Hk (%d)", Hv, Hk);
+    if (Dk < 1 || Dk > gdn::kMaxHeadDim || Dv < 1 || Dv > gdn::kMaxHeadDim)
+        return fail(GDN_EINVAL, "gdn_prefill: need 1 <= Dk, Dv <= %d (got Dk=%d Dv=%d)",
+                    gdn::kMaxHeadDim, Dk, Dv);
+    if (dt != GDN_DTYPE_F32 && dt != GDN_DTYPE_BF16)
+        return fail(GDN_EINVAL, "gdn_prefill: unknown dtype %d", (int)dt);
+    return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t gdn_prefill_workspace_bytes(int B, int Hk, int Hv, int S, int Dk, int Dv,
+                                   gdn_dtype dtype) {
+    if (check_prefill_shape(B, Hk, Hv, S, Dk, Dv, dtype) != GDN_OK) return (size_t)-1;
+    return 0;
+}
+
+gdn_status gdn_prefill(const void* q, const void* k, const void* v, const float* g_log,
+                       const float* beta, float scale, gdn_dtype dtype, int B, int Hk, int Hv,
+                       int S, int Dk, int Dv, float* state, int state_is_input, void* out,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+    gdn_status st = check_prefill_shape(B, Hk, Hv, S, Dk, Dv, dtype);
+    if (st != GDN_OK) return st;
+    const bool tok = S > 0;  // per-token tensors may be NULL only when S == 0
+    if (!ptr_ok(q, tok) || !ptr_ok(k, tok) || !ptr_ok(v, tok) || !ptr_ok(g_log, tok) ||
+        !ptr_ok(beta, tok) || !ptr_ok(out, tok) || !ptr_ok(state, true))
+        return fail(GDN_EINVAL, "gdn_prefill: q, k, v, g_log, beta, out and state must be "
+                    "non-NULL, 16-byte aligned device pointers");
+    const size_t need = gdn_prefill_workspace_bytes(B, Hk, Hv, S, Dk, Dv, dtype);
+    if (workspace_bytes < need || (need > 0 && !ptr_ok(workspace, true)))
+        return fail(GDN_EINVAL, "gdn_prefill: workspace of %zu bytes needed, %zu given",
+                    need, workspace_bytes);
+
+    gdn::PrefillArgs a{q, k, v, g_log, beta, scale, B, Hk, Hv, S, Dk, Dv,
+                       state, state_is_input ? 1 : 0, out, workspace, workspace_bytes};
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int launched = 0;
+    const cudaError_t e = gdn::launch_prefill_simt(a, dtype == GDN_DTYPE_BF16, s, &launched);
+    g_launches += (unsigned long long)launched;
+    if (e != cudaSuccess)
+        return fail(GDN_ECUDA, "gdn_prefill: launch failed: %s", cudaGetErrorString(e));
+    return GDN_OK;
+}
+
+gdn_status gdn_decode_step(const void* q, const void* k, const void* v, const void* b,
+                           const void* a, const float* A_log, const float* dt_bias,
+                           const void* z, const float* norm_weight, const float* state_in,
+                           float* state_out, void* out, int BH, int num_v_heads, int K, int V,
+                           void* stream) {
+    if (BH < 0 || num_v_heads < 1 || BH % num_v_heads != 0)
+        return fail(GDN_EINVAL, "gdn_decode_step: need BH >= 0 and BH %% num_v_heads == 0 "
+                    "(got BH=%d num_v_heads=%d)", BH, num_v_heads);
+    if (K < 1 || K > gdn::kMaxHeadDim || V < 1 || V > gdn::kMaxHeadDim)
+        return fail(GDN_EINVAL, "gdn_decode_step: need 1 <= K, V <= %d (got K=%d V=%d)",
+                    gdn::kMaxHeadDim, K, V);
+    const bool rows = BH > 0;
+    if (!ptr_ok(q, rows) || !ptr_ok(k, rows) || !ptr_ok(v, rows) || !ptr_ok(b, rows) ||
+        !ptr_ok(a, rows) || !ptr_ok(z, rows) || !ptr_ok(state_in, rows) ||
+        !ptr_ok(state_out, rows) || !ptr_ok(out, rows) || !ptr_ok(A_log, true) ||
+        !ptr_ok(dt_bias, true) || !ptr_ok(norm_weight, true))
+        return fail(GDN_EINVAL, "gdn_decode_step: every pointer must be a non-NULL, "
+                    "16-byte aligned device pointer");
+    if (state_in != state_out && rows) {
+        const uintptr_t i0 = reinterpret_cast<uintptr_t>(state_in);
+        const uintptr_t o0 = reinterpret_cast<uintptr_t>(state_out);
+        const uintptr_t n = (uintptr_t)BH * K * V * sizeof(float);
+        if (i0 < o0 + n && o0 < i0 + n)
+            return fail(GDN_EINVAL, "gdn_decode_step: state_out overlaps state_in without "
+                        "being equal to it");
+    }
+    gdn::DecodeArgs d{static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
+                      static_cast<const __nv_bfloat16*>(v), static_cast<const __nv_bfloat16*>(b),
+                      static_cast<const __nv_bfloat16*>(a), A_log, dt_bias,
+                      static_cast<const __nv_bfloat16*>(z), norm_weight, state_in, state_out,
+                      static_cast<__nv_bfloat16*>(out), BH, num_v_heads, K, V};
+    const cudaError_t e = gdn::launch_decode(d, static_cast<cudaStream_t>(stream));
+    if (BH > 0) g_launches += 1;
+    if (e != cudaSuccess)
+        return fail(GDN_ECUDA, "gdn_decode_step: launch failed: %s", cudaGetErrorString(e));
+    return GDN_OK;
+}
+
+const char* gdn_last_error(void) { return g_last_error.c_str(); }
+
+unsigned long long gdn_launch_count(void) { return g_launches.load(); }
+
+gdn_status gdn_get_device_status(void* stream) {
+    const cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return fail(GDN_ECUDA, "gdn_get_device_status: %s", cudaGetErrorString(e));
+    const uint32_t bits = gdn::prefill_tc_take_status();
+    if (bits != 0)
+        return fail(GDN_ETIMEOUT, "a kernel gave up a bounded wait (status bits 0x%x)", bits);
+    return GDN_OK;
+}
+
+}  // extern "C"

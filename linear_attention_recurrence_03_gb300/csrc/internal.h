@@ -1,0 +1,64 @@
+// internal.h -- declarations shared by the library's translation units (not part of
+// the C ABI; see include/gdn.h for that).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace gdn {
+
+// Largest head dimension ("GDN CTE Kernel API Reference", Notes: Dk, Dv <= 128).
+constexpr int kMaxHeadDim = 128;
+
+// Unstated constants, read as the usual choices: l2norm eps and RMSNorm eps
+// ("GDN TKG Kernel API Reference" names both operations but no eps).
+constexpr float kEpsL2 = 1e-6f;
+constexpr float kEpsRms = 1e-6f;
+
+struct PrefillArgs {
+    const void* q;      // [B, Hk, S, Dk]
+    const void* k;      // [B, Hk, S, Dk]
+    const void* v;      // [B, Hv, S, Dv]
+    const float* g;     // [B, Hv, S]
+    const float* beta;  // [B, Hv, S]
+    float scale;
+    int B, Hk, Hv, S, Dk, Dv;
+    float* state;       // [B, Hv, Dk, Dv]
+    int state_is_input;
+    void* out;          // [B, Hv, S, Dv]
+    void* workspace;
+    size_t workspace_bytes;
+};
+
+struct DecodeArgs {
+    const __nv_bfloat16* q;   // [BH, K]
+    const __nv_bfloat16* k;   // [BH, K]
+    const __nv_bfloat16* v;   // [BH, V]
+    const __nv_bfloat16* b;   // [BH]
+    const __nv_bfloat16* a;   // [BH]
+    const float* A_log;       // [H]
+    const float* dt_bias;     // [H]
+    const __nv_bfloat16* z;   // [BH, V]
+    const float* norm_weight; // [V]
+    const float* state_in;    // [BH, K, V]
+    float* state_out;         // [BH, K, V]
+    __nv_bfloat16* out;       // [BH, V]
+    int BH, H, K, V;
+};
+
+// SIMT fp32 chunked prefill (any Dk, Dv <= 128; q/k/v fp32 or bf16). *launched
+// receives the number of kernels enqueued.
+cudaError_t launch_prefill_simt(const PrefillArgs& a, bool bf16, cudaStream_t stream,
+                                int* launched);
+
+// Fused decode step.
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+// Device status word of each translation unit that has bounded waits: returns the
+// bits set since the last call and clears them (the stream must be synchronised).
+uint32_t prefill_tc_take_status();
+
+}  // namespace gdn

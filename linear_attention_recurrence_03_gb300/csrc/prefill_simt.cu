@@ -1,0 +1,219 @@
+// prefill_simt.cu -- chunked GDN prefill on the CUDA cores, computed in fp32.
+//
+// "GDN CTE Kernel API Reference": the recurrence in chunk-parallel form with an
+// intra-chunk (I+A) inverse; the state is fp32 whatever the compute dtype (Notes).
+// This kernel is the fp32 compute-dtype path and serves shapes the tensor-core kernel
+// does not cover. All arithmetic is fp32 FFMA.
+//
+// Chunk algebra (derived from S_t = exp(g_t)(I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T,
+// o_t = scale S_t^T q_t), for a chunk of C tokens, local index r, starting state S0:
+//   gamma_r = sum_{i<=r} g_i,  Gamma_r = exp(gamma_r),  D[r,j] = exp(gamma_r - gamma_j)
+//   A[r,j]  = beta_r (k_r . k_j) D[r,j]   (j < r),    T = (I + A)^-1
+//   Y       = diag(beta) (V - diag(Gamma) K S0),       U = T Y
+//   P[r,j]  = (q_r . k_j) D[r,j]          (j <= r)
+//   O       = scale (diag(Gamma) Q S0 + P U)
+//   S1      = Gamma_{C-1} S0 + sum_j exp(gamma_{C-1} - gamma_j) k_j u_j^T
+// U = T Y is the same as U~ - W S0 with W = T diag(beta Gamma) K, U~ = T diag(beta) V.
+//
+// A ragged last chunk is padded with tokens that have g = 0 and beta = 0: such a token
+// leaves the state unchanged (alpha = 1, u = 0), so padding is exact.
+//
+// Grid: (ceil(Dv/32) value-column slices, Hv, B); the columns of S evolve
+// independently (left-multiplication by (I - beta k k^T) never mixes them), so each
+// CTA carries its own 32 columns of the state through the whole sequence in shared
+// memory.
+#include "internal.h"
+
+namespace gdn {
+namespace {
+
+constexpr int C = 64;      // chunk length
+constexpr int NS = 32;     // state columns per CTA
+constexpr int NT = 256;    // threads per CTA
+constexpr int DKP = 129;   // padded row stride (floats) of the q/k tiles
+constexpr int CP = C + 1;  // padded row stride of the C x C tiles
+constexpr int NSP = NS + 1;
+
+struct Smem {
+    float Q[C][DKP];
+    float K[C][DKP];
+    float Y[C][NSP];    // V slice, then Y = diag(beta)(V - diag(Gamma) K S0)
+    float KS[C][NSP];
+    float QS[C][NSP];
+    float U[C][NSP];
+    float S[kMaxHeadDim][NSP];
+    float A[C][CP];
+    float T[C][CP];
+    float P[C][CP];
+    float gam[C];
+    float beta[C];
+    float dec[C];       // exp(gamma_last - gamma_j)
+};
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ void store_as(float* p, float x) { *p = x; }
+__device__ __forceinline__ void store_as(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+
+template <typename Tin>
+__global__ void __launch_bounds__(NT) prefill_simt_kernel(PrefillArgs a) {
+    extern __shared__ float4 smem_raw[];
+    Smem& s = *reinterpret_cast<Smem*>(smem_raw);
+    const int tid = threadIdx.x;
+    const int n0 = blockIdx.x * NS, h = blockIdx.y, b = blockIdx.z;
+    const int Dk = a.Dk, Dv = a.Dv, S = a.S;
+    const int nw = min(NS, Dv - n0);
+    const int kh = h / (a.Hv / a.Hk);  // value head h reads key head h // (Hv/Hk)
+
+    const Tin* q = static_cast<const Tin*>(a.q) + ((size_t)b * a.Hk + kh) * (size_t)S * Dk;
+    const Tin* k = static_cast<const Tin*>(a.k) + ((size_t)b * a.Hk + kh) * (size_t)S * Dk;
+    const Tin* v = static_cast<const Tin*>(a.v) + ((size_t)b * a.Hv + h) * (size_t)S * Dv;
+    const float* g = a.g + ((size_t)b * a.Hv + h) * (size_t)S;
+    const float* be = a.beta + ((size_t)b * a.Hv + h) * (size_t)S;
+    Tin* out = static_cast<Tin*>(a.out) + ((size_t)b * a.Hv + h) * (size_t)S * Dv;
+    float* st = a.state + ((size_t)b * a.Hv + h) * (size_t)Dk * Dv;
+
+    // Initial state: the supplied one, else zero with no load.
+    for (int idx = tid; idx < kMaxHeadDim * NS; idx += NT) {
+        const int i = idx / NS, n = idx % NS;
+        s.S[i][n] = (a.state_is_input && i < Dk && n < nw) ? st[(size_t)i * Dv + n0 + n] : 0.f;
+    }
+
+    for (int c0 = 0; c0 < S; c0 += C) {
+        const int L = min(C, S - c0);
+        __syncthreads();
+        for (int idx = tid; idx < C * Dk; idx += NT) {
+            const int r = idx / Dk, i = idx % Dk;
+            const bool live = r < L;
+            s.Q[r][i] = live ? to_f32(q[(size_t)(c0 + r) * Dk + i]) : 0.f;
+            s.K[r][i] = live ? to_f32(k[(size_t)(c0 + r) * Dk + i]) : 0.f;
+        }
+        for (int idx = tid; idx < C * NS; idx += NT) {
+            const int r = idx / NS, n = idx % NS;
+            s.Y[r][n] = (r < L && n < nw) ? to_f32(v[(size_t)(c0 + r) * Dv + n0 + n]) : 0.f;
+        }
+        if (tid < C) {
+            s.gam[tid] = tid < L ? g[c0 + tid] : 0.f;
+            s.beta[tid] = tid < L ? be[c0 + tid] : 0.f;
+        }
+        __syncthreads();
+        // decay cumsum: two 32-wide warp scans joined by the first half's total
+        if (tid < C) {
+            float x = s.gam[tid];
+            const int lane = tid & 31;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, x, off);
+                if (lane >= off) x += y;
+            }
+            s.gam[tid] = x;
+        }
+        __syncthreads();
+        if (tid >= 32 && tid < C) s.gam[tid] += s.gam[31];
+        __syncthreads();
+        const float gl = s.gam[C - 1];
+        if (tid < C) s.dec[tid] = expf(gl - s.gam[tid]);
+
+        // A (strictly lower, beta and decay folded in) and P (lower incl. diagonal)
+        {
+            const int j = tid % C;
+            for (int r = tid / C; r < C; r += NT / C) {
+                float kk = 0.f, qk = 0.f;
+                if (j <= r) {
+                    for (int i = 0; i < Dk; ++i) {
+                        const float kj = s.K[j][i];
+                        kk = fmaf(s.K[r][i], kj, kk);
+                        qk = fmaf(s.Q[r][i], kj, qk);
+                    }
+                }
+                const float d = (j <= r) ? expf(s.gam[r] - s.gam[j]) : 0.f;
+                s.A[r][j] = (j < r) ? s.beta[r] * kk * d : 0.f;
+                s.P[r][j] = qk * d;
+            }
+        }
+        // K S0 and Q S0
+        for (int idx = tid; idx < C * NS; idx += NT) {
+            const int r = idx / NS, n = idx % NS;
+            float ks = 0.f, qs = 0.f;
+            for (int i = 0; i < Dk; ++i) {
+                const float sv = s.S[i][n];
+                ks = fmaf(s.K[r][i], sv, ks);
+                qs = fmaf(s.Q[r][i], sv, qs);
+            }
+            s.KS[r][n] = ks;
+            s.QS[r][n] = qs;
+        }
+        __syncthreads();
+        // T = (I + A)^-1, one column per thread, forward substitution
+        if (tid < C) {
+            const int j = tid;
+            for (int r = 0; r < j; ++r) s.T[r][j] = 0.f;
+            s.T[j][j] = 1.f;
+            for (int r = j + 1; r < C; ++r) {
+                float acc = 0.f;
+                for (int m = j; m < r; ++m) acc = fmaf(s.A[r][m], s.T[m][j], acc);
+                s.T[r][j] = -acc;
+            }
+        }
+        // Y = diag(beta) (V - diag(Gamma) K S0)
+        for (int idx = tid; idx < C * NS; idx += NT) {
+            const int r = idx / NS, n = idx % NS;
+            s.Y[r][n] = s.beta[r] * (s.Y[r][n] - expf(s.gam[r]) * s.KS[r][n]);
+        }
+        __syncthreads();
+        // U = T Y
+        for (int idx = tid; idx < C * NS; idx += NT) {
+            const int r = idx / NS, n = idx % NS;
+            float acc = 0.f;
+            for (int j = 0; j <= r; ++j) acc = fmaf(s.T[r][j], s.Y[j][n], acc);
+            s.U[r][n] = acc;
+        }
+        __syncthreads();
+        // O = scale (diag(Gamma) Q S0 + P U), written for live rows and columns
+        for (int idx = tid; idx < C * NS; idx += NT) {
+            const int r = idx / NS, n = idx % NS;
+            float pu = 0.f;
+            for (int j = 0; j <= r; ++j) pu = fmaf(s.P[r][j], s.U[j][n], pu);
+            const float o = a.scale * fmaf(expf(s.gam[r]), s.QS[r][n], pu);
+            if (r < L && n < nw) store_as(&out[(size_t)(c0 + r) * Dv + n0 + n], o);
+        }
+        // S1 = Gamma_last S0 + sum_j exp(gamma_last - gamma_j) k_j u_j^T
+        const float Gl = expf(gl);
+        for (int idx = tid; idx < Dk * NS; idx += NT) {
+            const int i = idx / NS, n = idx % NS;
+            float acc = Gl * s.S[i][n];
+            for (int j = 0; j < C; ++j) acc = fmaf(s.dec[j] * s.K[j][i], s.U[j][n], acc);
+            s.S[i][n] = acc;
+        }
+    }
+    __syncthreads();
+    for (int idx = tid; idx < Dk * NS; idx += NT) {
+        const int i = idx / NS, n = idx % NS;
+        if (n < nw) st[(size_t)i * Dv + n0 + n] = s.S[i][n];
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_simt(const PrefillArgs& a, bool bf16, cudaStream_t stream,
+                                int* launched) {
+    *launched = 0;
+    const dim3 grid((a.Dv + NS - 1) / NS, a.Hv, a.B);
+    const size_t smem = sizeof(Smem);
+    cudaError_t e;
+    if (bf16) {
+        e = cudaFuncSetAttribute(prefill_simt_kernel<__nv_bfloat16>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        prefill_simt_kernel<__nv_bfloat16><<<grid, NT, smem, stream>>>(a);
+    } else {
+        e = cudaFuncSetAttribute(prefill_simt_kernel<float>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        prefill_simt_kernel<float><<<grid, NT, smem, stream>>>(a);
+    }
+    *launched = 1;
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -1,0 +1,95 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports every
+function include/gdn.h declares, and rejects invalid arguments before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+import linear_attention_recurrence_03_gb300 as gdn
+from linear_attention_recurrence_03_gb300 import build as lib_build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    lib_build.build()
+    return gdn.load_library()
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "gdn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_binding_exports():
+    assert header_functions() == sorted(gdn.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+
+
+def test_library_is_built_for_sm_103a_only(lib):
+    flags = " ".join(lib_build.NVCC_FLAGS)
+    assert "arch=compute_103a,code=sm_103a" in flags
+    assert flags.count("-gencode") == 1
+
+
+def _prefill(lib, **kw):
+    args = dict(q=16, k=16, v=16, g=16, beta=16, scale=1.0, dtype=1, B=1, Hk=1, Hv=1, S=64,
+                Dk=128, Dv=128, state=16, sin=0, out=16, ws=None, wsb=0, stream=None)
+    args.update(kw)
+    vp = ctypes.c_void_p
+    return lib.gdn_prefill(vp(args["q"]), vp(args["k"]), vp(args["v"]), vp(args["g"]),
+                           vp(args["beta"]), args["scale"], args["dtype"], args["B"],
+                           args["Hk"], args["Hv"], args["S"], args["Dk"], args["Dv"],
+                           vp(args["state"]), args["sin"], vp(args["out"]), args["ws"],
+                           args["wsb"], args["stream"])
+
+
+@pytest.mark.parametrize("kw,msg", [
+    (dict(Hk=3, Hv=4), "multiple of Hk"),
+    (dict(Dk=129), "Dk, Dv"),
+    (dict(Dv=0), "Dk, Dv"),
+    (dict(B=0), "B >= 1"),
+    (dict(S=-1), "S >= 0"),
+    (dict(dtype=7), "dtype"),
+    (dict(q=None), "non-NULL"),
+    (dict(state=8), "16-byte"),
+])
+def test_prefill_rejects_bad_arguments(lib, kw, msg):
+    assert _prefill(lib, **kw) == gdn.GDN_EINVAL
+    assert msg in lib.gdn_last_error().decode()
+
+
+def test_workspace_query(lib):
+    assert lib.gdn_prefill_workspace_bytes(1, 3, 4, 64, 128, 128, 1) == ctypes.c_size_t(-1).value
+    n = lib.gdn_prefill_workspace_bytes(1, 16, 32, 8192, 128, 128, 1)
+    assert n != ctypes.c_size_t(-1).value
+
+
+@pytest.mark.parametrize("kw,msg", [
+    (dict(BH=10, H=4), "BH % num_v_heads"),
+    (dict(K=200), "K, V"),
+    (dict(out=None), "non-NULL"),
+    (dict(state_out=16 + 64), "overlaps"),
+])
+def test_decode_rejects_bad_arguments(lib, kw, msg):
+    a = dict(q=16, k=16, v=16, b=16, a=16, A_log=16, dt_bias=16, z=16, w=16, state_in=16,
+             state_out=1 << 40, out=16, BH=8, H=4, K=128, V=128)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    rc = lib.gdn_decode_step(*(vp(a[n]) for n in ("q", "k", "v", "b", "a", "A_log", "dt_bias",
+                                                  "z", "w", "state_in", "state_out", "out")),
+                             a["BH"], a["H"], a["K"], a["V"], None)
+    assert rc == gdn.GDN_EINVAL
+    assert msg in lib.gdn_last_error().decode()
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(RuntimeError, match="missing"):
+        gdn.load_library(str(tmp_path / "libgdn.so"))
