@@ -48,6 +48,8 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-batched", action="store_true",
                    help="skip the extra B=8, S=4096 prefill measurement")
+    p.add_argument("--spinup-seconds", type=float, default=1.0,
+                   help="untimed load before the warm-up, so clock samples see the GPU busy")
     return p.parse_args()
 
 
@@ -320,7 +322,7 @@ def run_gdn(args):
     clocks = ClockSampler(local)
     clocks.start()
     # spin-up (untimed) so that the clock samples see the GPU under this load
-    t_end = time.perf_counter() + 1.0
+    t_end = time.perf_counter() + args.spinup_seconds
     while time.perf_counter() < t_end:
         prefill()
         decode()
@@ -365,7 +367,7 @@ def run_gdn(args):
     bf16 = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
     t_bytes, t_flops = pb / (hbm * 1e9), pf / (bf16 * 1e12)
     bound = "hbm" if t_bytes >= t_flops else "tensor"
-    src_name = "prefill_simt.cu"
+    src_name = "prefill_tc.cu"
     sha = _kernel_source_sha(src_name)
     traffic = NCU_TRAFFIC.get(f"{src_name}@{sha}")
     roof = {"bound": bound, "achieved": p_gbs if bound == "hbm" else p_tfs,

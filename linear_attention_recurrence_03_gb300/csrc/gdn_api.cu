@@ -77,7 +77,10 @@ gdn_status gdn_prefill(const void* q, const void* k, const void* v, const float*
                        state, state_is_input ? 1 : 0, out, workspace, workspace_bytes};
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     int launched = 0;
-    const cudaError_t e = gdn::launch_prefill_simt(a, dtype == GDN_DTYPE_BF16, s, &launched);
+    const bool bf16 = dtype == GDN_DTYPE_BF16;
+    const cudaError_t e = gdn::prefill_tc_supported(a, bf16)
+                              ? gdn::launch_prefill_tc(a, s, &launched)
+                              : gdn::launch_prefill_simt(a, bf16, s, &launched);
     g_launches += (unsigned long long)launched;
     if (e != cudaSuccess)
         return fail(GDN_ECUDA, "gdn_prefill: launch failed: %s", cudaGetErrorString(e));

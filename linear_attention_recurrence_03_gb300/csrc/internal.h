@@ -54,6 +54,10 @@ struct DecodeArgs {
 cudaError_t launch_prefill_simt(const PrefillArgs& a, bool bf16, cudaStream_t stream,
                                 int* launched);
 
+// tcgen05 chunked prefill (bf16, Dk = Dv = 128, S > 0).
+bool prefill_tc_supported(const PrefillArgs& a, bool bf16);
+cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream, int* launched);
+
 // Fused decode step.
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 
