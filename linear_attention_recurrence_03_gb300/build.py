@@ -43,17 +43,24 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(d) <= t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False) -> str:
-    """Compile and link the library if any source is newer than it. Returns its path."""
-    if not force and up_to_date():
+def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False,
+          defines=(), lib_path: str | None = None) -> str:
+    """Compile and link the library if any source is newer than it. Returns its path.
+
+    ``defines`` (e.g. ``("GDN_TRACE",)``) and ``lib_path`` build a variant library
+    elsewhere (profiling aids); the default build has neither."""
+    out_lib = lib_path or LIB
+    if not force and not defines and lib_path is None and up_to_date():
         return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    build_dir = BUILD if not defines else BUILD + "_" + "_".join(d.lower() for d in defines)
+    os.makedirs(build_dir, exist_ok=True)
     srcs, _ = _inputs()
     nvcc = _nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_v else []
+    extra += [f"-D{d}" for d in defines]
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -64,13 +71,13 @@ def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False) -> 
 
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = out_lib + f".tmp{os.getpid()}"
     r = subprocess.run([nvcc, "-shared", "-gencode", "arch=compute_103a,code=sm_103a",
                         *objs, "-o", tmp], capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, out_lib)
+    return out_lib
 
 
 if __name__ == "__main__":
