@@ -303,11 +303,14 @@ def run_gdn(args):
     vp = ctypes.c_void_p
     sptr = vp(stream.cuda_stream)
     pargs = [vp(P[n].data_ptr()) for n in ("q", "k", "v", "g_log", "beta")]
+    p_wsb = gdn.gdn_prefill_workspace_bytes(wp.B, wp.Hk, wp.Hv, wp.S, wp.Dk, wp.Dv,
+                                            torch.bfloat16)
+    p_ws = torch.empty(max(p_wsb, 16), dtype=torch.uint8, device=dev)
 
     def prefill():
         rc = lib.gdn_prefill(*pargs, float(xp["scale"]), gdn.GDN_DTYPE_BF16, wp.B, wp.Hk, wp.Hv,
                              wp.S, wp.Dk, wp.Dv, vp(p_state.data_ptr()), 0,
-                             vp(p_out.data_ptr()), None, 0, sptr)
+                             vp(p_out.data_ptr()), vp(p_ws.data_ptr()), p_wsb, sptr)
         if rc != 0:
             raise RuntimeError(gdn.gdn_last_error())
 
@@ -408,11 +411,14 @@ def run_gdn(args):
         b_state = xb["state"].to(dev)
         b_out = torch.empty((wb.B, wb.Hv, wb.S, wb.Dv), dtype=torch.bfloat16, device=dev)
         bargs = [vp(PB[n].data_ptr()) for n in ("q", "k", "v", "g_log", "beta")]
+        b_wsb = gdn.gdn_prefill_workspace_bytes(wb.B, wb.Hk, wb.Hv, wb.S, wb.Dk, wb.Dv,
+                                                torch.bfloat16)
+        b_ws = torch.empty(max(b_wsb, 16), dtype=torch.uint8, device=dev)
 
         def prefill_b():
             rc = lib.gdn_prefill(*bargs, float(xb["scale"]), gdn.GDN_DTYPE_BF16, wb.B, wb.Hk,
                                  wb.Hv, wb.S, wb.Dk, wb.Dv, vp(b_state.data_ptr()), 1,
-                                 vp(b_out.data_ptr()), None, 0, sptr)
+                                 vp(b_out.data_ptr()), vp(b_ws.data_ptr()), b_wsb, sptr)
             if rc != 0:
                 raise RuntimeError(gdn.gdn_last_error())
 
@@ -448,7 +454,7 @@ def run_gdn(args):
             for n in H:
                 P[n].copy_(H[n], non_blocking=True)
             _, st = gdn.gdn_prefill(P["q"], P["k"], P["v"], P["g_log"], P["beta"],
-                                    xp["scale"], out=p_out, stream=stream)
+                                    xp["scale"], out=p_out, workspace=p_ws, stream=stream)
             h_out.copy_(p_out, non_blocking=True)
             h_state.copy_(st, non_blocking=True)
 

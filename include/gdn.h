@@ -52,6 +52,9 @@ typedef enum gdn_dtype {
 /*
  * gdn_prefill_workspace_bytes -- scratch (device memory) gdn_prefill needs for this
  * shape. Returns 0 when no workspace is needed, or (size_t)-1 if the shape is invalid.
+ * The bf16 path with Dk = Dv = 128 (the tensor-core kernels) needs 32768 bytes per
+ * (batch, value head, 64-token chunk): B * Hv * ceil(S / 64) * 32768; every other
+ * shape needs none.
  */
 size_t gdn_prefill_workspace_bytes(int B, int Hk, int Hv, int S, int Dk, int Dv,
                                    gdn_dtype dtype);
@@ -75,8 +78,10 @@ size_t gdn_prefill_workspace_bytes(int B, int Hk, int Hv, int S, int Dk, int Dv,
  *              if 0 the initial state is zero, nothing is read from it, and the final
  *              state is written to it.
  *   out        device, [B, Hv, S, Dv], dtype `dtype`, head-major, un-normalised.
- *   workspace  device scratch of gdn_prefill_workspace_bytes(...) bytes (may be NULL
- *              when that is 0). Its contents on entry do not matter.
+ *   workspace  device scratch of gdn_prefill_workspace_bytes(...) bytes, 16-byte
+ *              aligned (may be NULL when that is 0), owned by the caller and in use
+ *              until the enqueued work completes. Its contents on entry do not matter
+ *              and are unspecified on exit.
  *   stream     cudaStream_t to enqueue on.
  *
  * Errors: GDN_EINVAL for a bad shape, a NULL or misaligned pointer, or too little

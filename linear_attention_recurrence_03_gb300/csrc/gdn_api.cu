@@ -54,7 +54,11 @@ extern "C" {
 size_t gdn_prefill_workspace_bytes(int B, int Hk, int Hv, int S, int Dk, int Dv,
                                    gdn_dtype dtype) {
     if (check_prefill_shape(B, Hk, Hv, S, Dk, Dv, dtype) != GDN_OK) return (size_t)-1;
-    return 0;
+    gdn::PrefillArgs a{};
+    a.B = B, a.Hk = Hk, a.Hv = Hv, a.S = S, a.Dk = Dk, a.Dv = Dv;
+    return gdn::prefill_tc_supported(a, dtype == GDN_DTYPE_BF16)
+               ? gdn::prefill_tc_workspace_bytes(B, Hv, S)
+               : 0;
 }
 
 gdn_status gdn_prefill(const void* q, const void* k, const void* v, const float* g_log,

@@ -54,8 +54,11 @@ struct DecodeArgs {
 cudaError_t launch_prefill_simt(const PrefillArgs& a, bool bf16, cudaStream_t stream,
                                 int* launched);
 
-// tcgen05 chunked prefill (bf16, Dk = Dv = 128, S > 0).
+// tcgen05 chunked prefill (bf16, Dk = Dv = 128, S > 0): a parallel prep kernel writes
+// 32 KB of operand tiles per (batch, value head, 64-token chunk) to the workspace, then a
+// carry kernel runs the sequential part. *launched receives the kernels enqueued.
 bool prefill_tc_supported(const PrefillArgs& a, bool bf16);
+size_t prefill_tc_workspace_bytes(int B, int Hv, int S);
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream, int* launched);
 
 // Fused decode step.

@@ -1,5 +1,5 @@
-// prefill_tc.cu -- chunked GDN prefill on the tcgen05 tensor cores: bf16 operands,
-// fp32 accumulation in tensor memory (TMEM), fp32 state master in registers.
+// prefill_tc.cu -- chunked GDN prefill on the tcgen05 tensor cores: bf16 operands, fp32
+// accumulation in tensor memory (TMEM), fp32 state master in TMEM.
 //
 // "GDN CTE Kernel API Reference": the gated delta rule in chunk-parallel form with an
 // intra-chunk (I+A) inverse; q/k/v token-major, out head-major, state fp32 (Notes: the
@@ -18,24 +18,25 @@
 // exp(gamma_r - gamma_j), across blocks as exp(gamma_r - gamma_end) exp(gamma_end - gamma_j),
 // both factors <= 1.
 //
-// One CTA per (batch, value head, 64-column slice of the state); the state's columns
-// evolve independently, so slices never communicate. Per chunk, on the tensor cores:
-//   Gram   [Q;K] K^T               -> QK^T, KK^T          (M128 N64  K128)
-//   WY     [T_W;P] K, [T_U;T_W] V   -> W, U~               (M128 N128 K64, M128 N64 K64)
-//   carry  [W;Q] S0                 -> W S0, Q S0          (M128 N64  K128)
-//          [T_W;P] U                -> P U                 (M128 N64  K64)
-//          K^T U'                   -> state increment     (M128 N64  K64)
+// Two kernels. Everything that does not depend on S0 (the Gram matrices, the decay
+// masks, the (I+A)^-1 solve, T_U, P and W) is independent across chunks, so it runs
+// first as a fully parallel grid ("prep", one CTA per (batch, value head, chunk)) that
+// writes three bf16 operand tiles per chunk to a workspace, already in the 128-byte
+// swizzled layout the tensor cores read. The sequential part ("carry", one CTA per
+// (batch, value head, 64-column slice of the state); the slices never communicate)
+// then streams q, k, v and those tiles through a two-stage ring and keeps only the
+// S0-dependent chain per chunk:
+//   prep   [Q;K] K^T              -> QK^T, KK^T           (M128 N64  K128)
+//          [T_W;P] K              -> W                    (M128 N128 K64)
+//   carry  [T_U;P] V              -> U~                   (M128 N64  K64)
+//          [W;Q] S0               -> W S0, Q S0           (M128 N64  K128)
+//          [T_U;P] U              -> P U                  (M128 N64  K64)
+//          K^T U'                 -> state increment      (M128 N64  K64)
 // Stacking two 64-row operands into one 128-row operand fills the M = 128 data path;
 // the half of a result that is not needed is ignored.
 //
-// Warp roles (14 warps): 0 = TMA producer, which also computes the chunk's decay tables
-// from g and beta; 1 = MMA issuer (one thread, carry MMAs first); 2-5 = carry (fp32
-// state master, U, output, state update); 6-13 = prep (P and A from the Gram matrices,
-// the (I+A)^-1 solve, the WY operands). The prep of chunk c+1 overlaps the carry of
-// chunk c. The 16x16 block merges of the solve run on tf32 mma.sync.
-//
-// Every wait is bounded; on a timeout the kernel records a status bit, unwinds, waits
-// for its own copies and MMAs, frees TMEM and returns.
+// Every wait is bounded; on a timeout a kernel records a status bit, unwinds, waits for
+// its own copies and MMAs, frees TMEM and returns.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -60,7 +61,8 @@ uint32_t prefill_tc_take_status() {
 
 #ifdef GDN_TRACE
 // Profiling aid, compiled only with -DGDN_TRACE: per-chunk SM clock stamps of the
-// pipeline events of CTA (0,0,0), read back with gdn_trace_read().
+// pipeline events of carry CTA (0,0,0) and of the prep CTAs of head 0, batch 0, read
+// back with gdn_trace_read().
 constexpr int kTraceChunks = 64, kTraceEvents = 48;
 __device__ unsigned long long g_trace[kTraceChunks][kTraceEvents];
 #define TRACE(c, ev)                                                                    \
@@ -68,70 +70,106 @@ __device__ unsigned long long g_trace[kTraceChunks][kTraceEvents];
         if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (c) < kTraceChunks) \
             g_trace[(c)][(ev)] = clock64();                                             \
     } while (0)
+#define TRACE_PREP(ev)                                                        \
+    do {                                                                      \
+        if (blockIdx.y == 0 && blockIdx.z == 0 && blockIdx.x < kTraceChunks) \
+            g_trace[blockIdx.x][(ev)] = clock64();                            \
+    } while (0)
 #else
 #define TRACE(c, ev) \
     do {             \
+    } while (0)
+#define TRACE_PREP(ev) \
+    do {               \
     } while (0)
 #endif
 
 namespace {
 using namespace ptx;
 
-constexpr int C = 64;           // chunk length
-constexpr int NS = 64;          // state columns per CTA
-constexpr int NTHREADS = 448;   // 14 warps
+constexpr int C = 64;    // chunk length
+constexpr int NS = 64;   // state columns per carry CTA
 constexpr uint64_t kWaitNs = 2000000000ull;
 
-// ---- shared memory map (offsets from a 1024-byte aligned base) ----
-// stage s (two stages, one chunk each):
-//   block b (b = 0,1 covers Dk columns 64b..64b+63): W | Q | K, 8 KB each (SW128, 64 rows)
-//   V slice (64 tokens x 64 columns), T_U, T_W, P (64 x 64 each)
+// ---- workspace: per (batch, value head, chunk) unit, 32 KB of bf16 tiles, each 64 rows
+// x 64 columns in the 128-byte swizzled layout: T_U | P | W[:, 0:64] | W[:, 64:128]
+constexpr uint32_t WS_UNIT = 32768;
+constexpr uint32_t WS_TU = 0, WS_P = 8192, WS_W = 16384;
+
+// ---- prep kernel: shared memory map (offsets from a 1024-byte aligned base)
+//   block b (Dk columns 64b..64b+63): Q_b | K_b (8 KB each), stride 16 KB
+//   T_U, T_W, P (adjacent: [T_W; P] is one 128-row operand), W staging (two 8 KB blocks)
+//   fp32 blocks of A and T, scalars, barriers
+constexpr int PREP_THREADS = 288;  // warp 0: producer + MMA issuer; warps 1..8: prep
+constexpr uint32_t PQ_STRIDE = 16384;
+constexpr uint32_t PQ_Q = 0, PQ_K = 8192;
+constexpr uint32_t P_TU = 32768, P_TW = 40960, P_P = 49152, P_W = 57344;
+static_assert(P_P == P_TW + 8192 && P_W == P_P + 8192, "[T_W; P] one operand, P | W contiguous");
+constexpr int BS = 20;  // row stride (floats) of a 16x16 fp32 block
+constexpr uint32_t BLOCK_BYTES = 16 * BS * 4;
+constexpr uint32_t P_AB = 73728;                    // 10 lower blocks of A
+constexpr uint32_t P_TB = P_AB + 10 * BLOCK_BYTES;  // 10 lower blocks of T
+constexpr uint32_t P_SCAL = P_TB + 10 * BLOCK_BYTES;
+
+struct PrepScalars {
+    float gam[C];     // gamma_r
+    float beta[C];    // beta_r
+    float ctab[C];    // exp(gamma_{end of r's 16-block} - gamma_r)
+    float Gam[C];     // exp(gamma_r)
+    float endgam[4];  // gamma at the end of each 16-block
+};
+constexpr uint32_t P_BAR = P_SCAL + sizeof(PrepScalars);
+constexpr uint32_t P_MISC = P_BAR + 64;
+constexpr uint32_t PREP_SMEM = P_MISC + 64 + 1024;  // + alignment slack
+static_assert(P_BAR % 8 == 0, "barrier alignment");
+static_assert(2 * (PREP_SMEM + 1024) <= 233472, "two prep CTAs per SM");
+
+// prep TMEM columns (fp32, 128 lanes)
+constexpr uint32_t PT_G = 0;    // Gram [QK^T; KK^T], 64 columns
+constexpr uint32_t PT_W = 128;  // [W; -], 128 columns
+constexpr uint32_t PT_COLS = 256;
+
+enum { PB_FULL = 0, PB_GRAM, PB_PREP, PB_WDONE, PB_DRAIN, PB_COUNT };
+
+// ---- carry kernel: shared memory map
+//   stage s (two stages, one chunk each):
+//     block b: W_b | Q_b | K_b (8 KB each, stride 24 KB)  ([W_b; Q_b] is one operand)
+//     V slice (64 tokens x 64 columns), T_U, P            ([T_U; P] is one operand)
+//   U, U' tiles, the bf16 state operand, per-stage scalars, barriers
+constexpr int CARRY_THREADS = 192;  // warp 0: producer; warp 1: U~ issuer; 2..5: carry
 constexpr uint32_t BLK_STRIDE = 24576;
 constexpr uint32_t OFF_W = 0, OFF_Q = 8192, OFF_K = 16384;
-constexpr uint32_t OFF_V = 49152;
-constexpr uint32_t OFF_TU = 57344, OFF_TW = 65536, OFF_P = 73728;
-constexpr uint32_t STAGE_BYTES = 81920;
-constexpr uint32_t OFF_U = 2 * STAGE_BYTES;   // U tile  (64 tokens x 64 columns)
-constexpr uint32_t OFF_U2 = OFF_U + 8192;     // U' tile (decayed U)
-constexpr uint32_t OFF_S = OFF_U2 + 8192;     // bf16 state operand (128 x 64)
-constexpr uint32_t OFF_F32 = OFF_S + 16384;   // prep fp32 work area
-constexpr int BS = 20;                        // row stride (floats) of a 16x16 block
-constexpr uint32_t BLOCK_BYTES = 16 * BS * 4;
-constexpr uint32_t OFF_AB = OFF_F32;                      // 10 lower blocks of A
-constexpr uint32_t OFF_TB = OFF_AB + 10 * BLOCK_BYTES;    // 10 lower blocks of T
-constexpr uint32_t OFF_XB = OFF_TB + 10 * BLOCK_BYTES;    // 16x8 scratch per prep warp
-constexpr uint32_t OFF_SCAL = OFF_XB + 8 * 16 * 8 * 4;
+constexpr uint32_t OFF_V = 49152, OFF_TU = 57344, OFF_P = 65536;
+constexpr uint32_t STAGE_BYTES = 73728;
+static_assert(OFF_P == OFF_TU + 8192, "[T_U; P] is one 128-row operand");
+constexpr uint32_t OFF_U = 2 * STAGE_BYTES;  // U tile  (64 tokens x 64 columns)
+constexpr uint32_t OFF_U2 = OFF_U + 8192;    // U' tile (decayed U)
+constexpr uint32_t OFF_S = OFF_U2 + 8192;    // bf16 state operand (128 x 64)
+constexpr uint32_t OFF_SCAL = OFF_S + 16384;
 
-struct StageScalars {
-    float gam[C];    // gamma_r
-    float beta[C];   // beta_r
-    float ctab[C];   // exp(gamma_{end of r's 16-block} - gamma_r)
-    float Gam[C];    // exp(gamma_r)
-    float kdec[C];   // exp(gamma_last - gamma_r)
-    float endgam[4]; // gamma at the end of each 16-block
-    float Gl;        // exp(gamma_last)
+struct CarryScalars {
+    float Gam[C];   // exp(gamma_r)
+    float kdec[C];  // exp(gamma_last - gamma_r)
+    float Gl;       // exp(gamma_last)
     float pad[3];
 };
-constexpr uint32_t OFF_BAR = OFF_SCAL + 2 * sizeof(StageScalars);
+constexpr uint32_t OFF_BAR = OFF_SCAL + 2 * sizeof(CarryScalars);
 constexpr uint32_t OFF_MISC = OFF_BAR + 128;
-constexpr uint32_t SMEM_USED = OFF_MISC + 64;
-constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // alignment slack
+constexpr uint32_t CARRY_SMEM = OFF_MISC + 64 + 1024;
 static_assert(OFF_BAR % 8 == 0, "barrier alignment");
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(CARRY_SMEM <= 232448, "shared memory budget");
 
-// TMEM columns (fp32, 128 lanes)
-constexpr uint32_t TM_G = 0;     // Gram [QK^T; KK^T], 64 columns
-constexpr uint32_t TM_W = 64;    // [W; -], 128 columns
-constexpr uint32_t TM_U = 192;   // [U~; -], 64 columns
-constexpr uint32_t TM_A = 256;   // [W S0; Q S0], 64 columns
-constexpr uint32_t TM_S = 320;   // state increment, 64 columns
-constexpr uint32_t TM_B = 384;   // [-; P U], 64 columns
+// carry TMEM columns
+constexpr uint32_t TM_U = 0;     // [U~; -], 64 columns
+constexpr uint32_t TM_A = 64;    // [W S0; Q S0], 64 columns
+constexpr uint32_t TM_S = 128;   // state increment, 64 columns
+constexpr uint32_t TM_B = 192;   // [-; P U], 64 columns
+constexpr uint32_t TM_SS = 256;  // the fp32 state slice (row = Dk index), 64 columns
 constexpr uint32_t TM_COLS = 512;
 
-// barrier indices
 enum {
-    B_FULL0 = 0, B_FULL1, B_EMPTY0, B_EMPTY1, B_GRAM, B_GFREE, B_PREP, B_WDONE,
-    B_ADONE, B_CDONE, B_DRAIN, B_COUNT
+    B_FULL0 = 0, B_FULL1, B_EMPTY0, B_EMPTY1, B_UDONE, B_UFREE, B_ADONE, B_CDONE,
+    B_DRAIN_U, B_DRAIN_C, B_COUNT
 };
 
 // status bits
@@ -145,7 +183,12 @@ struct TcArgs {
     float* state;
     int state_is_input;
     __nv_bfloat16* out;
+    uint8_t* ws;
 };
+
+__device__ __forceinline__ size_t ws_offset(int b, int h, int c, int Hv, int nch) {
+    return ((size_t)(b * Hv + h) * (size_t)nch + (size_t)c) * WS_UNIT;
+}
 
 __device__ __forceinline__ void bar_sync(uint32_t id, uint32_t n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
@@ -226,6 +269,22 @@ __device__ __forceinline__ void record_failure(volatile int* abort_flag, uint32_
     *abort_flag = 1;
 }
 
+// Waits for the phase with the given parity, suspending between polls; gives up when
+// another role has set the abort flag, or after kWaitNs (then records `bit`).
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
+                                              volatile int* abort_flag, uint32_t bit) {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait_sleep(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > kWaitNs) {
+            record_failure(abort_flag, bit);
+            return false;
+        }
+    }
+}
+
 // Lower-triangular 16x16 block index of block (i, j), i >= j.
 __host__ __device__ constexpr int bidx(int i, int j) { return i * (i + 1) / 2 + j; }
 
@@ -265,30 +324,40 @@ __device__ __forceinline__ void block_mma(float (&d)[4], const float* Ablk, cons
     }
 }
 
-// Finishes T(i,j)[:, 8 nt ..] = -T(i,i) X for X held in x (C fragment): stores the fp32
-// block and the bf16 T_U / T_W entries (columns scaled by beta_j and beta_j Gamma_j).
-__device__ __forceinline__ void block_finish(const float (&x)[4], const float* Tii, float* Tout,
-                                             float* xw, int i, int j, int nt, int g, int t,
-                                             const float* beta, const float* Gam, uint32_t tu,
-                                             uint32_t tw) {
-    xw[g * 8 + 2 * t] = x[0];
-    xw[g * 8 + 2 * t + 1] = x[1];
-    xw[(g + 8) * 8 + 2 * t] = x[2];
-    xw[(g + 8) * 8 + 2 * t + 1] = x[3];
-    __syncwarp();
-    float e[4] = {0.f, 0.f, 0.f, 0.f};
+// C fragment of X (16x8) -> tf32 B fragments of X for the two k-steps of a 16-deep
+// product, through warp shuffles: b[ks] = {X[8 ks + t][g], X[8 ks + t + 4][g]}.
+__device__ __forceinline__ void c_to_b(const float (&x)[4], int g, int t, uint32_t (&b)[2][2]) {
+    const int s0 = 4 * t + (g >> 1), s1 = s0 + 16;
+    const float a0 = __shfl_sync(0xffffffffu, x[0], s0), a1 = __shfl_sync(0xffffffffu, x[1], s0);
+    const float a2 = __shfl_sync(0xffffffffu, x[2], s0), a3 = __shfl_sync(0xffffffffu, x[3], s0);
+    const float d0 = __shfl_sync(0xffffffffu, x[0], s1), d1 = __shfl_sync(0xffffffffu, x[1], s1);
+    const float d2 = __shfl_sync(0xffffffffu, x[2], s1), d3 = __shfl_sync(0xffffffffu, x[3], s1);
+    const bool odd = (g & 1) != 0;
+    b[0][0] = to_tf32(odd ? a1 : a0);
+    b[0][1] = to_tf32(odd ? d1 : d0);
+    b[1][0] = to_tf32(odd ? a3 : a2);
+    b[1][1] = to_tf32(odd ? d3 : d2);
+}
+
+// e += Tblk (16x16 fp32 block) * X, with X given as B fragments
+__device__ __forceinline__ void block_mma_b(float (&e)[4], const float* Tblk,
+                                            const uint32_t (&b)[2][2], int g, int t) {
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {
-        uint32_t a[4], b[2];
-        a[0] = to_tf32(Tii[g * BS + ks * 8 + t]);
-        a[1] = to_tf32(Tii[(g + 8) * BS + ks * 8 + t]);
-        a[2] = to_tf32(Tii[g * BS + ks * 8 + t + 4]);
-        a[3] = to_tf32(Tii[(g + 8) * BS + ks * 8 + t + 4]);
-        b[0] = to_tf32(xw[(ks * 8 + t) * 8 + g]);
-        b[1] = to_tf32(xw[(ks * 8 + t + 4) * 8 + g]);
-        mma_tf32(e, a, b);
+        uint32_t a[4];
+        a[0] = to_tf32(Tblk[g * BS + ks * 8 + t]);
+        a[1] = to_tf32(Tblk[(g + 8) * BS + ks * 8 + t]);
+        a[2] = to_tf32(Tblk[g * BS + ks * 8 + t + 4]);
+        a[3] = to_tf32(Tblk[(g + 8) * BS + ks * 8 + t + 4]);
+        mma_tf32(e, a, b[ks]);
     }
-    __syncwarp();
+}
+
+// Stores T(i,j)[:, 8 nt .. 8 nt + 7] = -e (C fragment): the fp32 block and the bf16
+// T_U / T_W entries (columns scaled by beta_j and beta_j Gamma_j).
+__device__ __forceinline__ void block_store(const float (&e)[4], float* Tout, int i, int j, int nt,
+                                            int g, int t, const float* beta, const float* Gam,
+                                            uint32_t tu, uint32_t tw) {
     const int c0 = nt * 8 + 2 * t;  // column inside the block
     Tout[g * BS + c0] = -e[0];
     Tout[g * BS + c0 + 1] = -e[1];
@@ -309,31 +378,37 @@ __device__ __forceinline__ void block_finish(const float (&x)[4], const float* T
 // to the start-address field (offsets stay inside the 14-bit field).
 __device__ __forceinline__ uint64_t dadd(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
 
-__device__ __forceinline__ void issue_gram(uint32_t tmem, uint32_t st) {
+// prep: [QK^T; KK^T] = [Q; K] K^T over Dk = 128 (two 64-column blocks)
+__device__ __forceinline__ void issue_gram(uint32_t tmem, uint32_t sb) {
     constexpr uint32_t id = idesc_bf16(128, 64, false, false);
-    const uint64_t a0 = smem_desc_sw128(st + OFF_Q, 16, 1024);
-    const uint64_t b0 = smem_desc_sw128(st + OFF_K, 16, 1024);
+    const uint64_t a0 = smem_desc_sw128(sb + PQ_Q, 16, 1024);
+    const uint64_t b0 = smem_desc_sw128(sb + PQ_K, 16, 1024);
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-        const uint32_t off = (uint32_t)(k >> 2) * BLK_STRIDE + (uint32_t)(k & 3) * 32u;
-        mma_bf16(tmem + TM_G, dadd(a0, off), dadd(b0, off), id, k > 0);
+        const uint32_t off = (uint32_t)(k >> 2) * PQ_STRIDE + (uint32_t)(k & 3) * 32u;
+        mma_bf16(tmem + PT_G, dadd(a0, off), dadd(b0, off), id, k > 0);
     }
 }
 
-__device__ __forceinline__ void issue_wy(uint32_t tmem, uint32_t st) {
-    constexpr uint32_t idw = idesc_bf16(128, 128, false, true);
-    const uint64_t aw = smem_desc_sw128(st + OFF_TW, 16, 1024);
-    const uint64_t bk = smem_desc_sw128(st + OFF_K, BLK_STRIDE, 1024);
+// prep: [W; P K] = [T_W; P] K over the 64 tokens (K read N-major: Dk contiguous)
+__device__ __forceinline__ void issue_w(uint32_t tmem, uint32_t sb) {
+    constexpr uint32_t id = idesc_bf16(128, 128, false, true);
+    const uint64_t aw = smem_desc_sw128(sb + P_TW, 16, 1024);
+    const uint64_t bk = smem_desc_sw128(sb + PQ_K, PQ_STRIDE, 1024);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) mma_bf16(tmem + TM_W, dadd(aw, k * 32), dadd(bk, k * 2048), idw, k > 0);
-    constexpr uint32_t idu = idesc_bf16(128, 64, false, true);
-    const uint64_t au = smem_desc_sw128(st + OFF_TU, 16, 1024);
-    const uint64_t bv = smem_desc_sw128(st + OFF_V, 8192, 1024);
-    const uint32_t du = tmem + TM_U;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) mma_bf16(du, dadd(au, k * 32), dadd(bv, k * 2048), idu, k > 0);
+    for (int k = 0; k < 4; ++k) mma_bf16(tmem + PT_W, dadd(aw, k * 32), dadd(bk, k * 2048), id, k > 0);
 }
 
+// carry: [U~; P V] = [T_U; P] V over the 64 tokens
+__device__ __forceinline__ void issue_u(uint32_t tmem, uint32_t st) {
+    constexpr uint32_t id = idesc_bf16(128, 64, false, true);
+    const uint64_t au = smem_desc_sw128(st + OFF_TU, 16, 1024);
+    const uint64_t bv = smem_desc_sw128(st + OFF_V, 8192, 1024);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) mma_bf16(tmem + TM_U, dadd(au, k * 32), dadd(bv, k * 2048), id, k > 0);
+}
+
+// carry: [W S0; Q S0] = [W; Q] S0 over Dk = 128
 __device__ __forceinline__ void issue_carry1(uint32_t tmem, uint32_t st, uint32_t s_tile) {
     constexpr uint32_t id = idesc_bf16(128, 64, false, true);
     const uint64_t a0 = smem_desc_sw128(st + OFF_W, 16, 1024);
@@ -345,13 +420,14 @@ __device__ __forceinline__ void issue_carry1(uint32_t tmem, uint32_t st, uint32_
     }
 }
 
+// carry: [T_U U; P U] = [T_U; P] U over the tokens, and K^T U' (K read M-major)
 __device__ __forceinline__ void issue_carry23(uint32_t tmem, uint32_t st, uint32_t u_tile,
                                               uint32_t u2_tile) {
     constexpr uint32_t id2 = idesc_bf16(128, 64, false, true);
-    const uint64_t aw = smem_desc_sw128(st + OFF_TW, 16, 1024);
+    const uint64_t ap = smem_desc_sw128(st + OFF_TU, 16, 1024);
     const uint64_t bu = smem_desc_sw128(u_tile, 8192, 1024);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) mma_bf16(tmem + TM_B, dadd(aw, k * 32), dadd(bu, k * 2048), id2, k > 0);
+    for (int k = 0; k < 4; ++k) mma_bf16(tmem + TM_B, dadd(ap, k * 32), dadd(bu, k * 2048), id2, k > 0);
     constexpr uint32_t id3 = idesc_bf16(128, 64, true, true);
     const uint64_t ak = smem_desc_sw128(st + OFF_K, BLK_STRIDE, 1024);
     const uint64_t bu2 = smem_desc_sw128(u2_tile, 8192, 1024);
@@ -360,37 +436,324 @@ __device__ __forceinline__ void issue_carry23(uint32_t tmem, uint32_t st, uint32
         mma_bf16(tmem + TM_S, dadd(ak, k * 2048), dadd(bu2, k * 2048), id3, k > 0);
 }
 
-// ---------------------------------------------------------------- the kernel
+// ---------------------------------------------------------------- the prep kernel
 
-__global__ void __launch_bounds__(NTHREADS, 1)
-    prefill_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
-                      const __grid_constant__ CUtensorMap mv, TcArgs a) {
+// One CTA per (chunk c, value head h, batch b). Warp 0 loads Q and K of the chunk (TMA),
+// builds the decay tables from g and beta, and issues the two MMAs; warps 1..8 turn the
+// Gram matrices into P and A, solve (I+A)^-1 in 16x16 blocks, write T_U, T_W and P as
+// bf16 tiles, read W back from TMEM, and store T_U | P | W to the workspace.
+__global__ void __launch_bounds__(PREP_THREADS, 2)
+    prep_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                   TcArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte alignment by a byte offset from the shared array itself, so every
-    // pointer derived from `sm` stays a shared-memory pointer (an integer round trip
-    // would turn the accesses into generic loads and stores).
+    // pointer derived from `sm` stays a shared-memory pointer.
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    const uint32_t sbase = smem_u32(sm);
-    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
-    uint32_t* misc = reinterpret_cast<uint32_t*>(sm + OFF_MISC);
+    const uint32_t sb = smem_u32(sm);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + P_BAR);
+    uint32_t* misc = reinterpret_cast<uint32_t*>(sm + P_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
-    uint32_t* u_ctr = misc + 2;  // chunks whose U~ the carry has consumed
-    StageScalars* scal = reinterpret_cast<StageScalars*>(sm + OFF_SCAL);
-    float* Ab = reinterpret_cast<float*>(sm + OFF_AB);
-    float* Tb = reinterpret_cast<float*>(sm + OFF_TB);
-    float* Xb = reinterpret_cast<float*>(sm + OFF_XB);
+    PrepScalars& sc = *reinterpret_cast<PrepScalars*>(sm + P_SCAL);
+    float* Ab = reinterpret_cast<float*>(sm + P_AB);
+    float* Tb = reinterpret_cast<float*>(sm + P_TB);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int n0 = blockIdx.x * NS, h = blockIdx.y, b = blockIdx.z;
+    const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int kh = h / (a.Hv / a.Hk);  // value head h reads key head h // (Hv/Hk)
     const int S = a.S;
     const int nch = (S + C - 1) / C;
 
     if (tid == 0) {
-        for (int i = 0; i < B_COUNT + 1; ++i)
+        for (int i = 0; i < PB_COUNT; ++i) mbar_init(&bar[i], i == PB_FULL ? 2 : 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(misc, PT_COLS);
+        tmem_relinquish();
+    }
+    // T_U / T_W blocks above the diagonal are never written: zero both tiles
+    for (int i = tid; i < 2 * 8192 / 16; i += PREP_THREADS)
+        st_shared_v4(sb + P_TU + 16 * i, 0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+
+    if (warp == 0) {
+        // -------------------------------------------- loads, decay tables, MMA issue
+        const int zq = b * a.Hk + kh, zv = b * a.Hv + h;
+        if (lane == 0) {
+            prefetch_tensormap(&mq);
+            prefetch_tensormap(&mk);
+            mbar_arrive_expect_tx(&bar[PB_FULL], 2 * 16384);
+            for (int blk = 0; blk < 2; ++blk) {
+                tma_load_3d(sm + blk * PQ_STRIDE + PQ_Q, &mq, &bar[PB_FULL], blk * 64, c * C, zq);
+                tma_load_3d(sm + blk * PQ_STRIDE + PQ_K, &mk, &bar[PB_FULL], blk * 64, c * C, zq);
+            }
+            TRACE_PREP(20);
+        }
+        // decay tables (padding tokens: g = beta = 0, an exact no-op)
+        const float* gp = a.g + (size_t)zv * S;
+        const float* bp = a.beta + (size_t)zv * S;
+        const int t0 = c * C + lane, t1 = t0 + 32;
+        float x0 = (t0 < S) ? gp[t0] : 0.f, x1 = (t1 < S) ? gp[t1] : 0.f;
+        const float be0 = (t0 < S) ? bp[t0] : 0.f, be1 = (t1 < S) ? bp[t1] : 0.f;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float y0 = __shfl_up_sync(0xffffffffu, x0, off);
+            const float y1 = __shfl_up_sync(0xffffffffu, x1, off);
+            if (lane >= off) {
+                x0 += y0;
+                x1 += y1;
+            }
+        }
+        x1 += __shfl_sync(0xffffffffu, x0, 31);
+        const float e0 = __shfl_sync(0xffffffffu, x0, lane | 15);
+        const float e1 = __shfl_sync(0xffffffffu, x1, lane | 15);
+        sc.gam[lane] = x0;
+        sc.gam[lane + 32] = x1;
+        sc.beta[lane] = be0;
+        sc.beta[lane + 32] = be1;
+        sc.ctab[lane] = __expf(e0 - x0);
+        sc.ctab[lane + 32] = __expf(e1 - x1);
+        sc.Gam[lane] = __expf(x0);
+        sc.Gam[lane + 32] = __expf(x1);
+        if (lane == 15) {
+            sc.endgam[0] = x0;
+            sc.endgam[2] = x1;
+        }
+        if (lane == 31) {
+            sc.endgam[1] = x0;
+            sc.endgam[3] = x1;
+        }
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(&bar[PB_FULL]);  // the tables are written
+            int issued = 0;
+            if (wait_or_abort(&bar[PB_FULL], 0, abort_flag, ST_PREP)) {
+                tc_fence_after();
+                issue_gram(tmem, sb);
+                tc_commit(&bar[PB_GRAM]);
+                issued = 1;
+                TRACE_PREP(21);
+                if (wait_or_abort(&bar[PB_PREP], 0, abort_flag, ST_PREP)) {
+                    tc_fence_after();
+                    issue_w(tmem, sb);
+                    tc_commit(&bar[PB_WDONE]);
+                    TRACE_PREP(22);
+                }
+            } else {
+                // the copies must land before the CTA exits
+                mbar_wait_bounded(&bar[PB_FULL], 0, kWaitNs);
+            }
+            if (issued) {
+                // no MMA may be in flight when TMEM is freed
+                tc_commit(&bar[PB_DRAIN]);
+                mbar_wait_bounded(&bar[PB_DRAIN], 0, kWaitNs);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ prep (256 threads)
+        const int P = tid - 32;
+        const int pw = P >> 5;  // prep warp 0..7
+        const int wg = P >> 7;  // which 8 columns of each 16-block of the Gram matrices
+        const int q = warp & 3;
+        const int L = 32 * q + lane;
+        const int g8 = lane >> 2, t4 = lane & 3;
+        const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+        const uint32_t tu = sb + P_TU, tw = sb + P_TW;
+
+        bool ok = wait_or_abort(&bar[PB_FULL], 0, abort_flag, ST_PREP) &&
+                  wait_or_abort(&bar[PB_GRAM], 0, abort_flag, ST_PREP);
+        if (!bar_any(2, 256, !ok || *abort_flag)) {
+            tc_fence_after();
+            if (P == 0) TRACE_PREP(23);
+
+            // ---- P (bf16 tile) and A (fp32 blocks) from the Gram matrices: thread (wg, L)
+            // takes row L of [QK^T; KK^T], columns 16 bj + 8 wg .. + 7 of every 16-block bj
+            {
+                const int r = L & 63, br = r >> 4, rl = r & 15;
+                const bool isP = L < 64;
+                const float gr = sc.gam[r];
+                const float scl = isP ? 1.f : sc.beta[r];
+                const int lim = isP ? rl : rl - 1;
+                float gv[32];
+                tmem_ld8x4(tmem + lane_off + PT_G + 8 * wg, gv);
+#pragma unroll
+                for (int bj = 0; bj < 4; ++bj) {
+                    float* v = gv + 8 * bj;
+                    if (bj < br) {
+                        const float f = __expf(gr - sc.endgam[bj]) * scl;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) v[e] *= f * sc.ctab[16 * bj + 8 * wg + e];
+                    } else if (bj == br) {
+                        // branch-free: exp of a non-positive argument, then the mask
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int jj = 8 * wg + e;
+                            const float ex = __expf(fminf(gr - sc.gam[16 * bj + jj], 0.f));
+                            v[e] *= ex * ((jj <= lim) ? scl : 0.f);
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) v[e] = 0.f;
+                    }
+                    if (isP) {
+                        st_shared_v4(sw128_chunk(sb + P_P, r, 2 * bj + wg), pack_bf16(v[0], v[1]),
+                                     pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]),
+                                     pack_bf16(v[6], v[7]));
+                    } else if (bj <= br) {
+                        float* dst = Ab + bidx(br, bj) * 16 * BS + rl * BS + 8 * wg;
+                        *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+                        *reinterpret_cast<float4*>(dst + 4) = make_float4(v[4], v[5], v[6], v[7]);
+                    }
+                }
+            }
+            bar_sync(2, 256);
+            if (P == 0) TRACE_PREP(24);
+
+            // ---- T = (I + A)^-1 in 16x16 blocks
+            // diagonal blocks: forward substitution, four threads per column (thread rq
+            // holds rows 4 rq .. 4 rq + 3), x_m broadcast from its owner at step m. A's
+            // diagonal blocks hold zeros on and above the diagonal, so every row may
+            // accumulate at every step.
+            {
+                const int i = P >> 6, cc = (P >> 2) & 15, rq = P & 3;
+                const float* Ad = Ab + bidx(i, i) * 16 * BS + 4 * rq * BS;
+                float acc[4] = {0.f, 0.f, 0.f, 0.f}, xr[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int m = 0; m < 16; ++m) {
+                    const float sh =
+                        __shfl_sync(0xffffffffu, -acc[m & 3], (lane & ~3) | (m >> 2));
+                    const float xm = (m < cc) ? 0.f : ((m == cc) ? 1.f : sh);
+                    if ((m >> 2) == rq) xr[m & 3] = xm;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc[e] = fmaf(Ad[e * BS + m], xm, acc[e]);
+                }
+                float* Td = Tb + bidx(i, i) * 16 * BS + 4 * rq * BS;
+                const int J = 16 * i + cc;
+                const float bj = sc.beta[J], wj = bj * sc.Gam[J];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    Td[e * BS + cc] = xr[e];
+                    st_shared_b16(sw128_elem(tu, 16 * i + 4 * rq + e, J), xr[e] * bj);
+                    st_shared_b16(sw128_elem(tw, 16 * i + 4 * rq + e, J), xr[e] * wj);
+                }
+            }
+            bar_sync(2, 256);
+            if (P == 0) TRACE_PREP(25);
+            // off-diagonal blocks by doubling. Step 1: T(i,i-1) = -T(i,i) A(i,i-1) T(i-1,i-1)
+            // for i = 1, 3; warp: (i, 8 columns)
+            if (pw < 4) {
+                const int i = (pw & 2) ? 3 : 1, j = i - 1, nt = pw & 1;
+                float x[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
+                block_mma(x, Ab + bidx(i, j) * 16 * BS, Tb + bidx(j, j) * 16 * BS, nt, g8, t4);
+                uint32_t bx[2][2];
+                c_to_b(x, g8, t4, bx);
+                block_mma_b(e, Tb + bidx(i, i) * 16 * BS, bx, g8, t4);
+                block_store(e, Tb + bidx(i, j) * 16 * BS, i, j, nt, g8, t4, sc.beta, sc.Gam, tu,
+                            tw);
+            }
+            bar_sync(2, 256);
+            if (P == 0) TRACE_PREP(26);
+            // Step 2: the lower-left 32x32 quadrant, T_BA = -T_BB (A_BA T_AA): with
+            // X(l,j) = sum_{m=j..1} A(l,m) T(m,j), T(2,j) = -T(2,2) X(2,j) and
+            // T(3,j) = -(T(3,2) X(2,j) + T(3,3) X(3,j)); warp: (i, j, 8 columns)
+            {
+                const int i = 2 + (pw >> 2), j = (pw >> 1) & 1, nt = pw & 1;
+                float x2[4] = {0.f, 0.f, 0.f, 0.f}, x3[4] = {0.f, 0.f, 0.f, 0.f};
+                float e[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int m = j; m < 2; ++m) {
+                    block_mma(x2, Ab + bidx(2, m) * 16 * BS, Tb + bidx(m, j) * 16 * BS, nt, g8,
+                              t4);
+                    if (i == 3)
+                        block_mma(x3, Ab + bidx(3, m) * 16 * BS, Tb + bidx(m, j) * 16 * BS, nt,
+                                  g8, t4);
+                }
+                uint32_t bx[2][2];
+                c_to_b(x2, g8, t4, bx);
+                block_mma_b(e, Tb + bidx(i, 2) * 16 * BS, bx, g8, t4);
+                if (i == 3) {
+                    c_to_b(x3, g8, t4, bx);
+                    block_mma_b(e, Tb + bidx(3, 3) * 16 * BS, bx, g8, t4);
+                }
+                block_store(e, Tb + bidx(i, j) * 16 * BS, i, j, nt, g8, t4, sc.beta, sc.Gam, tu,
+                            tw);
+            }
+            bar_sync(2, 256);
+            fence_proxy_async_smem();
+            if (P == 0) {
+                TRACE_PREP(27);
+                mbar_arrive(&bar[PB_PREP]);
+            }
+            // ---- W = T_W K from TMEM (rows 0..63: lanes 0..63) into the W staging tiles;
+            // two warps per lane quadrant, one 64-column block each
+            ok = wait_or_abort(&bar[PB_WDONE], 0, abort_flag, ST_PREP);
+            if (!bar_any(2, 256, !ok || *abort_flag)) {
+                tc_fence_after();
+                if (q < 2) {
+                    const int hc = (warp >= 5) ? 1 : 0;
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        float w[32];
+                        tmem_ld32(tmem + lane_off + PT_W + 64 * hc + 32 * hh, w);
+                        write_row32(sb + P_W + 8192 * hc, L, 4 * hh, w);
+                    }
+                }
+                fence_proxy_async_smem();
+                bar_sync(2, 256);
+                if (P == 0) {
+                    TRACE_PREP(28);
+                    // T_U, then P | W (adjacent here and in the workspace)
+                    uint8_t* ws = a.ws + ws_offset(b, h, c, a.Hv, nch);
+                    bulk_s2g(ws + WS_TU, sb + P_TU, 8192);
+                    bulk_s2g(ws + WS_P, sb + P_P, 8192 + 16384);
+                    bulk_commit();
+                    bulk_wait_all();
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, PT_COLS);
+    }
+}
+
+// ---------------------------------------------------------------- the carry kernel
+
+// One CTA per (64-column state slice, value head h, batch b), sequential over chunks.
+// Warp 0 streams q, k, v and the prep's tiles of each chunk into a two-stage ring and
+// writes the chunk's decay scalars; warp 1 issues U~ = T_U V once the chunk has landed
+// and U~(c-1) has been consumed; warps 2..5 (one per TMEM lane quadrant, thread = state
+// row) issue the S0-dependent MMAs themselves and do U, the output and the state update.
+__global__ void __launch_bounds__(CARRY_THREADS, 1)
+    carry_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                    const __grid_constant__ CUtensorMap mv, TcArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sbase = smem_u32(sm);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+    uint32_t* misc = reinterpret_cast<uint32_t*>(sm + OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+    CarryScalars* scal = reinterpret_cast<CarryScalars*>(sm + OFF_SCAL);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int n0 = blockIdx.x * NS, h = blockIdx.y, b = blockIdx.z;
+    const int kh = h / (a.Hv / a.Hk);
+    const int S = a.S;
+    const int nch = (S + C - 1) / C;
+
+    if (tid == 0) {
+        for (int i = 0; i < B_COUNT; ++i)
             mbar_init(&bar[i], (i == B_FULL0 || i == B_FULL1) ? 2 : 1);
         *abort_flag = 0;
-        *u_ctr = 0;
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -402,56 +765,65 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         prefetch_tensormap(&mk);
         prefetch_tensormap(&mv);
     }
-    // T_U / T_W blocks above the diagonal are never written: zero both stages once
-    for (int i = tid; i < 4 * 8192 / 16; i += NTHREADS) {
-        const int tile = i >> 9, off = (i & 511) * 16;
-        const uint32_t base =
-            sbase + (uint32_t)(tile >> 1) * STAGE_BYTES + ((tile & 1) ? OFF_TW : OFF_TU);
-        st_shared_v4(base + off, 0u, 0u, 0u, 0u);
-    }
-    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = misc[0];
 
     if (warp == 0) {
-        // -------------------------------------------- TMA producer + decay tables (warp)
+        // ------------------------------------------ loads + decay scalars (warp)
         const int zq = b * a.Hk + kh, zv = b * a.Hv + h;
         const float* gp = a.g + (size_t)zv * S;
-        const float* bp = a.beta + (size_t)zv * S;
+        const uint8_t* wsh = a.ws + ws_offset(b, h, 0, a.Hv, nch);
         int issued = 0;
+        float ng0, ng1;  // g of the next chunk, loaded one iteration ahead
+        ng0 = (lane < S) ? gp[lane] : 0.f;
+        ng1 = (lane + 32 < S) ? gp[lane + 32] : 0.f;
         for (int c = 0; c < nch; ++c) {
             const int s = c & 1;
             int ok = 1;
             if (lane == 0) {
-                if (c >= 2 &&
-                    !mbar_wait_bounded(&bar[B_EMPTY0 + s], ((c >> 1) + 1) & 1, kWaitNs)) {
-                    record_failure(abort_flag, ST_PRODUCER);
+                if (c >= 2 && !wait_or_abort(&bar[B_EMPTY0 + s], ((c >> 1) + 1) & 1, abort_flag,
+                                             ST_PRODUCER))
                     ok = 0;
-                }
                 if (*abort_flag) ok = 0;
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             if (lane == 0) {
                 uint8_t* st = sm + s * STAGE_BYTES;
+                const uint8_t* wsc = wsh + (size_t)c * WS_UNIT;
                 TRACE(c, 0);
-                mbar_arrive_expect_tx(&bar[B_FULL0 + s], 2 * 16384 + 8192);
+                mbar_arrive_expect_tx(&bar[B_FULL0 + s], 2 * 16384 + 8192 + WS_UNIT);
                 for (int blk = 0; blk < 2; ++blk) {
                     tma_load_3d(st + blk * BLK_STRIDE + OFF_Q, &mq, &bar[B_FULL0 + s], blk * 64,
                                 c * C, zq);
                     tma_load_3d(st + blk * BLK_STRIDE + OFF_K, &mk, &bar[B_FULL0 + s], blk * 64,
                                 c * C, zq);
+                    bulk_g2s(st + blk * BLK_STRIDE + OFF_W, wsc + WS_W + blk * 8192, 8192,
+                             &bar[B_FULL0 + s]);
                 }
                 tma_load_3d(st + OFF_V, &mv, &bar[B_FULL0 + s], n0, c * C, zv);
+                bulk_g2s(st + OFF_TU, wsc + WS_TU, 16384, &bar[B_FULL0 + s]);  // T_U | P
+                // chunk c + 2 goes to L2 now; its copy is issued once this stage is free
+                if (c + 2 < nch) {
+                    for (int blk = 0; blk < 2; ++blk) {
+                        tma_prefetch_l2_3d(&mq, blk * 64, (c + 2) * C, zq);
+                        tma_prefetch_l2_3d(&mk, blk * 64, (c + 2) * C, zq);
+                    }
+                    tma_prefetch_l2_3d(&mv, n0, (c + 2) * C, zv);
+                    bulk_prefetch_l2(wsc + 2 * WS_UNIT, WS_UNIT);
+                }
             }
             issued = c + 1;
-            // decay tables of chunk c (padding tokens: g = beta = 0, an exact no-op)
-            StageScalars& sc = scal[s];
-            const int t0 = c * C + lane, t1 = t0 + 32;
-            float x0 = (t0 < S) ? gp[t0] : 0.f, x1 = (t1 < S) ? gp[t1] : 0.f;
-            const float be0 = (t0 < S) ? bp[t0] : 0.f, be1 = (t1 < S) ? bp[t1] : 0.f;
+            // decay scalars of chunk c (padding tokens: g = 0)
+            CarryScalars& sc = scal[s];
+            float x0 = ng0, x1 = ng1;
+            {
+                const int t0 = (c + 1) * C + lane, t1 = t0 + 32;
+                ng0 = (t0 < S) ? gp[t0] : 0.f;
+                ng1 = (t1 < S) ? gp[t1] : 0.f;
+            }
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
                 const float y0 = __shfl_up_sync(0xffffffffu, x0, off);
@@ -463,27 +835,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
             x1 += __shfl_sync(0xffffffffu, x0, 31);
             const float gl = __shfl_sync(0xffffffffu, x1, 31);
-            const float e0 = __shfl_sync(0xffffffffu, x0, lane | 15);
-            const float e1 = __shfl_sync(0xffffffffu, x1, lane | 15);
-            sc.gam[lane] = x0;
-            sc.gam[lane + 32] = x1;
-            sc.beta[lane] = be0;
-            sc.beta[lane + 32] = be1;
-            sc.ctab[lane] = __expf(e0 - x0);
-            sc.ctab[lane + 32] = __expf(e1 - x1);
             sc.Gam[lane] = __expf(x0);
             sc.Gam[lane + 32] = __expf(x1);
             sc.kdec[lane] = __expf(gl - x0);
             sc.kdec[lane + 32] = __expf(gl - x1);
-            if (lane == 15) {
-                sc.endgam[0] = x0;
-                sc.endgam[2] = x1;
-            }
-            if (lane == 31) {
-                sc.endgam[1] = x0;
-                sc.endgam[3] = x1;
-                sc.Gl = __expf(gl);
-            }
+            if (lane == 31) sc.Gl = __expf(gl);
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar[B_FULL0 + s]);
         }
@@ -493,54 +849,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 mbar_wait_bounded(&bar[B_FULL0 + (c & 1)], (c >> 1) & 1, kWaitNs);
         }
     } else if (warp == 1) {
-        // ------------------------------------------- MMA issuer for the prep (one thread)
-        // Gram(c) once the chunk has landed and the prep has read Gram(c-1); WY(c) once
-        // the prep has written T_U/T_W/P and the carry has consumed U~(c-1). The carry's
-        // own MMAs are issued by the carry.
+        // ------------------------------------------------------ U~ issuer (one thread)
         if (lane == 0) {
-            int g = 0, wu = 0;
-            uint32_t idle = 0;
-            uint64_t t_last = globaltimer_ns();
-            while (wu < nch) {
-                bool did = false;
-                if (g < nch && (g == 0 || mbar_test_wait(&bar[B_GFREE], (g - 1) & 1)) &&
-                    mbar_test_wait(&bar[B_FULL0 + (g & 1)], (g >> 1) & 1)) {
-                    tc_fence_after();
-                    issue_gram(tmem, sbase + (g & 1) * STAGE_BYTES);
-                    tc_commit(&bar[B_GRAM]);
-                    TRACE(g, 1);
-                    ++g;
-                    did = true;
-                } else if (wu < g && ld_acquire_u32(u_ctr) >= (uint32_t)wu &&
-                           mbar_test_wait(&bar[B_PREP], wu & 1)) {
-                    tc_fence_after();
-                    issue_wy(tmem, sbase + (wu & 1) * STAGE_BYTES);
-                    tc_commit(&bar[B_WDONE]);
-                    TRACE(wu, 2);
-                    ++wu;
-                    did = true;
-                }
-                if (did) {
-                    idle = 0;
-                } else if ((++idle & 255) == 0) {
-                    // time and the abort flag are checked every 256 idle polls
-                    const uint64_t now = globaltimer_ns();
-                    if (idle == 256) t_last = now;
-                    if (now - t_last > kWaitNs) {
-                        record_failure(abort_flag, ST_MMA);
-                        break;
-                    }
-                    if (*abort_flag) break;
-                }
+            int c = 0;
+            for (; c < nch; ++c) {
+                const bool ok =
+                    wait_or_abort(&bar[B_FULL0 + (c & 1)], (c >> 1) & 1, abort_flag, ST_MMA) &&
+                    (c == 0 || wait_or_abort(&bar[B_UFREE], (c - 1) & 1, abort_flag, ST_MMA));
+                if (!ok) break;
+                tc_fence_after();
+                issue_u(tmem, sbase + (c & 1) * STAGE_BYTES);
+                tc_commit(&bar[B_UDONE]);
+                TRACE(c, 2);
             }
-            // no MMA of this thread may be in flight when TMEM is freed
-            tc_commit(&bar[B_DRAIN]);
-            mbar_wait_bounded(&bar[B_DRAIN], 0, kWaitNs);
+            if (c > 0) {
+                // no MMA of this thread may be in flight when TMEM is freed
+                tc_commit(&bar[B_DRAIN_U]);
+                mbar_wait_bounded(&bar[B_DRAIN_U], 0, kWaitNs);
+            }
         }
-    } else if (warp < 6) {
+    } else {
         // ------------------------------------------------------------ carry (128 threads)
-        // Issues its own MMAs (thread L = 0) so that the sequential chain carry ->
-        // tensor core -> carry has no hand-off through another warp.
         const int q = warp & 3;
         const int L = 32 * q + lane;  // TMEM lane = state row (Dk index) = token for L < 64
         const uint32_t lane_off = (uint32_t)(32 * q) << 16;
@@ -548,58 +877,53 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         float* gstate = a.state + ((size_t)(b * a.Hv + h) * 128 + L) * 128 + n0;
         __nv_bfloat16* gout = a.out + (size_t)(b * a.Hv + h) * S * 128 + n0;
 
-        float Sm[NS];
-        if (a.state_is_input) {
+        // the fp32 state lives in TMEM (columns TM_SS), its bf16 copy in the S tile
 #pragma unroll
-            for (int j = 0; j < NS; j += 4) {
-                const float4 x = *reinterpret_cast<const float4*>(gstate + j);
-                Sm[j] = x.x;
-                Sm[j + 1] = x.y;
-                Sm[j + 2] = x.z;
-                Sm[j + 3] = x.w;
+        for (int hh = 0; hh < 2; ++hh) {
+            float Sm[32];
+            if (a.state_is_input) {
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {
+                    const float4 x = *reinterpret_cast<const float4*>(gstate + 32 * hh + j);
+                    Sm[j] = x.x;
+                    Sm[j + 1] = x.y;
+                    Sm[j + 2] = x.z;
+                    Sm[j + 3] = x.w;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) Sm[j] = 0.f;
             }
-        } else {
-#pragma unroll
-            for (int j = 0; j < NS; ++j) Sm[j] = 0.f;
+            tmem_st32(tmem + lane_off + TM_SS + 32 * hh, Sm);
+            write_row32(s_tile, L, 4 * hh, Sm);
         }
-        write_row32(s_tile, L, 0, Sm);
-        write_row32(s_tile, L, 4, Sm + 32);
+        tmem_wait_st();
         fence_proxy_async_smem();
+        tc_fence_before();
         bar_sync(1, 128);
 
+        int mmas = 0;
         for (int c = 0; c < nch; ++c) {
             const int s = c & 1;
             const uint32_t st = sbase + s * STAGE_BYTES;
-            // W(c) = T_W K from TMEM into the W tile (bf16), then MMA1: [W; Q] S0
-            bool ok = mbar_wait_bounded(&bar[B_WDONE], c & 1, kWaitNs);
-            if (!ok) record_failure(abort_flag, ST_CARRY);
+            // MMA1: [W; Q] S0 once the chunk has landed (the state tile is current)
+            bool ok = wait_or_abort(&bar[B_FULL0 + s], (c >> 1) & 1, abort_flag, ST_CARRY);
             if (bar_any(1, 128, !ok || *abort_flag)) break;
-            if (L == 0) TRACE(c, 12);
-            tc_fence_after();
-            if (L < 64) {
-#pragma unroll
-                for (int qd = 0; qd < 4; ++qd) {
-                    float w[32];
-                    tmem_ld32(tmem + lane_off + TM_W + 32 * qd, w);
-                    write_row32(st + (qd >> 1) * BLK_STRIDE + OFF_W, L, 4 * (qd & 1), w);
-                }
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            bar_sync(1, 128);
             if (L == 0) {
+                TRACE(c, 12);
                 tc_fence_after();
                 issue_carry1(tmem, st, s_tile);
                 tc_commit(&bar[B_ADONE]);
+                mmas = 1;
                 TRACE(c, 3);
             }
-            ok = mbar_wait_bounded(&bar[B_ADONE], c & 1, kWaitNs);
-            if (!ok) record_failure(abort_flag, ST_CARRY);
+            ok = wait_or_abort(&bar[B_ADONE], c & 1, abort_flag, ST_CARRY) &&
+                 wait_or_abort(&bar[B_UDONE], c & 1, abort_flag, ST_CARRY);
             if (bar_any(1, 128, !ok || *abort_flag)) break;
             if (L == 0) TRACE(c, 13);
             tc_fence_after();
-            // per-chunk scalars are read now: the producer may rewrite this stage's tables
-            // once the chunk's last MMAs complete
+            // per-chunk scalars are read now: the producer may rewrite this stage's
+            // scalars once the chunk's last MMAs complete
             const float Gl = scal[s].Gl;
             float gm = 0.f;
             if (L < 64) {
@@ -625,15 +949,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             bar_sync(1, 128);
             if (L == 0) {
                 TRACE(c, 14);
-                st_release_u32(u_ctr, (uint32_t)(c + 1));  // U~(c) consumed
+                mbar_arrive(&bar[B_UFREE]);  // U~(c) consumed: U~(c + 1) may overwrite it
                 tc_fence_after();
                 issue_carry23(tmem, st, u_tile, u2_tile);
                 tc_commit(&bar[B_CDONE]);
                 tc_commit(&bar[B_EMPTY0 + s]);
                 TRACE(c, 4);
             }
-            ok = mbar_wait_bounded(&bar[B_CDONE], c & 1, kWaitNs);
-            if (!ok) record_failure(abort_flag, ST_CARRY);
+            ok = wait_or_abort(&bar[B_CDONE], c & 1, abort_flag, ST_CARRY);
             if (bar_any(1, 128, !ok || *abort_flag)) break;
             if (L == 0) TRACE(c, 15);
             tc_fence_after();
@@ -665,179 +988,37 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
             // S1 = Gamma_last S0 + K^T U' for state row L
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                float d[32];
-                tmem_ld32(tmem + lane_off + TM_S + 32 * hh, d);
+            for (int qq = 0; qq < 4; ++qq) {
+                float d[16], sv[16];
+                tmem_ld16x2(tmem + lane_off + TM_S + 16 * qq, tmem + lane_off + TM_SS + 16 * qq, d,
+                            sv);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) Sm[32 * hh + j] = fmaf(Gl, Sm[32 * hh + j], d[j]);
-                write_row32(s_tile, L, 4 * hh, Sm + 32 * hh);
+                for (int j = 0; j < 16; ++j) sv[j] = fmaf(Gl, sv[j], d[j]);
+                tmem_st16(tmem + lane_off + TM_SS + 16 * qq, sv);
+                write_row16(s_tile, L, 2 * qq, sv);
             }
+            tmem_wait_st();
             fence_proxy_async_smem();
             tc_fence_before();
             bar_sync(1, 128);
             if (L == 0) TRACE(c, 16);
         }
         if (!*abort_flag) {
+            tc_fence_after();
 #pragma unroll
-            for (int j = 0; j < NS; j += 4)
-                *reinterpret_cast<float4*>(gstate + j) =
-                    make_float4(Sm[j], Sm[j + 1], Sm[j + 2], Sm[j + 3]);
+            for (int hh = 0; hh < 2; ++hh) {
+                float Sm[32];
+                tmem_ld32(tmem + lane_off + TM_SS + 32 * hh, Sm);
+#pragma unroll
+                for (int j = 0; j < 32; j += 4)
+                    *reinterpret_cast<float4*>(gstate + 32 * hh + j) =
+                        make_float4(Sm[j], Sm[j + 1], Sm[j + 2], Sm[j + 3]);
+            }
         }
         // no MMA of the carry may be in flight when TMEM is freed
-        if (L == 0 && *abort_flag) {
-            tc_commit(&bar[B_DRAIN + 1]);
-            mbar_wait_bounded(&bar[B_DRAIN + 1], 0, kWaitNs);
-        }
-    } else {
-        // ------------------------------------------------------------ prep (256 threads)
-        const int P = tid - 192;
-        const int pw = P >> 5;  // prep warp 0..7
-        const int wg = P >> 7;  // column half of the Gram matrices
-        const int q = warp & 3;
-        const int L = 32 * q + lane;
-        const int g8 = lane >> 2, t4 = lane & 3;
-        const uint32_t lane_off = (uint32_t)(32 * q) << 16;
-        float* xw = Xb + pw * 16 * 8;
-
-        for (int c = 0; c < nch; ++c) {
-            const int s = c & 1;
-            const uint32_t st = sbase + s * STAGE_BYTES;
-            const uint32_t tu = st + OFF_TU, tw = st + OFF_TW;
-            const StageScalars& sc = scal[s];
-            bool ok = mbar_wait_bounded(&bar[B_FULL0 + s], (c >> 1) & 1, kWaitNs) &&
-                      mbar_wait_bounded(&bar[B_GRAM], c & 1, kWaitNs);
-            if (!ok) record_failure(abort_flag, ST_PREP);
-            if (bar_any(2, 256, !ok || *abort_flag)) break;
-            if (P == 0) TRACE(c, 7);
-            tc_fence_after();
-
-            // ---- P (bf16 tile) and A (fp32 blocks) from the Gram matrices:
-            // thread (wg, L) takes row L of [QK^T; KK^T], columns 32 wg .. 32 wg + 31
-            {
-                const int r = L & 63, br = r >> 4, rl = r & 15;
-                const bool isP = L < 64;
-                const float gr = sc.gam[r];
-                const float scl = isP ? 1.f : sc.beta[r];
-                float gv[32];
-                tmem_ld32(tmem + lane_off + TM_G + 32 * wg, gv);
-                if (P == 0) TRACE(c, 19);
-                if (lane == 0) TRACE(c, 24 + pw);
-#pragma unroll
-                for (int bq = 0; bq < 2; ++bq) {
-                    const int bj = 2 * wg + bq;
-                    if (bj < br) {
-                        const float f = __expf(gr - sc.endgam[bj]) * scl;
-#pragma unroll
-                        for (int jj = 0; jj < 16; ++jj)
-                            gv[16 * bq + jj] *= f * sc.ctab[16 * bj + jj];
-                    } else if (bj == br) {
-                        // branch-free: exp of a non-positive argument, then the mask
-                        const int lim = isP ? rl : rl - 1;
-#pragma unroll
-                        for (int jj = 0; jj < 16; ++jj) {
-                            const float e = __expf(fminf(gr - sc.gam[16 * bj + jj], 0.f));
-                            const float m = (jj <= lim) ? scl : 0.f;
-                            gv[16 * bq + jj] *= e * m;
-                        }
-                    } else {
-#pragma unroll
-                        for (int jj = 0; jj < 16; ++jj) gv[16 * bq + jj] = 0.f;
-                    }
-                }
-                if (isP) {
-                    write_row32(st + OFF_P, r, 4 * wg, gv);
-                } else {
-#pragma unroll
-                    for (int bq = 0; bq < 2; ++bq) {
-                        const int bj = 2 * wg + bq;
-                        if (bj <= br) {
-                            float* dst = Ab + bidx(br, bj) * 16 * BS + rl * BS;
-#pragma unroll
-                            for (int jj = 0; jj < 16; jj += 4)
-                                *reinterpret_cast<float4*>(dst + jj) =
-                                    make_float4(gv[16 * bq + jj], gv[16 * bq + jj + 1],
-                                                gv[16 * bq + jj + 2], gv[16 * bq + jj + 3]);
-                        }
-                    }
-                }
-            }
-            if (lane == 0) TRACE(c, 32 + pw);
-            tc_fence_before();
-            bar_sync(2, 256);
-            if (P == 0) {
-                TRACE(c, 8);
-                mbar_arrive(&bar[B_GFREE]);  // Gram(c) read: Gram(c+1) may overwrite it
-            }
-
-            // ---- T = (I + A)^-1 in 16x16 blocks
-            // diagonal blocks: forward substitution, one column per thread
-            if (P < 64) {
-                const int i = P >> 4, cc = P & 15;
-                const float* Ad = Ab + bidx(i, i) * 16 * BS;
-                float xs[16], acc[16];
-#pragma unroll
-                for (int r = 0; r < 16; ++r) acc[r] = 0.f;
-#pragma unroll
-                for (int m = 0; m < 16; ++m) {
-                    const float xm = (m < cc) ? 0.f : ((m == cc) ? 1.f : -acc[m]);
-                    xs[m] = xm;
-#pragma unroll
-                    for (int r = m + 1; r < 16; ++r) acc[r] = fmaf(Ad[r * BS + m], xm, acc[r]);
-                }
-                float* Td = Tb + bidx(i, i) * 16 * BS;
-                const int J = 16 * i + cc;
-                const float bj = sc.beta[J], wj = bj * sc.Gam[J];
-#pragma unroll
-                for (int r = 0; r < 16; ++r) {
-                    Td[r * BS + cc] = xs[r];
-                    st_shared_b16(sw128_elem(tu, 16 * i + r, J), xs[r] * bj);
-                    st_shared_b16(sw128_elem(tw, 16 * i + r, J), xs[r] * wj);
-                }
-            }
-            bar_sync(2, 256);
-            if (P == 0) TRACE(c, 9);
-            // level 1: T(i,i-1) = -T(i,i) A(i,i-1) T(i-1,i-1), i = 1..3 (warp: block, 8 columns)
-            if (pw < 6) {
-                const int i = 1 + (pw >> 1), nt = pw & 1;
-                float x[4] = {0.f, 0.f, 0.f, 0.f};
-                block_mma(x, Ab + bidx(i, i - 1) * 16 * BS, Tb + bidx(i - 1, i - 1) * 16 * BS, nt,
-                          g8, t4);
-                block_finish(x, Tb + bidx(i, i) * 16 * BS, Tb + bidx(i, i - 1) * 16 * BS, xw, i,
-                             i - 1, nt, g8, t4, sc.beta, sc.Gam, tu, tw);
-            }
-            bar_sync(2, 256);
-            // level 2: T(j+2,j) = -T(j+2,j+2) (A(j+2,j) T(j,j) + A(j+2,j+1) T(j+1,j))
-            if (pw < 4) {
-                const int j = pw >> 1, i = j + 2, nt = pw & 1;
-                float x[4] = {0.f, 0.f, 0.f, 0.f};
-                block_mma(x, Ab + bidx(i, j) * 16 * BS, Tb + bidx(j, j) * 16 * BS, nt, g8, t4);
-                block_mma(x, Ab + bidx(i, j + 1) * 16 * BS, Tb + bidx(j + 1, j) * 16 * BS, nt, g8,
-                          t4);
-                block_finish(x, Tb + bidx(i, i) * 16 * BS, Tb + bidx(i, j) * 16 * BS, xw, i, j, nt,
-                             g8, t4, sc.beta, sc.Gam, tu, tw);
-            }
-            bar_sync(2, 256);
-            // level 3: T(3,0) = -T(3,3) (A(3,0) T(0,0) + A(3,1) T(1,0) + A(3,2) T(2,0))
-            if (pw < 2) {
-                const int nt = pw;
-                float x[4] = {0.f, 0.f, 0.f, 0.f};
-                block_mma(x, Ab + bidx(3, 0) * 16 * BS, Tb + bidx(0, 0) * 16 * BS, nt, g8, t4);
-                block_mma(x, Ab + bidx(3, 1) * 16 * BS, Tb + bidx(1, 0) * 16 * BS, nt, g8, t4);
-                block_mma(x, Ab + bidx(3, 2) * 16 * BS, Tb + bidx(2, 0) * 16 * BS, nt, g8, t4);
-                block_finish(x, Tb + bidx(3, 3) * 16 * BS, Tb + bidx(3, 0) * 16 * BS, xw, 3, 0, nt,
-                             g8, t4, sc.beta, sc.Gam, tu, tw);
-            }
-            fence_proxy_async_smem();
-            // the issuer must have taken prep_ready(c-1) (its WY has completed) before
-            // prep_ready(c) is posted, so that barrier never runs two phases ahead
-            ok = c == 0 || mbar_wait_bounded(&bar[B_WDONE], (c - 1) & 1, kWaitNs);
-            if (!ok) record_failure(abort_flag, ST_PREP);
-            if (bar_any(2, 256, !ok || *abort_flag)) break;
-            if (P == 0) {
-                TRACE(c, 10);
-                mbar_arrive(&bar[B_PREP]);
-            }
-
+        if (L == 0 && mmas && *abort_flag) {
+            tc_commit(&bar[B_DRAIN_C]);
+            mbar_wait_bounded(&bar[B_DRAIN_C], 0, kWaitNs);
         }
     }
 
@@ -849,6 +1030,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tmem_dealloc(tmem, TM_COLS);
     }
 }
+
+// ---------------------------------------------------------------- host side
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -883,21 +1066,37 @@ bool prefill_tc_supported(const PrefillArgs& a, bool bf16) {
     return bf16 && a.Dk == 128 && a.Dv == 128 && a.S > 0;
 }
 
+size_t prefill_tc_workspace_bytes(int B, int Hv, int S) {
+    const size_t nch = ((size_t)S + C - 1) / C;
+    return (size_t)B * (size_t)Hv * nch * WS_UNIT;
+}
+
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream, int* launched) {
     *launched = 0;
+    if (a.workspace == nullptr || a.workspace_bytes < prefill_tc_workspace_bytes(a.B, a.Hv, a.S))
+        return cudaErrorInvalidValue;
     CUtensorMap mq, mk, mv;
     if (!encode_3d(&mq, a.q, a.S, a.B * a.Hk) || !encode_3d(&mk, a.k, a.S, a.B * a.Hk) ||
         !encode_3d(&mv, a.v, a.S, a.B * a.Hv))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(prep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)PREP_SMEM);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(carry_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)CARRY_SMEM);
     if (e != cudaSuccess) return e;
     TcArgs t{a.g, a.beta, a.scale, a.B, a.Hk, a.Hv, a.S, a.state, a.state_is_input,
-             static_cast<__nv_bfloat16*>(a.out)};
-    const dim3 grid(128 / NS, a.Hv, a.B);
-    prefill_tc_kernel<<<grid, NTHREADS, SMEM_BYTES, stream>>>(mq, mk, mv, t);
+             static_cast<__nv_bfloat16*>(a.out), static_cast<uint8_t*>(a.workspace)};
+    const int nch = (a.S + C - 1) / C;
+    prep_tc_kernel<<<dim3(nch, a.Hv, a.B), PREP_THREADS, PREP_SMEM, stream>>>(mq, mk, t);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
     *launched = 1;
-    return cudaGetLastError();
+    carry_tc_kernel<<<dim3(128 / NS, a.Hv, a.B), CARRY_THREADS, CARRY_SMEM, stream>>>(mq, mk, mv,
+                                                                                       t);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) *launched = 2;
+    return e;
 }
 
 }  // namespace gdn
