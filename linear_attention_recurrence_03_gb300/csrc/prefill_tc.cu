@@ -91,24 +91,37 @@ constexpr int C = 64;    // chunk length
 constexpr int NS = 64;   // state columns per carry CTA
 constexpr uint64_t kWaitNs = 2000000000ull;
 
-// ---- workspace: per (batch, value head, chunk) unit, 32 KB of bf16 tiles, each 64 rows
-// x 64 columns in the 128-byte swizzled layout: T_U | P | W[:, 0:64] | W[:, 64:128]
-constexpr uint32_t WS_UNIT = 32768;
-constexpr uint32_t WS_TU = 0, WS_P = 8192, WS_W = 16384;
+// ---- workspace: per (batch, value head, chunk) unit, four bf16 tiles of 64 rows x 64
+// columns in the 128-byte swizzled layout, T_U | P | W[:, 0:64] | W[:, 64:128], then
+// the carry's decay scalars of the chunk (CarryScalars)
+constexpr uint32_t WS_UNIT = 33792;
+constexpr uint32_t WS_TU = 0, WS_P = 8192, WS_W = 16384, WS_CS = 32768;
 
-// ---- prep kernel: shared memory map (offsets from a 1024-byte aligned base)
-//   block b (Dk columns 64b..64b+63): Q_b | K_b (8 KB each), stride 16 KB
-//   T_U, T_W, P (adjacent: [T_W; P] is one 128-row operand), W staging (two 8 KB blocks)
-//   fp32 blocks of A and T, scalars, barriers
+struct CarryScalars {
+    float Gam[C];   // exp(gamma_r)
+    float kdec[C];  // exp(gamma_last - gamma_r)
+    float Gl;       // exp(gamma_last)
+    float pad[3];
+};
+static_assert(sizeof(CarryScalars) % 16 == 0 && WS_CS + sizeof(CarryScalars) <= WS_UNIT,
+              "scalars fit the unit as whole 16-byte rows");
+
+// ---- prep kernel: shared memory map (offsets from a 1024-byte aligned base), sized
+// for three CTAs per SM
+//   block b (Dk columns 64b..64b+63): Q_b | K_b (8 KB each), stride 16 KB. Once the Gram
+//   MMA has read Q, the Q_b slots hold the fp32 blocks of A (blocks 0-5 | 6-9), and once
+//   the W MMA has read K and the solve is done, the bf16 W blocks (W_b in slot Q_b)
+//   T_U, T_W, P (adjacent: [T_W; P] is one 128-row operand)
+//   fp32 blocks of T, scalars, barriers
 constexpr int PREP_THREADS = 288;  // warp 0: producer + MMA issuer; warps 1..8: prep
 constexpr uint32_t PQ_STRIDE = 16384;
 constexpr uint32_t PQ_Q = 0, PQ_K = 8192;
-constexpr uint32_t P_TU = 32768, P_TW = 40960, P_P = 49152, P_W = 57344;
-static_assert(P_P == P_TW + 8192 && P_W == P_P + 8192, "[T_W; P] one operand, P | W contiguous");
+constexpr uint32_t P_TU = 32768, P_TW = 40960, P_P = 49152;
+static_assert(P_P == P_TW + 8192, "[T_W; P] is one 128-row operand");
 constexpr int BS = 20;  // row stride (floats) of a 16x16 fp32 block
 constexpr uint32_t BLOCK_BYTES = 16 * BS * 4;
-constexpr uint32_t P_AB = 73728;                    // 10 lower blocks of A
-constexpr uint32_t P_TB = P_AB + 10 * BLOCK_BYTES;  // 10 lower blocks of T
+static_assert(6 * BLOCK_BYTES <= 8192 && 4 * BLOCK_BYTES <= 8192, "A blocks fit the Q slots");
+constexpr uint32_t P_TB = 57344;                      // 10 lower blocks of T
 constexpr uint32_t P_SCAL = P_TB + 10 * BLOCK_BYTES;
 
 struct PrepScalars {
@@ -118,16 +131,17 @@ struct PrepScalars {
     float Gam[C];     // exp(gamma_r)
     float endgam[4];  // gamma at the end of each 16-block
 };
-constexpr uint32_t P_BAR = P_SCAL + sizeof(PrepScalars);
+constexpr uint32_t P_CS = P_SCAL + sizeof(PrepScalars);  // CarryScalars staging
+constexpr uint32_t P_BAR = P_CS + sizeof(CarryScalars);
 constexpr uint32_t P_MISC = P_BAR + 64;
 constexpr uint32_t PREP_SMEM = P_MISC + 64 + 1024;  // + alignment slack
-static_assert(P_BAR % 8 == 0, "barrier alignment");
-static_assert(2 * (PREP_SMEM + 1024) <= 233472, "two prep CTAs per SM");
+static_assert(P_BAR % 8 == 0 && P_CS % 16 == 0, "barrier and copy alignment");
+static_assert(3 * (PREP_SMEM + 1024) <= 233472, "three prep CTAs per SM");
 
 // prep TMEM columns (fp32, 128 lanes)
-constexpr uint32_t PT_G = 0;    // Gram [QK^T; KK^T], 64 columns
-constexpr uint32_t PT_W = 128;  // [W; -], 128 columns
-constexpr uint32_t PT_COLS = 256;
+constexpr uint32_t PT_G = 0;  // Gram [QK^T; KK^T], 64 columns
+constexpr uint32_t PT_W = 0;  // [W; -], 128 columns (the Gram matrices are read by then)
+constexpr uint32_t PT_COLS = 128;
 
 enum { PB_FULL = 0, PB_GRAM, PB_PREP, PB_WDONE, PB_DRAIN, PB_COUNT };
 
@@ -136,7 +150,7 @@ enum { PB_FULL = 0, PB_GRAM, PB_PREP, PB_WDONE, PB_DRAIN, PB_COUNT };
 //     block b: W_b | Q_b | K_b (8 KB each, stride 24 KB)  ([W_b; Q_b] is one operand)
 //     V slice (64 tokens x 64 columns), T_U, P            ([T_U; P] is one operand)
 //   U, U' tiles, the bf16 state operand, per-stage scalars, barriers
-constexpr int CARRY_THREADS = 192;  // warp 0: producer; warp 1: U~ issuer; 2..5: carry
+constexpr int CARRY_THREADS = 320;  // warp 0: producer; warp 1: MMA issuer; 2..9: carry
 constexpr uint32_t BLK_STRIDE = 24576;
 constexpr uint32_t OFF_W = 0, OFF_Q = 8192, OFF_K = 16384;
 constexpr uint32_t OFF_V = 49152, OFF_TU = 57344, OFF_P = 65536;
@@ -147,12 +161,6 @@ constexpr uint32_t OFF_U2 = OFF_U + 8192;    // U' tile (decayed U)
 constexpr uint32_t OFF_S = OFF_U2 + 8192;    // bf16 state operand (128 x 64)
 constexpr uint32_t OFF_SCAL = OFF_S + 16384;
 
-struct CarryScalars {
-    float Gam[C];   // exp(gamma_r)
-    float kdec[C];  // exp(gamma_last - gamma_r)
-    float Gl;       // exp(gamma_last)
-    float pad[3];
-};
 constexpr uint32_t OFF_BAR = OFF_SCAL + 2 * sizeof(CarryScalars);
 constexpr uint32_t OFF_MISC = OFF_BAR + 128;
 constexpr uint32_t CARRY_SMEM = OFF_MISC + 64 + 1024;
@@ -160,16 +168,16 @@ static_assert(OFF_BAR % 8 == 0, "barrier alignment");
 static_assert(CARRY_SMEM <= 232448, "shared memory budget");
 
 // carry TMEM columns
-constexpr uint32_t TM_U = 0;     // [U~; -], 64 columns
-constexpr uint32_t TM_A = 64;    // [W S0; Q S0], 64 columns
-constexpr uint32_t TM_S = 128;   // state increment, 64 columns
-constexpr uint32_t TM_B = 192;   // [-; P U], 64 columns
-constexpr uint32_t TM_SS = 256;  // the fp32 state slice (row = Dk index), 64 columns
+// (U~ and [W S0; Q S0] have one buffer per chunk parity)
+constexpr uint32_t TM_U = 0;     // [U~; -], 2 x 64 columns
+constexpr uint32_t TM_A = 128;   // [W S0; Q S0], 2 x 64 columns
+constexpr uint32_t TM_S = 256;   // state increment, 64 columns
+constexpr uint32_t TM_B = 320;   // [-; P U], 64 columns
+constexpr uint32_t TM_SS = 384;  // the fp32 state slice (row = Dk index), 64 columns
 constexpr uint32_t TM_COLS = 512;
 
 enum {
-    B_FULL0 = 0, B_FULL1, B_EMPTY0, B_EMPTY1, B_UDONE, B_UFREE, B_ADONE, B_CDONE,
-    B_DRAIN_U, B_DRAIN_C, B_COUNT
+    B_FULL0 = 0, B_FULL1, B_EMPTY0, B_EMPTY1, B_ADONE, B_SDONE, B_CDONE, B_DRAIN, B_COUNT
 };
 
 // status bits
@@ -399,41 +407,45 @@ __device__ __forceinline__ void issue_w(uint32_t tmem, uint32_t sb) {
     for (int k = 0; k < 4; ++k) mma_bf16(tmem + PT_W, dadd(aw, k * 32), dadd(bk, k * 2048), id, k > 0);
 }
 
-// carry: [U~; P V] = [T_U; P] V over the 64 tokens
-__device__ __forceinline__ void issue_u(uint32_t tmem, uint32_t st) {
+// carry: [U~; P V] = [T_U; P] V over the 64 tokens, into the TMEM buffer `tu`
+__device__ __forceinline__ void issue_u(uint32_t tmem, uint32_t st, uint32_t tu) {
     constexpr uint32_t id = idesc_bf16(128, 64, false, true);
     const uint64_t au = smem_desc_sw128(st + OFF_TU, 16, 1024);
     const uint64_t bv = smem_desc_sw128(st + OFF_V, 8192, 1024);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) mma_bf16(tmem + TM_U, dadd(au, k * 32), dadd(bv, k * 2048), id, k > 0);
+    for (int k = 0; k < 4; ++k) mma_bf16(tmem + tu, dadd(au, k * 32), dadd(bv, k * 2048), id, k > 0);
 }
 
-// carry: [W S0; Q S0] = [W; Q] S0 over Dk = 128
-__device__ __forceinline__ void issue_carry1(uint32_t tmem, uint32_t st, uint32_t s_tile) {
+// carry: [W S0; Q S0] = [W; Q] S0 over Dk = 128, into the TMEM buffer `ta`
+__device__ __forceinline__ void issue_carry1(uint32_t tmem, uint32_t st, uint32_t s_tile,
+                                             uint32_t ta) {
     constexpr uint32_t id = idesc_bf16(128, 64, false, true);
     const uint64_t a0 = smem_desc_sw128(st + OFF_W, 16, 1024);
     const uint64_t b0 = smem_desc_sw128(s_tile, 8192, 1024);
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         const uint32_t off = (uint32_t)(k >> 2) * BLK_STRIDE + (uint32_t)(k & 3) * 32u;
-        mma_bf16(tmem + TM_A, dadd(a0, off), dadd(b0, k * 2048), id, k > 0);
+        mma_bf16(tmem + ta, dadd(a0, off), dadd(b0, k * 2048), id, k > 0);
     }
 }
 
-// carry: [T_U U; P U] = [T_U; P] U over the tokens, and K^T U' (K read M-major)
-__device__ __forceinline__ void issue_carry23(uint32_t tmem, uint32_t st, uint32_t u_tile,
-                                              uint32_t u2_tile) {
-    constexpr uint32_t id2 = idesc_bf16(128, 64, false, true);
-    const uint64_t ap = smem_desc_sw128(st + OFF_TU, 16, 1024);
-    const uint64_t bu = smem_desc_sw128(u_tile, 8192, 1024);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) mma_bf16(tmem + TM_B, dadd(ap, k * 32), dadd(bu, k * 2048), id2, k > 0);
-    constexpr uint32_t id3 = idesc_bf16(128, 64, true, true);
+// carry: the state increment K^T U' over the tokens (K read M-major)
+__device__ __forceinline__ void issue_carry3(uint32_t tmem, uint32_t st, uint32_t u2_tile) {
+    constexpr uint32_t id = idesc_bf16(128, 64, true, true);
     const uint64_t ak = smem_desc_sw128(st + OFF_K, BLK_STRIDE, 1024);
     const uint64_t bu2 = smem_desc_sw128(u2_tile, 8192, 1024);
 #pragma unroll
     for (int k = 0; k < 4; ++k)
-        mma_bf16(tmem + TM_S, dadd(ak, k * 2048), dadd(bu2, k * 2048), id3, k > 0);
+        mma_bf16(tmem + TM_S, dadd(ak, k * 2048), dadd(bu2, k * 2048), id, k > 0);
+}
+
+// carry: [T_U U; P U] = [T_U; P] U over the tokens
+__device__ __forceinline__ void issue_carry2(uint32_t tmem, uint32_t st, uint32_t u_tile) {
+    constexpr uint32_t id = idesc_bf16(128, 64, false, true);
+    const uint64_t ap = smem_desc_sw128(st + OFF_TU, 16, 1024);
+    const uint64_t bu = smem_desc_sw128(u_tile, 8192, 1024);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) mma_bf16(tmem + TM_B, dadd(ap, k * 32), dadd(bu, k * 2048), id, k > 0);
 }
 
 // ---------------------------------------------------------------- the prep kernel
@@ -442,7 +454,7 @@ __device__ __forceinline__ void issue_carry23(uint32_t tmem, uint32_t st, uint32
 // builds the decay tables from g and beta, and issues the two MMAs; warps 1..8 turn the
 // Gram matrices into P and A, solve (I+A)^-1 in 16x16 blocks, write T_U, T_W and P as
 // bf16 tiles, read W back from TMEM, and store T_U | P | W to the workspace.
-__global__ void __launch_bounds__(PREP_THREADS, 2)
+__global__ void __launch_bounds__(PREP_THREADS, 3)
     prep_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                    TcArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -454,8 +466,13 @@ __global__ void __launch_bounds__(PREP_THREADS, 2)
     uint32_t* misc = reinterpret_cast<uint32_t*>(sm + P_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
     PrepScalars& sc = *reinterpret_cast<PrepScalars*>(sm + P_SCAL);
-    float* Ab = reinterpret_cast<float*>(sm + P_AB);
     float* Tb = reinterpret_cast<float*>(sm + P_TB);
+    // fp32 block (i, j) of A, in the Q slots
+    auto Ablk = [&](int i, int j) -> float* {
+        const int x = bidx(i, j);
+        return reinterpret_cast<float*>(sm + (x < 6 ? PQ_Q : PQ_STRIDE + PQ_Q)) +
+               (x < 6 ? x : x - 6) * 16 * BS;
+    };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -463,10 +480,28 @@ __global__ void __launch_bounds__(PREP_THREADS, 2)
     const int S = a.S;
     const int nch = (S + C - 1) / C;
 
+    const int zq = b * a.Hk + kh, zv = b * a.Hv + h;
+    // g and beta of the chunk are loaded first and the copies of Q and K started at
+    // once, so that their latency overlaps the setup (padding tokens: g = beta = 0,
+    // an exact no-op)
+    float x0 = 0.f, x1 = 0.f, be0 = 0.f, be1 = 0.f;
+    if (warp == 0) {
+        const float* gp = a.g + (size_t)zv * S;
+        const float* bp = a.beta + (size_t)zv * S;
+        const int t0 = c * C + lane, t1 = t0 + 32;
+        if (t0 < S) x0 = gp[t0], be0 = bp[t0];
+        if (t1 < S) x1 = gp[t1], be1 = bp[t1];
+    }
     if (tid == 0) {
         for (int i = 0; i < PB_COUNT; ++i) mbar_init(&bar[i], i == PB_FULL ? 2 : 1);
         *abort_flag = 0;
         fence_mbar_init();
+        mbar_arrive_expect_tx(&bar[PB_FULL], 2 * 16384);
+        for (int blk = 0; blk < 2; ++blk) {
+            tma_load_3d(sm + blk * PQ_STRIDE + PQ_Q, &mq, &bar[PB_FULL], blk * 64, c * C, zq);
+            tma_load_3d(sm + blk * PQ_STRIDE + PQ_K, &mk, &bar[PB_FULL], blk * 64, c * C, zq);
+        }
+        TRACE_PREP(20);
     }
     if (warp == 0) {
         tmem_alloc(misc, PT_COLS);
@@ -482,24 +517,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2)
     const uint32_t tmem = misc[0];
 
     if (warp == 0) {
-        // -------------------------------------------- loads, decay tables, MMA issue
-        const int zq = b * a.Hk + kh, zv = b * a.Hv + h;
-        if (lane == 0) {
-            prefetch_tensormap(&mq);
-            prefetch_tensormap(&mk);
-            mbar_arrive_expect_tx(&bar[PB_FULL], 2 * 16384);
-            for (int blk = 0; blk < 2; ++blk) {
-                tma_load_3d(sm + blk * PQ_STRIDE + PQ_Q, &mq, &bar[PB_FULL], blk * 64, c * C, zq);
-                tma_load_3d(sm + blk * PQ_STRIDE + PQ_K, &mk, &bar[PB_FULL], blk * 64, c * C, zq);
-            }
-            TRACE_PREP(20);
-        }
-        // decay tables (padding tokens: g = beta = 0, an exact no-op)
-        const float* gp = a.g + (size_t)zv * S;
-        const float* bp = a.beta + (size_t)zv * S;
-        const int t0 = c * C + lane, t1 = t0 + 32;
-        float x0 = (t0 < S) ? gp[t0] : 0.f, x1 = (t1 < S) ? gp[t1] : 0.f;
-        const float be0 = (t0 < S) ? bp[t0] : 0.f, be1 = (t1 < S) ? bp[t1] : 0.f;
+        // -------------------------------------------- decay tables, MMA issue
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
             const float y0 = __shfl_up_sync(0xffffffffu, x0, off);
@@ -510,8 +528,13 @@ __global__ void __launch_bounds__(PREP_THREADS, 2)
             }
         }
         x1 += __shfl_sync(0xffffffffu, x0, 31);
+        const float gl = __shfl_sync(0xffffffffu, x1, 31);
         const float e0 = __shfl_sync(0xffffffffu, x0, lane | 15);
         const float e1 = __shfl_sync(0xffffffffu, x1, lane | 15);
+        CarryScalars& cs = *reinterpret_cast<CarryScalars*>(sm + P_CS);
+        cs.kdec[lane] = __expf(gl - x0);
+        cs.kdec[lane + 32] = __expf(gl - x1);
+        if (lane == 31) cs.Gl = __expf(gl);
         sc.gam[lane] = x0;
         sc.gam[lane + 32] = x1;
         sc.beta[lane] = be0;
@@ -520,6 +543,8 @@ __global__ void __launch_bounds__(PREP_THREADS, 2)
         sc.ctab[lane + 32] = __expf(e1 - x1);
         sc.Gam[lane] = __expf(x0);
         sc.Gam[lane + 32] = __expf(x1);
+        cs.Gam[lane] = sc.Gam[lane];
+        cs.Gam[lane + 32] = sc.Gam[lane + 32];
         if (lane == 15) {
             sc.endgam[0] = x0;
             sc.endgam[2] = x1;
@@ -528,6 +553,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2)
             sc.endgam[1] = x0;
             sc.endgam[3] = x1;
         }
+        fence_proxy_async_smem();  // the scalar staging is stored by a bulk copy
         __syncwarp();
         if (lane == 0) {
             mbar_arrive(&bar[PB_FULL]);  // the tables are written
@@ -605,12 +631,13 @@ __global__ void __launch_bounds__(PREP_THREADS, 2)
                                      pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]),
                                      pack_bf16(v[6], v[7]));
                     } else if (bj <= br) {
-                        float* dst = Ab + bidx(br, bj) * 16 * BS + rl * BS + 8 * wg;
+                        float* dst = Ablk(br, bj) + rl * BS + 8 * wg;
                         *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
                         *reinterpret_cast<float4*>(dst + 4) = make_float4(v[4], v[5], v[6], v[7]);
                     }
                 }
             }
+            tc_fence_before();  // the Gram columns are reused by the W MMA
             bar_sync(2, 256);
             if (P == 0) TRACE_PREP(24);
 
@@ -621,7 +648,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2)
             // accumulate at every step.
             {
                 const int i = P >> 6, cc = (P >> 2) & 15, rq = P & 3;
-                const float* Ad = Ab + bidx(i, i) * 16 * BS + 4 * rq * BS;
+                const float* Ad = Ablk(i, i) + 4 * rq * BS;
                 float acc[4] = {0.f, 0.f, 0.f, 0.f}, xr[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int m = 0; m < 16; ++m) {
@@ -649,7 +676,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2)
             if (pw < 4) {
                 const int i = (pw & 2) ? 3 : 1, j = i - 1, nt = pw & 1;
                 float x[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
-                block_mma(x, Ab + bidx(i, j) * 16 * BS, Tb + bidx(j, j) * 16 * BS, nt, g8, t4);
+                block_mma(x, Ablk(i, j), Tb + bidx(j, j) * 16 * BS, nt, g8, t4);
                 uint32_t bx[2][2];
                 c_to_b(x, g8, t4, bx);
                 block_mma_b(e, Tb + bidx(i, i) * 16 * BS, bx, g8, t4);
@@ -666,10 +693,10 @@ __global__ void __launch_bounds__(PREP_THREADS, 2)
                 float x2[4] = {0.f, 0.f, 0.f, 0.f}, x3[4] = {0.f, 0.f, 0.f, 0.f};
                 float e[4] = {0.f, 0.f, 0.f, 0.f};
                 for (int m = j; m < 2; ++m) {
-                    block_mma(x2, Ab + bidx(2, m) * 16 * BS, Tb + bidx(m, j) * 16 * BS, nt, g8,
+                    block_mma(x2, Ablk(2, m), Tb + bidx(m, j) * 16 * BS, nt, g8,
                               t4);
                     if (i == 3)
-                        block_mma(x3, Ab + bidx(3, m) * 16 * BS, Tb + bidx(m, j) * 16 * BS, nt,
+                        block_mma(x3, Ablk(3, m), Tb + bidx(m, j) * 16 * BS, nt,
                                   g8, t4);
                 }
                 uint32_t bx[2][2];
@@ -699,17 +726,19 @@ __global__ void __launch_bounds__(PREP_THREADS, 2)
                     for (int hh = 0; hh < 2; ++hh) {
                         float w[32];
                         tmem_ld32(tmem + lane_off + PT_W + 64 * hc + 32 * hh, w);
-                        write_row32(sb + P_W + 8192 * hc, L, 4 * hh, w);
+                        write_row32(sb + PQ_STRIDE * hc + PQ_Q, L, 4 * hh, w);
                     }
                 }
                 fence_proxy_async_smem();
                 bar_sync(2, 256);
                 if (P == 0) {
                     TRACE_PREP(28);
-                    // T_U, then P | W (adjacent here and in the workspace)
                     uint8_t* ws = a.ws + ws_offset(b, h, c, a.Hv, nch);
                     bulk_s2g(ws + WS_TU, sb + P_TU, 8192);
-                    bulk_s2g(ws + WS_P, sb + P_P, 8192 + 16384);
+                    bulk_s2g(ws + WS_P, sb + P_P, 8192);
+                    bulk_s2g(ws + WS_W, sb + PQ_Q, 8192);
+                    bulk_s2g(ws + WS_W + 8192, sb + PQ_STRIDE + PQ_Q, 8192);
+                    bulk_s2g(ws + WS_CS, sb + P_CS, sizeof(CarryScalars));
                     bulk_commit();
                     bulk_wait_all();
                 }
@@ -729,10 +758,8 @@ __global__ void __launch_bounds__(PREP_THREADS, 2)
 // ---------------------------------------------------------------- the carry kernel
 
 // One CTA per (64-column state slice, value head h, batch b), sequential over chunks.
-// Warp 0 streams q, k, v and the prep's tiles of each chunk into a two-stage ring and
-// writes the chunk's decay scalars; warp 1 issues U~ = T_U V once the chunk has landed
-// and U~(c-1) has been consumed; warps 2..5 (one per TMEM lane quadrant, thread = state
-// row) issue the S0-dependent MMAs themselves and do U, the output and the state update.
+// Warp 0 streams q, k, v, the prep's tiles and the decay scalars of each chunk into a
+// two-stage ring; warp 1 issues the MMAs; warps 2..9 form U, the output and the state.
 __global__ void __launch_bounds__(CARRY_THREADS, 1)
     carry_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                     const __grid_constant__ CUtensorMap mv, TcArgs a) {
@@ -752,7 +779,7 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
 
     if (tid == 0) {
         for (int i = 0; i < B_COUNT; ++i)
-            mbar_init(&bar[i], (i == B_FULL0 || i == B_FULL1) ? 2 : 1);
+            mbar_init(&bar[i], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -771,30 +798,22 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
     const uint32_t tmem = misc[0];
 
     if (warp == 0) {
-        // ------------------------------------------ loads + decay scalars (warp)
-        const int zq = b * a.Hk + kh, zv = b * a.Hv + h;
-        const float* gp = a.g + (size_t)zv * S;
-        const uint8_t* wsh = a.ws + ws_offset(b, h, 0, a.Hv, nch);
-        int issued = 0;
-        float ng0, ng1;  // g of the next chunk, loaded one iteration ahead
-        ng0 = (lane < S) ? gp[lane] : 0.f;
-        ng1 = (lane + 32 < S) ? gp[lane + 32] : 0.f;
-        for (int c = 0; c < nch; ++c) {
-            const int s = c & 1;
-            int ok = 1;
-            if (lane == 0) {
+        // ------------------------------------------------- loads (one thread)
+        if (lane == 0) {
+            const int zq = b * a.Hk + kh, zv = b * a.Hv + h;
+            const uint8_t* wsh = a.ws + ws_offset(b, h, 0, a.Hv, nch);
+            int issued = 0;
+            for (int c = 0; c < nch; ++c) {
+                const int s = c & 1;
                 if (c >= 2 && !wait_or_abort(&bar[B_EMPTY0 + s], ((c >> 1) + 1) & 1, abort_flag,
                                              ST_PRODUCER))
-                    ok = 0;
-                if (*abort_flag) ok = 0;
-            }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            if (lane == 0) {
+                    break;
+                if (*abort_flag) break;
                 uint8_t* st = sm + s * STAGE_BYTES;
                 const uint8_t* wsc = wsh + (size_t)c * WS_UNIT;
                 TRACE(c, 0);
-                mbar_arrive_expect_tx(&bar[B_FULL0 + s], 2 * 16384 + 8192 + WS_UNIT);
+                mbar_arrive_expect_tx(&bar[B_FULL0 + s],
+                                      2 * 16384 + 8192 + 32768 + (uint32_t)sizeof(CarryScalars));
                 for (int blk = 0; blk < 2; ++blk) {
                     tma_load_3d(st + blk * BLK_STRIDE + OFF_Q, &mq, &bar[B_FULL0 + s], blk * 64,
                                 c * C, zq);
@@ -805,6 +824,9 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
                 }
                 tma_load_3d(st + OFF_V, &mv, &bar[B_FULL0 + s], n0, c * C, zv);
                 bulk_g2s(st + OFF_TU, wsc + WS_TU, 16384, &bar[B_FULL0 + s]);  // T_U | P
+                bulk_g2s(&scal[s], wsc + WS_CS, sizeof(CarryScalars), &bar[B_FULL0 + s]);
+                TRACE(c, 7);
+                issued = c + 1;
                 // chunk c + 2 goes to L2 now; its copy is issued once this stage is free
                 if (c + 2 < nch) {
                     for (int blk = 0; blk < 2; ++blk) {
@@ -815,76 +837,37 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
                     bulk_prefetch_l2(wsc + 2 * WS_UNIT, WS_UNIT);
                 }
             }
-            issued = c + 1;
-            // decay scalars of chunk c (padding tokens: g = 0)
-            CarryScalars& sc = scal[s];
-            float x0 = ng0, x1 = ng1;
-            {
-                const int t0 = (c + 1) * C + lane, t1 = t0 + 32;
-                ng0 = (t0 < S) ? gp[t0] : 0.f;
-                ng1 = (t1 < S) ? gp[t1] : 0.f;
-            }
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float y0 = __shfl_up_sync(0xffffffffu, x0, off);
-                const float y1 = __shfl_up_sync(0xffffffffu, x1, off);
-                if (lane >= off) {
-                    x0 += y0;
-                    x1 += y1;
-                }
-            }
-            x1 += __shfl_sync(0xffffffffu, x0, 31);
-            const float gl = __shfl_sync(0xffffffffu, x1, 31);
-            sc.Gam[lane] = __expf(x0);
-            sc.Gam[lane + 32] = __expf(x1);
-            sc.kdec[lane] = __expf(gl - x0);
-            sc.kdec[lane + 32] = __expf(gl - x1);
-            if (lane == 31) sc.Gl = __expf(gl);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar[B_FULL0 + s]);
-        }
-        if (lane == 0 && *abort_flag) {
-            // let the copies already issued land before the CTA exits
-            for (int c = (issued > 2 ? issued - 2 : 0); c < issued; ++c)
-                mbar_wait_bounded(&bar[B_FULL0 + (c & 1)], (c >> 1) & 1, kWaitNs);
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------------ U~ issuer (one thread)
-        if (lane == 0) {
-            int c = 0;
-            for (; c < nch; ++c) {
-                const bool ok =
-                    wait_or_abort(&bar[B_FULL0 + (c & 1)], (c >> 1) & 1, abort_flag, ST_MMA) &&
-                    (c == 0 || wait_or_abort(&bar[B_UFREE], (c - 1) & 1, abort_flag, ST_MMA));
-                if (!ok) break;
-                tc_fence_after();
-                issue_u(tmem, sbase + (c & 1) * STAGE_BYTES);
-                tc_commit(&bar[B_UDONE]);
-                TRACE(c, 2);
-            }
-            if (c > 0) {
-                // no MMA of this thread may be in flight when TMEM is freed
-                tc_commit(&bar[B_DRAIN_U]);
-                mbar_wait_bounded(&bar[B_DRAIN_U], 0, kWaitNs);
+            if (*abort_flag) {
+                // let the copies already issued land before the CTA exits
+                for (int c = (issued > 2 ? issued - 2 : 0); c < issued; ++c)
+                    mbar_wait_bounded(&bar[B_FULL0 + (c & 1)], (c >> 1) & 1, kWaitNs);
             }
         }
     } else {
-        // ------------------------------------------------------------ carry (128 threads)
-        const int q = warp & 3;
-        const int L = 32 * q + lane;  // TMEM lane = state row (Dk index) = token for L < 64
-        const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+        // ------------------------------------------------- carry (warps 1..9, 288 threads)
+        // Warp 1, lane 0 issues every MMA of the carry: MMA1 [W; Q] S0 of chunk c and
+        // U~ = [T_U; P] V of chunk c+1 (which runs while U of chunk c is formed), then
+        // K^T U' and P U of chunk c (P U runs while the state is updated).
+        // Warps 2..9: two per TMEM lane quadrant; thread = state row L (Dk index; token L
+        // for L < 64, token L - 64 of the Q S0 / P U halves for L >= 64), 32 state columns
+        // (half hc of the CTA's 64). Quadrants 0-1 form U of chunk c while quadrants 2-3
+        // write the output of chunk c-1; then all update the state.
+        const bool issuer = warp == 1;
+        const bool leader = issuer && lane == 0;
+        const int q = warp & 3, hc = issuer ? 0 : (warp - 2) >> 2;
+        const int L = 32 * q + lane;
+        const uint32_t lane_off = ((uint32_t)(32 * q) << 16) + 32u * (uint32_t)hc;
         const uint32_t s_tile = sbase + OFF_S, u_tile = sbase + OFF_U, u2_tile = sbase + OFF_U2;
-        float* gstate = a.state + ((size_t)(b * a.Hv + h) * 128 + L) * 128 + n0;
-        __nv_bfloat16* gout = a.out + (size_t)(b * a.Hv + h) * S * 128 + n0;
+        float* gstate = a.state + ((size_t)(b * a.Hv + h) * 128 + L) * 128 + n0 + 32 * hc;
+        __nv_bfloat16* gout = a.out + (size_t)(b * a.Hv + h) * S * 128 + n0 + 32 * hc;
 
-        // the fp32 state lives in TMEM (columns TM_SS), its bf16 copy in the S tile
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
+        if (!issuer) {
+            // the fp32 state lives in TMEM (columns TM_SS), its bf16 copy in the S tile
             float Sm[32];
             if (a.state_is_input) {
 #pragma unroll
                 for (int j = 0; j < 32; j += 4) {
-                    const float4 x = *reinterpret_cast<const float4*>(gstate + 32 * hh + j);
+                    const float4 x = *reinterpret_cast<const float4*>(gstate + j);
                     Sm[j] = x.x;
                     Sm[j + 1] = x.y;
                     Sm[j + 2] = x.z;
@@ -894,131 +877,168 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
 #pragma unroll
                 for (int j = 0; j < 32; ++j) Sm[j] = 0.f;
             }
-            tmem_st32(tmem + lane_off + TM_SS + 32 * hh, Sm);
-            write_row32(s_tile, L, 4 * hh, Sm);
+            tmem_st32(tmem + lane_off + TM_SS, Sm);
+            write_row32(s_tile, L, 4 * hc, Sm);
+            tmem_wait_st();
+            fence_proxy_async_smem();
         }
-        tmem_wait_st();
-        fence_proxy_async_smem();
         tc_fence_before();
-        bar_sync(1, 128);
 
-        int mmas = 0;
+        // O = scale (Gamma Q S0 + P U) of chunk cc for token L - 64 (quadrants 2, 3)
+        auto write_out = [&](int cc, float gm) {
+            const int t = cc * C + (L - 64);
+            const uint32_t ta = TM_A + 64u * (uint32_t)(cc & 1);
+#pragma unroll
+            for (int qq = 0; qq < 2; ++qq) {
+                float qs[16], pu[16];
+                tmem_ld16x2(tmem + lane_off + ta + 16 * qq, tmem + lane_off + TM_B + 16 * qq, qs,
+                            pu);
+                if (t < S) {
+                    uint4* dst = reinterpret_cast<uint4*>(gout + (size_t)t * 128 + 16 * qq);
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        float o[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            o[e] = a.scale * fmaf(gm, qs[8 * j + e], pu[8 * j + e]);
+                        uint4 w;
+                        w.x = pack_bf16(o[0], o[1]);
+                        w.y = pack_bf16(o[2], o[3]);
+                        w.z = pack_bf16(o[4], o[5]);
+                        w.w = pack_bf16(o[6], o[7]);
+                        dst[j] = w;
+                    }
+                }
+            }
+        };
+
+        int mmas = 0, done = 0;
+        bool landed = true;   // leader: chunk c has landed and U~(c) is issued
+        float gm_prev = 0.f;  // Gamma of the previous chunk's token L - 64
+        if (leader) {
+            landed = wait_or_abort(&bar[B_FULL0], 0, abort_flag, ST_MMA);
+            if (landed) {
+                tc_fence_after();
+                issue_u(tmem, sbase, TM_U);
+                mmas = 1;
+            }
+        }
         for (int c = 0; c < nch; ++c) {
             const int s = c & 1;
             const uint32_t st = sbase + s * STAGE_BYTES;
-            // MMA1: [W; Q] S0 once the chunk has landed (the state tile is current)
-            bool ok = wait_or_abort(&bar[B_FULL0 + s], (c >> 1) & 1, abort_flag, ST_CARRY);
-            if (bar_any(1, 128, !ok || *abort_flag)) break;
-            if (L == 0) {
+            // the state tile is complete: MMA1 [W; Q] S0
+            if (bar_any(1, 288, !landed || *abort_flag)) break;
+            if (leader) {
                 TRACE(c, 12);
                 tc_fence_after();
-                issue_carry1(tmem, st, s_tile);
-                tc_commit(&bar[B_ADONE]);
-                mmas = 1;
+                issue_carry1(tmem, st, s_tile, TM_A + 64u * (uint32_t)s);
+                tc_commit(&bar[B_ADONE]);  // also covers U~(c), issued earlier
                 TRACE(c, 3);
-            }
-            ok = wait_or_abort(&bar[B_ADONE], c & 1, abort_flag, ST_CARRY) &&
-                 wait_or_abort(&bar[B_UDONE], c & 1, abort_flag, ST_CARRY);
-            if (bar_any(1, 128, !ok || *abort_flag)) break;
-            if (L == 0) TRACE(c, 13);
-            tc_fence_after();
-            // per-chunk scalars are read now: the producer may rewrite this stage's
-            // scalars once the chunk's last MMAs complete
-            const float Gl = scal[s].Gl;
-            float gm = 0.f;
-            if (L < 64) {
-                // U = U~ - W S0 and U' = exp(gamma_last - gamma_L) U for token L
-                const float kd = scal[s].kdec[L];
-#pragma unroll
-                for (int qq = 0; qq < 4; ++qq) {
-                    float ws[16], ut[16];
-                    tmem_ld16x2(tmem + lane_off + TM_A + 16 * qq, tmem + lane_off + TM_U + 16 * qq,
-                                ws, ut);
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) ut[j] -= ws[j];
-                    write_row16(u_tile, L, 2 * qq, ut);
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) ut[j] *= kd;
-                    write_row16(u2_tile, L, 2 * qq, ut);
+                if (c + 1 < nch) {
+                    landed = wait_or_abort(&bar[B_FULL0 + (s ^ 1)], ((c + 1) >> 1) & 1, abort_flag,
+                                           ST_MMA);
+                    if (landed) {
+                        issue_u(tmem, sbase + (s ^ 1) * STAGE_BYTES, TM_U + 64u * (uint32_t)(s ^ 1));
+                        TRACE(c + 1, 5);
+                    }
                 }
-            } else {
-                gm = scal[s].Gam[L - 64];
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            bar_sync(1, 128);
-            if (L == 0) {
+            bool ok = true;
+            if (!issuer) {
+                // P U of chunk c-1 must be complete before the U tile is rewritten and
+                // before its output is read
+                ok = c == 0 || wait_or_abort(&bar[B_CDONE], (c - 1) & 1, abort_flag, ST_CARRY);
+                if (q >= 2) {
+                    if (ok && c > 0) {
+                        tc_fence_after();
+                        write_out(c - 1, gm_prev);
+                    }
+                    // per-chunk scalars are read now: the producer may rewrite this stage's
+                    // scalars once the chunk's last MMAs complete
+                    gm_prev = scal[s].Gam[L - 64];
+                } else {
+                    ok = ok && wait_or_abort(&bar[B_ADONE], c & 1, abort_flag, ST_CARRY);
+                    if (ok) {
+                        if (warp == 4 && lane == 0) TRACE(c, 13);
+                        tc_fence_after();
+                        // U = U~ - W S0 and U' = exp(gamma_last - gamma_L) U for token L
+                        const float kd = scal[s].kdec[L];
+#pragma unroll
+                        for (int qq = 0; qq < 2; ++qq) {
+                            float ws[16], ut[16];
+                            tmem_ld16x2(tmem + lane_off + TM_A + 64u * (uint32_t)s + 16 * qq,
+                                        tmem + lane_off + TM_U + 64u * (uint32_t)s + 16 * qq, ws,
+                                        ut);
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) ut[j] -= ws[j];
+                            write_row16(u_tile, L, 4 * hc + 2 * qq, ut);
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) ut[j] *= kd;
+                            write_row16(u2_tile, L, 4 * hc + 2 * qq, ut);
+                        }
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+            }
+            const float Gl = scal[s].Gl;
+            if (bar_any(1, 288, !ok || *abort_flag)) break;
+            if (leader) {
                 TRACE(c, 14);
-                mbar_arrive(&bar[B_UFREE]);  // U~(c) consumed: U~(c + 1) may overwrite it
                 tc_fence_after();
-                issue_carry23(tmem, st, u_tile, u2_tile);
+                issue_carry3(tmem, st, u2_tile);
+                tc_commit(&bar[B_SDONE]);
+                issue_carry2(tmem, st, u_tile);
                 tc_commit(&bar[B_CDONE]);
                 tc_commit(&bar[B_EMPTY0 + s]);
                 TRACE(c, 4);
             }
-            ok = wait_or_abort(&bar[B_CDONE], c & 1, abort_flag, ST_CARRY);
-            if (bar_any(1, 128, !ok || *abort_flag)) break;
-            if (L == 0) TRACE(c, 15);
-            tc_fence_after();
-            if (L >= 64) {
-                // O = scale (Gamma Q S0 + P U) for token L - 64
-                const int t = c * C + (L - 64);
+            if (!issuer) {
+                // S1 = Gamma_last S0 + K^T U' for state row L
+                ok = wait_or_abort(&bar[B_SDONE], c & 1, abort_flag, ST_CARRY);
+                if (ok) {
+                    if (warp == 2 && lane == 0) TRACE(c, 15);
+                    tc_fence_after();
 #pragma unroll
-                for (int qq = 0; qq < 4; ++qq) {
-                    float qs[16], pu[16];
-                    tmem_ld16x2(tmem + lane_off + TM_A + 16 * qq, tmem + lane_off + TM_B + 16 * qq,
-                                qs, pu);
-                    if (t < S) {
-                        uint4* dst = reinterpret_cast<uint4*>(gout + (size_t)t * 128 + 16 * qq);
+                    for (int qq = 0; qq < 2; ++qq) {
+                        float d[16], sv[16];
+                        tmem_ld16x2(tmem + lane_off + TM_S + 16 * qq,
+                                    tmem + lane_off + TM_SS + 16 * qq, d, sv);
 #pragma unroll
-                        for (int j = 0; j < 2; ++j) {
-                            float o[8];
-#pragma unroll
-                            for (int e = 0; e < 8; ++e)
-                                o[e] = a.scale * fmaf(gm, qs[8 * j + e], pu[8 * j + e]);
-                            uint4 w;
-                            w.x = pack_bf16(o[0], o[1]);
-                            w.y = pack_bf16(o[2], o[3]);
-                            w.z = pack_bf16(o[4], o[5]);
-                            w.w = pack_bf16(o[6], o[7]);
-                            dst[j] = w;
-                        }
+                        for (int j = 0; j < 16; ++j) sv[j] = fmaf(Gl, sv[j], d[j]);
+                        tmem_st16(tmem + lane_off + TM_SS + 16 * qq, sv);
+                        write_row16(s_tile, L, 4 * hc + 2 * qq, sv);
                     }
+                    tmem_wait_st();
+                    fence_proxy_async_smem();
+                    if (warp == 2 && lane == 0) TRACE(c, 16);
                 }
+                tc_fence_before();
             }
-            // S1 = Gamma_last S0 + K^T U' for state row L
-#pragma unroll
-            for (int qq = 0; qq < 4; ++qq) {
-                float d[16], sv[16];
-                tmem_ld16x2(tmem + lane_off + TM_S + 16 * qq, tmem + lane_off + TM_SS + 16 * qq, d,
-                            sv);
-#pragma unroll
-                for (int j = 0; j < 16; ++j) sv[j] = fmaf(Gl, sv[j], d[j]);
-                tmem_st16(tmem + lane_off + TM_SS + 16 * qq, sv);
-                write_row16(s_tile, L, 2 * qq, sv);
-            }
-            tmem_wait_st();
-            fence_proxy_async_smem();
-            tc_fence_before();
-            bar_sync(1, 128);
-            if (L == 0) TRACE(c, 16);
+            done = c + 1;
         }
-        if (!*abort_flag) {
-            tc_fence_after();
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                float Sm[32];
-                tmem_ld32(tmem + lane_off + TM_SS + 32 * hh, Sm);
-#pragma unroll
-                for (int j = 0; j < 32; j += 4)
-                    *reinterpret_cast<float4*>(gstate + 32 * hh + j) =
-                        make_float4(Sm[j], Sm[j + 1], Sm[j + 2], Sm[j + 3]);
+        bool ok = !bar_any(1, 288, done < nch || *abort_flag);
+        if (ok && !issuer && q >= 2) {
+            // the output of the last chunk
+            ok = wait_or_abort(&bar[B_CDONE], (nch - 1) & 1, abort_flag, ST_CARRY);
+            if (ok) {
+                tc_fence_after();
+                write_out(nch - 1, gm_prev);
             }
+        }
+        if (ok && !issuer) {
+            tc_fence_after();
+            float Sm[32];
+            tmem_ld32(tmem + lane_off + TM_SS, Sm);
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<float4*>(gstate + j) =
+                    make_float4(Sm[j], Sm[j + 1], Sm[j + 2], Sm[j + 3]);
         }
         // no MMA of the carry may be in flight when TMEM is freed
-        if (L == 0 && mmas && *abort_flag) {
-            tc_commit(&bar[B_DRAIN_C]);
-            mbar_wait_bounded(&bar[B_DRAIN_C], 0, kWaitNs);
+        if (leader && mmas) {
+            tc_commit(&bar[B_DRAIN]);
+            mbar_wait_bounded(&bar[B_DRAIN], 0, kWaitNs);
         }
     }
 

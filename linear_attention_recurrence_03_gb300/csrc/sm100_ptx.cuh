@@ -53,17 +53,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity);
-
 // As mbar_try_wait, but lets the hardware suspend the thread for up to ~1 ms while the
 // phase is incomplete (it resumes as soon as the phase completes), so waiting warps do
 // not take issue slots from working warps of the same SM sub-partition.
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
-#if defined(GDN_WAIT_MODE) && GDN_WAIT_MODE == 1
-    return mbar_try_wait(bar, parity);
-#elif defined(GDN_WAIT_MODE) && GDN_WAIT_MODE == 2
-    return mbar_test_wait(bar, parity);
-#endif
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
