@@ -88,17 +88,15 @@ namespace {
 using namespace ptx;
 
 constexpr int C = 64;    // chunk length
-constexpr int NS = 64;   // state columns per carry CTA
 constexpr uint64_t kWaitNs = 2000000000ull;
 
-// ---- workspace: per (batch, value head, chunk) unit, four bf16 tiles of 64 rows x 64
-// columns in the 128-byte swizzled layout, T_U | P | W[:, 0:64] | W[:, 64:128], then
-// the carry's decay scalars of the chunk (CarryScalars)
-constexpr uint32_t WS_UNIT = 33792;
-constexpr uint32_t WS_TU = 0, WS_P = 8192, WS_W = 16384, WS_CS = 32768;
+// ---- workspace: per (batch, value head, chunk) unit, six bf16 tiles of 64 rows x 64
+// columns in the 128-byte swizzled layout, T_U | P | W[:, 0:64] | W[:, 64:128] |
+// Q~[:, 0:64] | Q~[:, 64:128] with Q~ = diag(Gamma) Q, then the carry's decay scalars
+constexpr uint32_t WS_UNIT = 50176;
+constexpr uint32_t WS_TU = 0, WS_P = 8192, WS_W = 16384, WS_QT = 32768, WS_CS = 49152;
 
 struct CarryScalars {
-    float Gam[C];   // exp(gamma_r)
     float kdec[C];  // exp(gamma_last - gamma_r)
     float Gl;       // exp(gamma_last)
     float pad[3];
@@ -145,39 +143,50 @@ constexpr uint32_t PT_COLS = 128;
 
 enum { PB_FULL = 0, PB_GRAM, PB_PREP, PB_WDONE, PB_DRAIN, PB_COUNT };
 
-// ---- carry kernel: shared memory map
-//   stage s (two stages, one chunk each):
-//     block b: W_b | Q_b | K_b (8 KB each, stride 24 KB)  ([W_b; Q_b] is one operand)
-//     V slice (64 tokens x 64 columns), T_U, P            ([T_U; P] is one operand)
-//   U, U' tiles, the bf16 state operand, per-stage scalars, barriers
-constexpr int CARRY_THREADS = 320;  // warp 0: producer; warp 1: MMA issuer; 2..9: carry
+// ---- carry kernel: one CTA per (NS-column slice of the state, value head, batch), NS = 64
+// or 128 (CarryCfg<NS>). Shared memory map:
+//   stage s (two stages, one chunk each), in two copy groups:
+//     block b (Dk columns 64b..64b+63): W_b | Q~_b | K_b (8 KB each, stride 24 KB)
+//       ([W_b; Q~_b] is one 128-row operand), then P ([K_1; P] one operand),
+//     V slice (64 tokens x NS columns, in 64-column blocks), T_U ([T_U; -] one operand)
+//     early group (read by U~ and [W; Q~] S0, freed as soon as they complete): W, Q~, V,
+//     T_U and the scalars; late group (read by K^T U' and P U): K and P
+//   U and U' tiles (64 tokens x NS), the bf16 state operand (128 x NS, 64-column blocks),
+//   per-stage scalars, barriers
+// warp 0: producer; warp 2: MMA issuer (an SM sub-partition whose SIMT warps only write the
+// output); warps 4..11: SIMT; warps 1 and 3 only take part in the setup and the teardown
+constexpr int CARRY_THREADS = 384;
 constexpr uint32_t BLK_STRIDE = 24576;
 constexpr uint32_t OFF_W = 0, OFF_Q = 8192, OFF_K = 16384;
-constexpr uint32_t OFF_V = 49152, OFF_TU = 57344, OFF_P = 65536;
-constexpr uint32_t STAGE_BYTES = 73728;
-static_assert(OFF_P == OFF_TU + 8192, "[T_U; P] is one 128-row operand");
-constexpr uint32_t OFF_U = 2 * STAGE_BYTES;  // U tile  (64 tokens x 64 columns)
-constexpr uint32_t OFF_U2 = OFF_U + 8192;    // U' tile (decayed U)
-constexpr uint32_t OFF_S = OFF_U2 + 8192;    // bf16 state operand (128 x 64)
-constexpr uint32_t OFF_SCAL = OFF_S + 16384;
+constexpr uint32_t OFF_P = 49152, OFF_V = 57344;
+static_assert(OFF_P == BLK_STRIDE + OFF_K + 8192, "[K_1; P] is one 128-row operand");
 
-constexpr uint32_t OFF_BAR = OFF_SCAL + 2 * sizeof(CarryScalars);
-constexpr uint32_t OFF_MISC = OFF_BAR + 128;
-constexpr uint32_t CARRY_SMEM = OFF_MISC + 64 + 1024;
-static_assert(OFF_BAR % 8 == 0, "barrier alignment");
-static_assert(CARRY_SMEM <= 232448, "shared memory budget");
+template <int NS>
+struct CarryCfg {
+    static constexpr int NB = NS / 64;    // 64-column blocks of the slice
+    static constexpr int CPT = NS / 2;    // state columns per SIMT thread
+    static constexpr uint32_t OFF_TU = OFF_V + 8192u * NB;
+    static constexpr uint32_t STAGE = OFF_TU + 8192u;
+    static constexpr uint32_t U = 2 * STAGE;             // U tile, NB blocks of 8 KB
+    static constexpr uint32_t U2 = U + 8192u * NB;        // U' tile (decayed U)
+    static constexpr uint32_t SM_S = U2 + 8192u * NB;     // state operand, NB blocks of 16 KB
+    static constexpr uint32_t SCAL = SM_S + 16384u * NB;
+    static constexpr uint32_t BAR = SCAL + 2 * sizeof(CarryScalars);
+    static constexpr uint32_t MISC = BAR + 128;
+    static constexpr uint32_t SMEM = MISC + 64 + 1024;
+    // TMEM (fp32 columns), two buffers of each kind by chunk parity:
+    //   B[p]: U~ of the chunk (upper half), then, once U is formed, its state increment
+    //   A[p]: [W S0; Q~ S0], then [-; Q~ S0 + P U] (the un-scaled output)
+    static constexpr uint32_t TMB = 0, TMA = 2 * NS;
+    static constexpr uint32_t TMCOLS = 4 * NS;
+    static_assert(BAR % 8 == 0 && SCAL % 16 == 0, "barrier and copy alignment");
+    static_assert(SMEM <= 232448, "shared memory budget");
+};
 
-// carry TMEM columns
-// (U~ and [W S0; Q S0] have one buffer per chunk parity)
-constexpr uint32_t TM_U = 0;     // [U~; -], 2 x 64 columns
-constexpr uint32_t TM_A = 128;   // [W S0; Q S0], 2 x 64 columns
-constexpr uint32_t TM_S = 256;   // state increment, 64 columns
-constexpr uint32_t TM_B = 320;   // [-; P U], 64 columns
-constexpr uint32_t TM_SS = 384;  // the fp32 state slice (row = Dk index), 64 columns
-constexpr uint32_t TM_COLS = 512;
-
+// FULLE/EMPTYE: the early copy group of stage s; FULLL/EMPTYL: the late group
 enum {
-    B_FULL0 = 0, B_FULL1, B_EMPTY0, B_EMPTY1, B_ADONE, B_SDONE, B_CDONE, B_DRAIN, B_COUNT
+    B_FULLE0 = 0, B_FULLE1, B_FULLL0, B_FULLL1, B_EMPTYE0, B_EMPTYE1, B_EMPTYL0, B_EMPTYL1,
+    B_ADONE, B_SDONE, B_CDONE, B_DRAIN, B_COUNT
 };
 
 // status bits
@@ -252,14 +261,13 @@ __device__ __forceinline__ uint32_t sw128_chunk(uint32_t tile, int r, int ch) {
            ((uint32_t)((ch ^ r) & 7) << 4);
 }
 
-// Writes 16 fp32 values as bf16 into logical chunks ch0, ch0+1 of row r.
-__device__ __forceinline__ void write_row16(uint32_t tile, int r, int ch0, const float* v) {
+// Writes 32 bf16 values (16 packed pairs) into logical chunks ch0..ch0+3 of row r.
+__device__ __forceinline__ void write_row32_packed(uint32_t tile, int r, int ch0,
+                                                   const uint32_t* u) {
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        st_shared_v4(sw128_chunk(tile, r, ch0 + j), pack_bf16(v[8 * j + 0], v[8 * j + 1]),
-                     pack_bf16(v[8 * j + 2], v[8 * j + 3]), pack_bf16(v[8 * j + 4], v[8 * j + 5]),
-                     pack_bf16(v[8 * j + 6], v[8 * j + 7]));
-    }
+    for (int j = 0; j < 4; ++j)
+        st_shared_v4(sw128_chunk(tile, r, ch0 + j), u[4 * j], u[4 * j + 1], u[4 * j + 2],
+                     u[4 * j + 3]);
 }
 
 // Writes 32 fp32 values as bf16 into logical chunks ch0..ch0+3 of row r.
@@ -407,21 +415,24 @@ __device__ __forceinline__ void issue_w(uint32_t tmem, uint32_t sb) {
     for (int k = 0; k < 4; ++k) mma_bf16(tmem + PT_W, dadd(aw, k * 32), dadd(bk, k * 2048), id, k > 0);
 }
 
-// carry: [U~; P V] = [T_U; P] V over the 64 tokens, into the TMEM buffer `tu`
-__device__ __forceinline__ void issue_u(uint32_t tmem, uint32_t st, uint32_t tu) {
-    constexpr uint32_t id = idesc_bf16(128, 64, false, true);
-    const uint64_t au = smem_desc_sw128(st + OFF_TU, 16, 1024);
+// carry: [U~; -] = [T_U; -] V over the 64 tokens (V read N-major), into TMEM buffer `tb`
+// (the lower half of the operand is whatever follows T_U; that half of the result is unused)
+template <int NS>
+__device__ __forceinline__ void issue_u(uint32_t tmem, uint32_t st, uint32_t tb) {
+    constexpr uint32_t id = idesc_bf16(128, NS, false, true);
+    const uint64_t au = smem_desc_sw128(st + CarryCfg<NS>::OFF_TU, 16, 1024);
     const uint64_t bv = smem_desc_sw128(st + OFF_V, 8192, 1024);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) mma_bf16(tmem + tu, dadd(au, k * 32), dadd(bv, k * 2048), id, k > 0);
+    for (int k = 0; k < 4; ++k) mma_bf16(tmem + tb, dadd(au, k * 32), dadd(bv, k * 2048), id, k > 0);
 }
 
-// carry: [W S0; Q S0] = [W; Q] S0 over Dk = 128, into the TMEM buffer `ta`
+// carry: [W S0; Q~ S0] = [W; Q~] S0 over Dk = 128, into the TMEM buffer `ta`
+template <int NS>
 __device__ __forceinline__ void issue_carry1(uint32_t tmem, uint32_t st, uint32_t s_tile,
                                              uint32_t ta) {
-    constexpr uint32_t id = idesc_bf16(128, 64, false, true);
+    constexpr uint32_t id = idesc_bf16(128, NS, false, true);
     const uint64_t a0 = smem_desc_sw128(st + OFF_W, 16, 1024);
-    const uint64_t b0 = smem_desc_sw128(s_tile, 8192, 1024);
+    const uint64_t b0 = smem_desc_sw128(s_tile, 16384, 1024);
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         const uint32_t off = (uint32_t)(k >> 2) * BLK_STRIDE + (uint32_t)(k & 3) * 32u;
@@ -429,23 +440,28 @@ __device__ __forceinline__ void issue_carry1(uint32_t tmem, uint32_t st, uint32_
     }
 }
 
-// carry: the state increment K^T U' over the tokens (K read M-major)
-__device__ __forceinline__ void issue_carry3(uint32_t tmem, uint32_t st, uint32_t u2_tile) {
-    constexpr uint32_t id = idesc_bf16(128, 64, true, true);
+// carry: the state increment K^T U' over the tokens (K read M-major), into `tb`
+template <int NS>
+__device__ __forceinline__ void issue_carry3(uint32_t tmem, uint32_t st, uint32_t u2_tile,
+                                             uint32_t tb) {
+    constexpr uint32_t id = idesc_bf16(128, NS, true, true);
     const uint64_t ak = smem_desc_sw128(st + OFF_K, BLK_STRIDE, 1024);
     const uint64_t bu2 = smem_desc_sw128(u2_tile, 8192, 1024);
 #pragma unroll
     for (int k = 0; k < 4; ++k)
-        mma_bf16(tmem + TM_S, dadd(ak, k * 2048), dadd(bu2, k * 2048), id, k > 0);
+        mma_bf16(tmem + tb, dadd(ak, k * 2048), dadd(bu2, k * 2048), id, k > 0);
 }
 
-// carry: [T_U U; P U] = [T_U; P] U over the tokens
-__device__ __forceinline__ void issue_carry2(uint32_t tmem, uint32_t st, uint32_t u_tile) {
-    constexpr uint32_t id = idesc_bf16(128, 64, false, true);
-    const uint64_t ap = smem_desc_sw128(st + OFF_TU, 16, 1024);
+// carry: [K_1 U; P U] = [K_1; P] U, accumulated onto [W S0; Q~ S0] in `ta`: the lower
+// half becomes the un-scaled output Q~ S0 + P U (the upper half is no longer needed)
+template <int NS>
+__device__ __forceinline__ void issue_carry2(uint32_t tmem, uint32_t st, uint32_t u_tile,
+                                             uint32_t ta) {
+    constexpr uint32_t id = idesc_bf16(128, NS, false, true);
+    const uint64_t ap = smem_desc_sw128(st + OFF_P - 8192, 16, 1024);
     const uint64_t bu = smem_desc_sw128(u_tile, 8192, 1024);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) mma_bf16(tmem + TM_B, dadd(ap, k * 32), dadd(bu, k * 2048), id, k > 0);
+    for (int k = 0; k < 4; ++k) mma_bf16(tmem + ta, dadd(ap, k * 32), dadd(bu, k * 2048), id, 1);
 }
 
 // ---------------------------------------------------------------- the prep kernel
@@ -543,8 +559,6 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
         sc.ctab[lane + 32] = __expf(e1 - x1);
         sc.Gam[lane] = __expf(x0);
         sc.Gam[lane + 32] = __expf(x1);
-        cs.Gam[lane] = sc.Gam[lane];
-        cs.Gam[lane + 32] = sc.Gam[lane + 32];
         if (lane == 15) {
             sc.endgam[0] = x0;
             sc.endgam[2] = x1;
@@ -596,6 +610,27 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
         if (!bar_any(2, 256, !ok || *abort_flag)) {
             tc_fence_after();
             if (P == 0) TRACE_PREP(23);
+
+            // ---- Q~ = diag(Gamma) Q straight to the workspace (the Q slots are reused
+            // next); 16-byte chunk j of the two Q blocks, same swizzled position
+            {
+                uint8_t* wq = a.ws + ws_offset(b, h, c, a.Hv, nch) + WS_QT;
+#pragma unroll
+                for (int it = 0; it < 4; ++it) {
+                    const int j = P + 256 * it, blk = j >> 9, off = (j & 511) * 16;
+                    const float gmr = sc.Gam[(j & 511) >> 3];
+                    const uint4 x = *reinterpret_cast<const uint4*>(sm + blk * PQ_STRIDE + PQ_Q + off);
+                    const uint32_t in[4] = {x.x, x.y, x.z, x.w};
+                    uint32_t o[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&in[e]));
+                        o[e] = pack_bf16(f.x * gmr, f.y * gmr);
+                    }
+                    *reinterpret_cast<uint4*>(wq + blk * 8192 + off) = make_uint4(o[0], o[1], o[2], o[3]);
+                }
+            }
+            bar_sync(2, 256);  // every Q chunk is read before A overwrites the Q slots
 
             // ---- P (bf16 tile) and A (fp32 blocks) from the Gram matrices: thread (wg, L)
             // takes row L of [QK^T; KK^T], columns 16 bj + 8 wg .. + 7 of every 16-block bj
@@ -757,19 +792,26 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
 
 // ---------------------------------------------------------------- the carry kernel
 
-// One CTA per (64-column state slice, value head h, batch b), sequential over chunks.
-// Warp 0 streams q, k, v, the prep's tiles and the decay scalars of each chunk into a
-// two-stage ring; warp 1 issues the MMAs; warps 2..9 form U, the output and the state.
+// One CTA per (NS-column slice of the state, value head h, batch b), sequential over
+// chunks. Warp 0 streams the chunk's k and v slice (TMA) and the prep's tiles and scalars
+// (bulk copies) into a two-stage ring; warp 2 (one thread) issues every MMA; warps 4..11
+// (two per TMEM lane quadrant, thread = state row L, NS/2 columns) keep the fp32 state in
+// registers, form U (rows 0-63) while writing the previous chunk's output (rows 64-127),
+// and update the state. MMA order per chunk c: [W; Q~] S0, U~ of chunk c+1 if it has
+// landed, then K^T U', U~ of chunk c+1 if not issued yet, P U.
+template <int NS>
 __global__ void __launch_bounds__(CARRY_THREADS, 1)
-    carry_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
-                    const __grid_constant__ CUtensorMap mv, TcArgs a) {
+    carry_tc_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
+                    TcArgs a) {
+    using Cfg = CarryCfg<NS>;
+    constexpr int CPT = Cfg::CPT, NP = CPT / 32;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(sm);
-    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
-    uint32_t* misc = reinterpret_cast<uint32_t*>(sm + OFF_MISC);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + Cfg::BAR);
+    uint32_t* misc = reinterpret_cast<uint32_t*>(sm + Cfg::MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
-    CarryScalars* scal = reinterpret_cast<CarryScalars*>(sm + OFF_SCAL);
+    CarryScalars* scal = reinterpret_cast<CarryScalars*>(sm + Cfg::SCAL);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n0 = blockIdx.x * NS, h = blockIdx.y, b = blockIdx.z;
@@ -778,17 +820,15 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
     const int nch = (S + C - 1) / C;
 
     if (tid == 0) {
-        for (int i = 0; i < B_COUNT; ++i)
-            mbar_init(&bar[i], 1);
+        for (int i = 0; i < B_COUNT; ++i) mbar_init(&bar[i], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(misc, TM_COLS);
+        tmem_alloc(misc, Cfg::TMCOLS);
         tmem_relinquish();
     }
     if (tid == 32) {
-        prefetch_tensormap(&mq);
         prefetch_tensormap(&mk);
         prefetch_tensormap(&mv);
     }
@@ -805,107 +845,108 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
             int issued = 0;
             for (int c = 0; c < nch; ++c) {
                 const int s = c & 1;
-                if (c >= 2 && !wait_or_abort(&bar[B_EMPTY0 + s], ((c >> 1) + 1) & 1, abort_flag,
+                uint8_t* st = sm + s * Cfg::STAGE;
+                const uint8_t* wsc = wsh + (size_t)c * WS_UNIT;
+                // early group of chunk c: W, Q~, V, T_U, scalars
+                if (c >= 2 && !wait_or_abort(&bar[B_EMPTYE0 + s], ((c >> 1) + 1) & 1, abort_flag,
                                              ST_PRODUCER))
                     break;
                 if (*abort_flag) break;
-                uint8_t* st = sm + s * STAGE_BYTES;
-                const uint8_t* wsc = wsh + (size_t)c * WS_UNIT;
                 TRACE(c, 0);
-                mbar_arrive_expect_tx(&bar[B_FULL0 + s],
-                                      2 * 16384 + 8192 + 32768 + (uint32_t)sizeof(CarryScalars));
+                uint64_t* fe = &bar[B_FULLE0 + s];
+                mbar_arrive_expect_tx(fe, 4 * 8192 + Cfg::NB * 8192 + 8192 +
+                                              (uint32_t)sizeof(CarryScalars));
                 for (int blk = 0; blk < 2; ++blk) {
-                    tma_load_3d(st + blk * BLK_STRIDE + OFF_Q, &mq, &bar[B_FULL0 + s], blk * 64,
-                                c * C, zq);
-                    tma_load_3d(st + blk * BLK_STRIDE + OFF_K, &mk, &bar[B_FULL0 + s], blk * 64,
-                                c * C, zq);
-                    bulk_g2s(st + blk * BLK_STRIDE + OFF_W, wsc + WS_W + blk * 8192, 8192,
-                             &bar[B_FULL0 + s]);
+                    uint8_t* sb = st + blk * BLK_STRIDE;
+                    bulk_g2s(sb + OFF_W, wsc + WS_W + blk * 8192, 8192, fe);
+                    bulk_g2s(sb + OFF_Q, wsc + WS_QT + blk * 8192, 8192, fe);
                 }
-                tma_load_3d(st + OFF_V, &mv, &bar[B_FULL0 + s], n0, c * C, zv);
-                bulk_g2s(st + OFF_TU, wsc + WS_TU, 16384, &bar[B_FULL0 + s]);  // T_U | P
-                bulk_g2s(&scal[s], wsc + WS_CS, sizeof(CarryScalars), &bar[B_FULL0 + s]);
-                TRACE(c, 7);
+                for (int blk = 0; blk < Cfg::NB; ++blk)
+                    tma_load_3d(st + OFF_V + blk * 8192, &mv, fe, n0 + blk * 64, c * C, zv);
+                bulk_g2s(st + Cfg::OFF_TU, wsc + WS_TU, 8192, fe);
+                bulk_g2s(&scal[s], wsc + WS_CS, sizeof(CarryScalars), fe);
+                // late group of chunk c: K, P
+                if (c >= 2 && !wait_or_abort(&bar[B_EMPTYL0 + s], ((c >> 1) + 1) & 1, abort_flag,
+                                             ST_PRODUCER))
+                    break;
+                uint64_t* fl = &bar[B_FULLL0 + s];
+                mbar_arrive_expect_tx(fl, 3 * 8192);
+                for (int blk = 0; blk < 2; ++blk)
+                    tma_load_3d(st + blk * BLK_STRIDE + OFF_K, &mk, fl, blk * 64, c * C, zq);
+                bulk_g2s(st + OFF_P, wsc + WS_P, 8192, fl);
                 issued = c + 1;
-                // chunk c + 2 goes to L2 now; its copy is issued once this stage is free
+                // chunk c + 2 goes to L2 now
                 if (c + 2 < nch) {
-                    for (int blk = 0; blk < 2; ++blk) {
-                        tma_prefetch_l2_3d(&mq, blk * 64, (c + 2) * C, zq);
+                    for (int blk = 0; blk < 2; ++blk)
                         tma_prefetch_l2_3d(&mk, blk * 64, (c + 2) * C, zq);
-                    }
-                    tma_prefetch_l2_3d(&mv, n0, (c + 2) * C, zv);
+                    for (int blk = 0; blk < Cfg::NB; ++blk)
+                        tma_prefetch_l2_3d(&mv, n0 + blk * 64, (c + 2) * C, zv);
                     bulk_prefetch_l2(wsc + 2 * WS_UNIT, WS_UNIT);
                 }
             }
             if (*abort_flag) {
-                // let the copies already issued land before the CTA exits
-                for (int c = (issued > 2 ? issued - 2 : 0); c < issued; ++c)
-                    mbar_wait_bounded(&bar[B_FULL0 + (c & 1)], (c >> 1) & 1, kWaitNs);
+                // let the copies already issued land before the CTA exits (a group whose
+                // copies were not issued completes no phase: its wait just runs out)
+                for (int c = (issued > 2 ? issued - 2 : 0); c < issued; ++c) {
+                    mbar_wait_bounded(&bar[B_FULLE0 + (c & 1)], (c >> 1) & 1, kWaitNs);
+                    mbar_wait_bounded(&bar[B_FULLL0 + (c & 1)], (c >> 1) & 1, kWaitNs);
+                }
             }
         }
-    } else {
-        // ------------------------------------------------- carry (warps 1..9, 288 threads)
-        // Warp 1, lane 0 issues every MMA of the carry: MMA1 [W; Q] S0 of chunk c and
-        // U~ = [T_U; P] V of chunk c+1 (which runs while U of chunk c is formed), then
-        // K^T U' and P U of chunk c (P U runs while the state is updated).
-        // Warps 2..9: two per TMEM lane quadrant; thread = state row L (Dk index; token L
-        // for L < 64, token L - 64 of the Q S0 / P U halves for L >= 64), 32 state columns
-        // (half hc of the CTA's 64). Quadrants 0-1 form U of chunk c while quadrants 2-3
-        // write the output of chunk c-1; then all update the state.
-        const bool issuer = warp == 1;
+    } else if (warp == 2 || warp >= 4) {
+        // ----------------------------------------- carry (warps 2, 4..11: 288 threads)
+        const bool issuer = warp == 2;
         const bool leader = issuer && lane == 0;
-        const int q = warp & 3, hc = issuer ? 0 : (warp - 2) >> 2;
+        const int q = warp & 3, hc = issuer ? 0 : (warp - 4) >> 2;
         const int L = 32 * q + lane;
-        const uint32_t lane_off = ((uint32_t)(32 * q) << 16) + 32u * (uint32_t)hc;
-        const uint32_t s_tile = sbase + OFF_S, u_tile = sbase + OFF_U, u2_tile = sbase + OFF_U2;
-        float* gstate = a.state + ((size_t)(b * a.Hv + h) * 128 + L) * 128 + n0 + 32 * hc;
-        __nv_bfloat16* gout = a.out + (size_t)(b * a.Hv + h) * S * 128 + n0 + 32 * hc;
+        const int col0 = CPT * hc;  // first state column of this thread within the slice
+        const uint32_t lane_off = ((uint32_t)(32 * q) << 16) + (uint32_t)col0;
+        const uint32_t s_base = sbase + Cfg::SM_S, u_tile = sbase + Cfg::U, u2_tile = sbase + Cfg::U2;
+        float* gstate = a.state + ((size_t)(b * a.Hv + h) * 128 + L) * 128 + n0 + col0;
+        __nv_bfloat16* gout = a.out + (size_t)(b * a.Hv + h) * S * 128 + n0 + col0;
+        // 32-column piece p of this thread: tile block and 16-byte chunk within the block
+        auto pblk = [&](int p) { return (uint32_t)((col0 + 32 * p) >> 6); };
+        auto pch = [&](int p) { return ((col0 + 32 * p) & 63) >> 3; };
 
+        // the fp32 state: row L, columns col0 .. col0 + CPT - 1 of the slice, in registers
+        float Sr[CPT];
         if (!issuer) {
-            // the fp32 state lives in TMEM (columns TM_SS), its bf16 copy in the S tile
-            float Sm[32];
             if (a.state_is_input) {
 #pragma unroll
-                for (int j = 0; j < 32; j += 4) {
+                for (int j = 0; j < CPT; j += 4) {
                     const float4 x = *reinterpret_cast<const float4*>(gstate + j);
-                    Sm[j] = x.x;
-                    Sm[j + 1] = x.y;
-                    Sm[j + 2] = x.z;
-                    Sm[j + 3] = x.w;
+                    Sr[j] = x.x;
+                    Sr[j + 1] = x.y;
+                    Sr[j + 2] = x.z;
+                    Sr[j + 3] = x.w;
                 }
             } else {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) Sm[j] = 0.f;
+                for (int j = 0; j < CPT; ++j) Sr[j] = 0.f;
             }
-            tmem_st32(tmem + lane_off + TM_SS, Sm);
-            write_row32(s_tile, L, 4 * hc, Sm);
-            tmem_wait_st();
+#pragma unroll
+            for (int p = 0; p < NP; ++p) write_row32(s_base + 16384u * pblk(p), L, pch(p), Sr + 32 * p);
             fence_proxy_async_smem();
         }
         tc_fence_before();
 
-        // O = scale (Gamma Q S0 + P U) of chunk cc for token L - 64 (quadrants 2, 3)
-        auto write_out = [&](int cc, float gm) {
+        // out = scale (Q~ S0 + P U) of chunk cc for token L - 64 (quadrants 2, 3)
+        auto write_out = [&](int cc) {
             const int t = cc * C + (L - 64);
-            const uint32_t ta = TM_A + 64u * (uint32_t)(cc & 1);
+            const uint32_t ta = Cfg::TMA + (uint32_t)NS * (uint32_t)(cc & 1);
 #pragma unroll
-            for (int qq = 0; qq < 2; ++qq) {
-                float qs[16], pu[16];
-                tmem_ld16x2(tmem + lane_off + ta + 16 * qq, tmem + lane_off + TM_B + 16 * qq, qs,
-                            pu);
+            for (int p = 0; p < NP; ++p) {
+                float o[32];
+                tmem_ld32(tmem + lane_off + ta + 32 * p, o);
                 if (t < S) {
-                    uint4* dst = reinterpret_cast<uint4*>(gout + (size_t)t * 128 + 16 * qq);
+                    uint4* dst = reinterpret_cast<uint4*>(gout + (size_t)t * 128 + 32 * p);
 #pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        float o[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            o[e] = a.scale * fmaf(gm, qs[8 * j + e], pu[8 * j + e]);
+                    for (int j = 0; j < 4; ++j) {
                         uint4 w;
-                        w.x = pack_bf16(o[0], o[1]);
-                        w.y = pack_bf16(o[2], o[3]);
-                        w.z = pack_bf16(o[4], o[5]);
-                        w.w = pack_bf16(o[6], o[7]);
+                        w.x = pack_bf16(a.scale * o[8 * j + 0], a.scale * o[8 * j + 1]);
+                        w.y = pack_bf16(a.scale * o[8 * j + 2], a.scale * o[8 * j + 3]);
+                        w.z = pack_bf16(a.scale * o[8 * j + 4], a.scale * o[8 * j + 5]);
+                        w.w = pack_bf16(a.scale * o[8 * j + 6], a.scale * o[8 * j + 7]);
                         dst[j] = w;
                     }
                 }
@@ -914,48 +955,55 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
 
         int mmas = 0, done = 0;
         bool landed = true;   // leader: chunk c has landed and U~(c) is issued
-        float gm_prev = 0.f;  // Gamma of the previous chunk's token L - 64
+        bool u_next = false;  // leader: U~(c+1) already issued
         if (leader) {
-            landed = wait_or_abort(&bar[B_FULL0], 0, abort_flag, ST_MMA);
+            landed = wait_or_abort(&bar[B_FULLE0], 0, abort_flag, ST_MMA);
             if (landed) {
                 tc_fence_after();
-                issue_u(tmem, sbase, TM_U);
+                issue_u<NS>(tmem, sbase, Cfg::TMB);
                 mmas = 1;
             }
         }
         for (int c = 0; c < nch; ++c) {
             const int s = c & 1;
-            const uint32_t st = sbase + s * STAGE_BYTES;
-            // the state tile is complete: MMA1 [W; Q] S0
-            if (bar_any(1, 288, !landed || *abort_flag)) break;
+            const uint32_t st = sbase + s * Cfg::STAGE;
+            const uint32_t ta = Cfg::TMA + (uint32_t)NS * (uint32_t)s;
+            const uint32_t tb = Cfg::TMB + (uint32_t)NS * (uint32_t)s;
+            // the state tile is complete: MMA1 [W; Q~] S0. (A thread that gives up sets the
+            // abort flag before it arrives, so every thread reads the same flag after the
+            // barrier.)
+            if (!landed && !*abort_flag) record_failure(abort_flag, ST_MMA);
+            bar_sync(1, 288);
+            if (*abort_flag) break;
             if (leader) {
                 TRACE(c, 12);
                 tc_fence_after();
-                issue_carry1(tmem, st, s_tile, TM_A + 64u * (uint32_t)s);
-                tc_commit(&bar[B_ADONE]);  // also covers U~(c), issued earlier
+                issue_carry1<NS>(tmem, st, s_base, ta);
+                tc_commit(&bar[B_ADONE]);        // also covers U~(c), issued earlier
+                tc_commit(&bar[B_EMPTYE0 + s]);  // the early group of chunk c is read
                 TRACE(c, 3);
-                if (c + 1 < nch) {
-                    landed = wait_or_abort(&bar[B_FULL0 + (s ^ 1)], ((c + 1) >> 1) & 1, abort_flag,
-                                           ST_MMA);
-                    if (landed) {
-                        issue_u(tmem, sbase + (s ^ 1) * STAGE_BYTES, TM_U + 64u * (uint32_t)(s ^ 1));
-                        TRACE(c + 1, 5);
-                    }
+                // U~(c+1) now if chunk c+1 has landed (it then runs while U is formed); its
+                // buffer was last read by the state update of chunk c-1
+                u_next = c + 1 < nch &&
+                         mbar_test_wait(&bar[B_FULLE0 + (s ^ 1)], ((c + 1) >> 1) & 1);
+                if (u_next) {
+                    tc_fence_after();
+                    issue_u<NS>(tmem, sbase + (s ^ 1) * Cfg::STAGE,
+                                Cfg::TMB + (uint32_t)NS * (uint32_t)(s ^ 1));
+                    TRACE(c + 1, 5);
                 }
             }
             bool ok = true;
+            float Gl = 0.f;
             if (!issuer) {
                 // P U of chunk c-1 must be complete before the U tile is rewritten and
-                // before its output is read
+                // before that chunk's output is read
                 ok = c == 0 || wait_or_abort(&bar[B_CDONE], (c - 1) & 1, abort_flag, ST_CARRY);
                 if (q >= 2) {
                     if (ok && c > 0) {
                         tc_fence_after();
-                        write_out(c - 1, gm_prev);
+                        write_out(c - 1);
                     }
-                    // per-chunk scalars are read now: the producer may rewrite this stage's
-                    // scalars once the chunk's last MMAs complete
-                    gm_prev = scal[s].Gam[L - 64];
                 } else {
                     ok = ok && wait_or_abort(&bar[B_ADONE], c & 1, abort_flag, ST_CARRY);
                     if (ok) {
@@ -964,76 +1012,94 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
                         // U = U~ - W S0 and U' = exp(gamma_last - gamma_L) U for token L
                         const float kd = scal[s].kdec[L];
 #pragma unroll
-                        for (int qq = 0; qq < 2; ++qq) {
-                            float ws[16], ut[16];
-                            tmem_ld16x2(tmem + lane_off + TM_A + 64u * (uint32_t)s + 16 * qq,
-                                        tmem + lane_off + TM_U + 64u * (uint32_t)s + 16 * qq, ws,
-                                        ut);
+                        for (int p = 0; p < NP; ++p) {
+                            float ws[32], ut[32];
+                            tmem_ld32x2(tmem + lane_off + ta + 32 * p, tmem + lane_off + tb + 32 * p,
+                                        ws, ut);
+                            uint32_t u[16], u2[16];
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) ut[j] -= ws[j];
-                            write_row16(u_tile, L, 4 * hc + 2 * qq, ut);
-#pragma unroll
-                            for (int j = 0; j < 16; ++j) ut[j] *= kd;
-                            write_row16(u2_tile, L, 4 * hc + 2 * qq, ut);
+                            for (int j = 0; j < 16; ++j) {
+                                const float x0 = ut[2 * j] - ws[2 * j], x1 = ut[2 * j + 1] - ws[2 * j + 1];
+                                u[j] = pack_bf16(x0, x1);
+                                u2[j] = pack_bf16(kd * x0, kd * x1);
+                            }
+                            write_row32_packed(u_tile + 8192u * pblk(p), L, pch(p), u);
+                            write_row32_packed(u2_tile + 8192u * pblk(p), L, pch(p), u2);
                         }
                     }
                 }
+                // the stage's scalars are read before its last MMAs are issued (after
+                // which the producer may overwrite them)
+                Gl = scal[s].Gl;
                 fence_proxy_async_smem();
                 tc_fence_before();
+                if (lane == 0 && (warp == 4 || warp == 6)) TRACE(c, warp == 4 ? 11 : 17);
+                if (lane == 0) TRACE(c, 26 + (warp - 4));
             }
-            const float Gl = scal[s].Gl;
-            if (bar_any(1, 288, !ok || *abort_flag)) break;
+            if (leader) TRACE(c, 34);
+            if (!ok && !*abort_flag) record_failure(abort_flag, ST_CARRY);
+            bar_sync(1, 288);
+            if (*abort_flag) break;
             if (leader) {
                 TRACE(c, 14);
+                ok = wait_or_abort(&bar[B_FULLL0 + s], (c >> 1) & 1, abort_flag, ST_MMA);
                 tc_fence_after();
-                issue_carry3(tmem, st, u2_tile);
+                if (ok) issue_carry3<NS>(tmem, st, u2_tile, tb);  // U~(c) is consumed
                 tc_commit(&bar[B_SDONE]);
-                issue_carry2(tmem, st, u_tile);
+                TRACE(c, 9);
+                if (c + 1 < nch && !u_next) {
+                    landed = wait_or_abort(&bar[B_FULLE0 + (s ^ 1)], ((c + 1) >> 1) & 1,
+                                           abort_flag, ST_MMA);
+                    TRACE(c, 8);
+                    if (landed) {
+                        issue_u<NS>(tmem, sbase + (s ^ 1) * Cfg::STAGE,
+                                    Cfg::TMB + (uint32_t)NS * (uint32_t)(s ^ 1));
+                        TRACE(c + 1, 5);
+                    }
+                }
+                if (ok) issue_carry2<NS>(tmem, st, u_tile, ta);
                 tc_commit(&bar[B_CDONE]);
-                tc_commit(&bar[B_EMPTY0 + s]);
+                tc_commit(&bar[B_EMPTYL0 + s]);
+                if (!ok) landed = false;  // the late group never landed: stop at the top
                 TRACE(c, 4);
             }
             if (!issuer) {
                 // S1 = Gamma_last S0 + K^T U' for state row L
                 ok = wait_or_abort(&bar[B_SDONE], c & 1, abort_flag, ST_CARRY);
                 if (ok) {
-                    if (warp == 2 && lane == 0) TRACE(c, 15);
+                    if (warp == 4 && lane == 0) TRACE(c, 15);
                     tc_fence_after();
 #pragma unroll
-                    for (int qq = 0; qq < 2; ++qq) {
-                        float d[16], sv[16];
-                        tmem_ld16x2(tmem + lane_off + TM_S + 16 * qq,
-                                    tmem + lane_off + TM_SS + 16 * qq, d, sv);
+                    for (int p = 0; p < NP; ++p) {
+                        float d[32];
+                        tmem_ld32(tmem + lane_off + tb + 32 * p, d);
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) sv[j] = fmaf(Gl, sv[j], d[j]);
-                        tmem_st16(tmem + lane_off + TM_SS + 16 * qq, sv);
-                        write_row16(s_tile, L, 4 * hc + 2 * qq, sv);
+                        for (int j = 0; j < 32; ++j) Sr[32 * p + j] = fmaf(Gl, Sr[32 * p + j], d[j]);
+                        write_row32(s_base + 16384u * pblk(p), L, pch(p), Sr + 32 * p);
                     }
-                    tmem_wait_st();
                     fence_proxy_async_smem();
-                    if (warp == 2 && lane == 0) TRACE(c, 16);
+                    if (warp == 4 && lane == 0) TRACE(c, 16);
                 }
                 tc_fence_before();
             }
             done = c + 1;
         }
-        bool ok = !bar_any(1, 288, done < nch || *abort_flag);
+        if (done < nch && !*abort_flag) record_failure(abort_flag, ST_CARRY);
+        bar_sync(1, 288);
+        bool ok = !*abort_flag;
         if (ok && !issuer && q >= 2) {
             // the output of the last chunk
             ok = wait_or_abort(&bar[B_CDONE], (nch - 1) & 1, abort_flag, ST_CARRY);
             if (ok) {
                 tc_fence_after();
-                write_out(nch - 1, gm_prev);
+                write_out(nch - 1);
             }
         }
         if (ok && !issuer) {
-            tc_fence_after();
-            float Sm[32];
-            tmem_ld32(tmem + lane_off + TM_SS, Sm);
 #pragma unroll
-            for (int j = 0; j < 32; j += 4)
+            for (int j = 0; j < CPT; j += 4)
                 *reinterpret_cast<float4*>(gstate + j) =
-                    make_float4(Sm[j], Sm[j + 1], Sm[j + 2], Sm[j + 3]);
+                    make_float4(Sr[j], Sr[j + 1], Sr[j + 2], Sr[j + 3]);
         }
         // no MMA of the carry may be in flight when TMEM is freed
         if (leader && mmas) {
@@ -1047,7 +1113,7 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
     if (warp == 0) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem, TM_COLS);
+        tmem_dealloc(tmem, Cfg::TMCOLS);
     }
 }
 
@@ -1102,9 +1168,6 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream, int* la
     cudaError_t e = cudaFuncSetAttribute(prep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)PREP_SMEM);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(carry_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)CARRY_SMEM);
-    if (e != cudaSuccess) return e;
     TcArgs t{a.g, a.beta, a.scale, a.B, a.Hk, a.Hv, a.S, a.state, a.state_is_input,
              static_cast<__nv_bfloat16*>(a.out), static_cast<uint8_t*>(a.workspace)};
     const int nch = (a.S + C - 1) / C;
@@ -1112,8 +1175,25 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream, int* la
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     *launched = 1;
-    carry_tc_kernel<<<dim3(128 / NS, a.Hv, a.B), CARRY_THREADS, CARRY_SMEM, stream>>>(mq, mk, mv,
-                                                                                       t);
+    // two CTAs per head (64-column state slices) while that still fits the GPU in one
+    // wave, else one CTA per head (128 columns: half the MMA instructions per head)
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const bool split = 2 * a.B * a.Hv <= sms;
+    if (split) {
+        e = cudaFuncSetAttribute(carry_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)CarryCfg<64>::SMEM);
+        if (e != cudaSuccess) return e;
+        carry_tc_kernel<64><<<dim3(2, a.Hv, a.B), CARRY_THREADS, CarryCfg<64>::SMEM, stream>>>(
+            mk, mv, t);
+    } else {
+        e = cudaFuncSetAttribute(carry_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)CarryCfg<128>::SMEM);
+        if (e != cudaSuccess) return e;
+        carry_tc_kernel<128><<<dim3(1, a.Hv, a.B), CARRY_THREADS, CarryCfg<128>::SMEM, stream>>>(
+            mk, mv, t);
+    }
     e = cudaGetLastError();
     if (e == cudaSuccess) *launched = 2;
     return e;
