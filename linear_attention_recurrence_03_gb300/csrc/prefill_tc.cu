@@ -90,11 +90,13 @@ using namespace ptx;
 constexpr int C = 64;    // chunk length
 constexpr uint64_t kWaitNs = 2000000000ull;
 
-// ---- workspace: per (batch, value head, chunk) unit, six bf16 tiles of 64 rows x 64
+// ---- workspace: per (batch, value head, chunk) unit, eight bf16 tiles of 64 rows x 64
 // columns in the 128-byte swizzled layout, T_U | P | W[:, 0:64] | W[:, 64:128] |
-// Q~[:, 0:64] | Q~[:, 64:128] with Q~ = diag(Gamma) Q, then the carry's decay scalars
-constexpr uint32_t WS_UNIT = 50176;
-constexpr uint32_t WS_TU = 0, WS_P = 8192, WS_W = 16384, WS_QT = 32768, WS_CS = 49152;
+// Q~[:, 0:64] | Q~[:, 64:128] | K~[:, 0:64] | K~[:, 64:128] with Q~ = diag(Gamma) Q and
+// K~ = diag(exp(gamma_last - gamma)) K, then the carry's decay scalars
+constexpr uint32_t WS_UNIT = 66560;
+constexpr uint32_t WS_TU = 0, WS_P = 8192, WS_W = 16384, WS_QT = 32768, WS_KT = 49152,
+                   WS_CS = 65536;
 
 struct CarryScalars {
     float kdec[C];  // exp(gamma_last - gamma_r)
@@ -146,13 +148,13 @@ enum { PB_FULL = 0, PB_GRAM, PB_PREP, PB_WDONE, PB_DRAIN, PB_COUNT };
 // ---- carry kernel: one CTA per (NS-column slice of the state, value head, batch), NS = 64
 // or 128 (CarryCfg<NS>). Shared memory map:
 //   stage s (two stages, one chunk each), in two copy groups:
-//     block b (Dk columns 64b..64b+63): W_b | Q~_b | K_b (8 KB each, stride 24 KB)
-//       ([W_b; Q~_b] is one 128-row operand), then P ([K_1; P] one operand),
+//     block b (Dk columns 64b..64b+63): W_b | Q~_b | K~_b (8 KB each, stride 24 KB)
+//       ([W_b; Q~_b] is one 128-row operand), then P ([K~_1; P] one operand),
 //     V slice (64 tokens x NS columns, in 64-column blocks), T_U ([T_U; -] one operand)
 //     early group (read by U~ and [W; Q~] S0, freed as soon as they complete): W, Q~, V,
-//     T_U and the scalars; late group (read by K^T U' and P U): K and P
-//   U and U' tiles (64 tokens x NS), the bf16 state operand (128 x NS, 64-column blocks),
-//   per-stage scalars, barriers
+//     T_U; late group (read by K~^T U, P U and the state update): K~, P and the scalars
+//   two U tiles (64 tokens x NS, by chunk parity), the bf16 state operand (128 x NS,
+//   64-column blocks), per-stage scalars, barriers
 // warp 0: producer; warp 2: MMA issuer (an SM sub-partition whose SIMT warps only write the
 // output); warps 4..11: SIMT; warps 1 and 3 only take part in the setup and the teardown
 constexpr int CARRY_THREADS = 384;
@@ -167,9 +169,9 @@ struct CarryCfg {
     static constexpr int CPT = NS / 2;    // state columns per SIMT thread
     static constexpr uint32_t OFF_TU = OFF_V + 8192u * NB;
     static constexpr uint32_t STAGE = OFF_TU + 8192u;
-    static constexpr uint32_t U = 2 * STAGE;             // U tile, NB blocks of 8 KB
-    static constexpr uint32_t U2 = U + 8192u * NB;        // U' tile (decayed U)
-    static constexpr uint32_t SM_S = U2 + 8192u * NB;     // state operand, NB blocks of 16 KB
+    static constexpr uint32_t U = 2 * STAGE;              // U tiles, NB blocks of 8 KB each
+    static constexpr uint32_t UT = 8192u * NB;            // bytes of one U tile
+    static constexpr uint32_t SM_S = U + 2 * UT;          // state operand, NB blocks of 16 KB
     static constexpr uint32_t SCAL = SM_S + 16384u * NB;
     static constexpr uint32_t BAR = SCAL + 2 * sizeof(CarryScalars);
     static constexpr uint32_t MISC = BAR + 128;
@@ -440,19 +442,19 @@ __device__ __forceinline__ void issue_carry1(uint32_t tmem, uint32_t st, uint32_
     }
 }
 
-// carry: the state increment K^T U' over the tokens (K read M-major), into `tb`
+// carry: the state increment K~^T U over the tokens (K~ read M-major), into `tb`
 template <int NS>
-__device__ __forceinline__ void issue_carry3(uint32_t tmem, uint32_t st, uint32_t u2_tile,
+__device__ __forceinline__ void issue_carry3(uint32_t tmem, uint32_t st, uint32_t u_tile,
                                              uint32_t tb) {
     constexpr uint32_t id = idesc_bf16(128, NS, true, true);
     const uint64_t ak = smem_desc_sw128(st + OFF_K, BLK_STRIDE, 1024);
-    const uint64_t bu2 = smem_desc_sw128(u2_tile, 8192, 1024);
+    const uint64_t bu2 = smem_desc_sw128(u_tile, 8192, 1024);
 #pragma unroll
     for (int k = 0; k < 4; ++k)
         mma_bf16(tmem + tb, dadd(ak, k * 2048), dadd(bu2, k * 2048), id, k > 0);
 }
 
-// carry: [K_1 U; P U] = [K_1; P] U, accumulated onto [W S0; Q~ S0] in `ta`: the lower
+// carry: [K~_1 U; P U] = [K~_1; P] U, accumulated onto [W S0; Q~ S0] in `ta`: the lower
 // half becomes the un-scaled output Q~ S0 + P U (the upper half is no longer needed)
 template <int NS>
 __device__ __forceinline__ void issue_carry2(uint32_t tmem, uint32_t st, uint32_t u_tile,
@@ -611,23 +613,29 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
             tc_fence_after();
             if (P == 0) TRACE_PREP(23);
 
-            // ---- Q~ = diag(Gamma) Q straight to the workspace (the Q slots are reused
-            // next); 16-byte chunk j of the two Q blocks, same swizzled position
+            // ---- Q~ = diag(Gamma) Q and K~ = diag(exp(gamma_last - gamma)) K straight to
+            // the workspace (the Q slots are reused next); 16-byte chunk j of the two
+            // blocks, same swizzled position
             {
-                uint8_t* wq = a.ws + ws_offset(b, h, c, a.Hv, nch) + WS_QT;
+                uint8_t* wsu = a.ws + ws_offset(b, h, c, a.Hv, nch);
+                const CarryScalars& cs = *reinterpret_cast<const CarryScalars*>(sm + P_CS);
 #pragma unroll
-                for (int it = 0; it < 4; ++it) {
-                    const int j = P + 256 * it, blk = j >> 9, off = (j & 511) * 16;
-                    const float gmr = sc.Gam[(j & 511) >> 3];
-                    const uint4 x = *reinterpret_cast<const uint4*>(sm + blk * PQ_STRIDE + PQ_Q + off);
+                for (int it = 0; it < 8; ++it) {
+                    const int j = P + 256 * (it & 3), blk = j >> 9, off = (j & 511) * 16;
+                    const int row = (j & 511) >> 3;
+                    const bool isq = it < 4;
+                    const float f = isq ? sc.Gam[row] : cs.kdec[row];
+                    const uint4 x = *reinterpret_cast<const uint4*>(
+                        sm + blk * PQ_STRIDE + (isq ? PQ_Q : PQ_K) + off);
                     const uint32_t in[4] = {x.x, x.y, x.z, x.w};
                     uint32_t o[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&in[e]));
-                        o[e] = pack_bf16(f.x * gmr, f.y * gmr);
+                        const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&in[e]));
+                        o[e] = pack_bf16(v.x * f, v.y * f);
                     }
-                    *reinterpret_cast<uint4*>(wq + blk * 8192 + off) = make_uint4(o[0], o[1], o[2], o[3]);
+                    *reinterpret_cast<uint4*>(wsu + (isq ? WS_QT : WS_KT) + blk * 8192 + off) =
+                        make_uint4(o[0], o[1], o[2], o[3]);
                 }
             }
             bar_sync(2, 256);  // every Q chunk is read before A overwrites the Q slots
@@ -801,8 +809,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
 // landed, then K^T U', U~ of chunk c+1 if not issued yet, P U.
 template <int NS>
 __global__ void __launch_bounds__(CARRY_THREADS, 1)
-    carry_tc_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
-                    TcArgs a) {
+    carry_tc_kernel(const __grid_constant__ CUtensorMap mv, TcArgs a) {
     using Cfg = CarryCfg<NS>;
     constexpr int CPT = Cfg::CPT, NP = CPT / 32;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -815,7 +822,6 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n0 = blockIdx.x * NS, h = blockIdx.y, b = blockIdx.z;
-    const int kh = h / (a.Hv / a.Hk);
     const int S = a.S;
     const int nch = (S + C - 1) / C;
 
@@ -828,10 +834,7 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
         tmem_alloc(misc, Cfg::TMCOLS);
         tmem_relinquish();
     }
-    if (tid == 32) {
-        prefetch_tensormap(&mk);
-        prefetch_tensormap(&mv);
-    }
+    if (tid == 32) prefetch_tensormap(&mv);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -840,22 +843,21 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------- loads (one thread)
         if (lane == 0) {
-            const int zq = b * a.Hk + kh, zv = b * a.Hv + h;
+            const int zv = b * a.Hv + h;
             const uint8_t* wsh = a.ws + ws_offset(b, h, 0, a.Hv, nch);
             int issued = 0;
             for (int c = 0; c < nch; ++c) {
                 const int s = c & 1;
                 uint8_t* st = sm + s * Cfg::STAGE;
                 const uint8_t* wsc = wsh + (size_t)c * WS_UNIT;
-                // early group of chunk c: W, Q~, V, T_U, scalars
+                // early group of chunk c: W, Q~, V, T_U
                 if (c >= 2 && !wait_or_abort(&bar[B_EMPTYE0 + s], ((c >> 1) + 1) & 1, abort_flag,
                                              ST_PRODUCER))
                     break;
                 if (*abort_flag) break;
                 TRACE(c, 0);
                 uint64_t* fe = &bar[B_FULLE0 + s];
-                mbar_arrive_expect_tx(fe, 4 * 8192 + Cfg::NB * 8192 + 8192 +
-                                              (uint32_t)sizeof(CarryScalars));
+                mbar_arrive_expect_tx(fe, 4 * 8192 + Cfg::NB * 8192 + 8192);
                 for (int blk = 0; blk < 2; ++blk) {
                     uint8_t* sb = st + blk * BLK_STRIDE;
                     bulk_g2s(sb + OFF_W, wsc + WS_W + blk * 8192, 8192, fe);
@@ -864,21 +866,19 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
                 for (int blk = 0; blk < Cfg::NB; ++blk)
                     tma_load_3d(st + OFF_V + blk * 8192, &mv, fe, n0 + blk * 64, c * C, zv);
                 bulk_g2s(st + Cfg::OFF_TU, wsc + WS_TU, 8192, fe);
-                bulk_g2s(&scal[s], wsc + WS_CS, sizeof(CarryScalars), fe);
-                // late group of chunk c: K, P
+                // late group of chunk c: K~, P, scalars
                 if (c >= 2 && !wait_or_abort(&bar[B_EMPTYL0 + s], ((c >> 1) + 1) & 1, abort_flag,
                                              ST_PRODUCER))
                     break;
                 uint64_t* fl = &bar[B_FULLL0 + s];
-                mbar_arrive_expect_tx(fl, 3 * 8192);
+                mbar_arrive_expect_tx(fl, 3 * 8192 + (uint32_t)sizeof(CarryScalars));
                 for (int blk = 0; blk < 2; ++blk)
-                    tma_load_3d(st + blk * BLK_STRIDE + OFF_K, &mk, fl, blk * 64, c * C, zq);
+                    bulk_g2s(st + blk * BLK_STRIDE + OFF_K, wsc + WS_KT + blk * 8192, 8192, fl);
                 bulk_g2s(st + OFF_P, wsc + WS_P, 8192, fl);
+                bulk_g2s(&scal[s], wsc + WS_CS, sizeof(CarryScalars), fl);
                 issued = c + 1;
                 // chunk c + 2 goes to L2 now
                 if (c + 2 < nch) {
-                    for (int blk = 0; blk < 2; ++blk)
-                        tma_prefetch_l2_3d(&mk, blk * 64, (c + 2) * C, zq);
                     for (int blk = 0; blk < Cfg::NB; ++blk)
                         tma_prefetch_l2_3d(&mv, n0 + blk * 64, (c + 2) * C, zv);
                     bulk_prefetch_l2(wsc + 2 * WS_UNIT, WS_UNIT);
@@ -901,7 +901,7 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
         const int L = 32 * q + lane;
         const int col0 = CPT * hc;  // first state column of this thread within the slice
         const uint32_t lane_off = ((uint32_t)(32 * q) << 16) + (uint32_t)col0;
-        const uint32_t s_base = sbase + Cfg::SM_S, u_tile = sbase + Cfg::U, u2_tile = sbase + Cfg::U2;
+        const uint32_t s_base = sbase + Cfg::SM_S, u_tile = sbase + Cfg::U;
         float* gstate = a.state + ((size_t)(b * a.Hv + h) * 128 + L) * 128 + n0 + col0;
         __nv_bfloat16* gout = a.out + (size_t)(b * a.Hv + h) * S * 128 + n0 + col0;
         // 32-column piece p of this thread: tile block and 16-byte chunk within the block
@@ -969,6 +969,7 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
             const uint32_t st = sbase + s * Cfg::STAGE;
             const uint32_t ta = Cfg::TMA + (uint32_t)NS * (uint32_t)s;
             const uint32_t tb = Cfg::TMB + (uint32_t)NS * (uint32_t)s;
+            const uint32_t ut = u_tile + Cfg::UT * (uint32_t)s;  // U tile of chunk c
             // the state tile is complete: MMA1 [W; Q~] S0. (A thread that gives up sets the
             // abort flag before it arrives, so every thread reads the same flag after the
             // barrier.)
@@ -982,55 +983,45 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
                 tc_commit(&bar[B_ADONE]);        // also covers U~(c), issued earlier
                 tc_commit(&bar[B_EMPTYE0 + s]);  // the early group of chunk c is read
                 TRACE(c, 3);
-                // U~(c+1) now if chunk c+1 has landed (it then runs while U is formed); its
-                // buffer was last read by the state update of chunk c-1
+                // U~(c+1) now if chunk c+1 has landed; its buffer was last read by the
+                // state update of chunk c-1
                 u_next = c + 1 < nch &&
                          mbar_test_wait(&bar[B_FULLE0 + (s ^ 1)], ((c + 1) >> 1) & 1);
                 if (u_next) {
-                    tc_fence_after();
                     issue_u<NS>(tmem, sbase + (s ^ 1) * Cfg::STAGE,
                                 Cfg::TMB + (uint32_t)NS * (uint32_t)(s ^ 1));
                     TRACE(c + 1, 5);
                 }
             }
             bool ok = true;
-            float Gl = 0.f;
             if (!issuer) {
-                // P U of chunk c-1 must be complete before the U tile is rewritten and
-                // before that chunk's output is read
-                ok = c == 0 || wait_or_abort(&bar[B_CDONE], (c - 1) & 1, abort_flag, ST_CARRY);
                 if (q >= 2) {
+                    // the output of chunk c-1, once its P U is complete
+                    ok = c == 0 ||
+                         wait_or_abort(&bar[B_CDONE], (c - 1) & 1, abort_flag, ST_CARRY);
                     if (ok && c > 0) {
                         tc_fence_after();
                         write_out(c - 1);
                     }
                 } else {
-                    ok = ok && wait_or_abort(&bar[B_ADONE], c & 1, abort_flag, ST_CARRY);
+                    ok = wait_or_abort(&bar[B_ADONE], c & 1, abort_flag, ST_CARRY);
                     if (ok) {
                         if (warp == 4 && lane == 0) TRACE(c, 13);
                         tc_fence_after();
-                        // U = U~ - W S0 and U' = exp(gamma_last - gamma_L) U for token L
-                        const float kd = scal[s].kdec[L];
+                        // U = U~ - W S0 for token L
 #pragma unroll
                         for (int p = 0; p < NP; ++p) {
-                            float ws[32], ut[32];
+                            float ws[32], uv[32];
                             tmem_ld32x2(tmem + lane_off + ta + 32 * p, tmem + lane_off + tb + 32 * p,
-                                        ws, ut);
-                            uint32_t u[16], u2[16];
+                                        ws, uv);
+                            uint32_t u[16];
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) {
-                                const float x0 = ut[2 * j] - ws[2 * j], x1 = ut[2 * j + 1] - ws[2 * j + 1];
-                                u[j] = pack_bf16(x0, x1);
-                                u2[j] = pack_bf16(kd * x0, kd * x1);
-                            }
-                            write_row32_packed(u_tile + 8192u * pblk(p), L, pch(p), u);
-                            write_row32_packed(u2_tile + 8192u * pblk(p), L, pch(p), u2);
+                            for (int j = 0; j < 16; ++j)
+                                u[j] = pack_bf16(uv[2 * j] - ws[2 * j], uv[2 * j + 1] - ws[2 * j + 1]);
+                            write_row32_packed(ut + 8192u * pblk(p), L, pch(p), u);
                         }
                     }
                 }
-                // the stage's scalars are read before its last MMAs are issued (after
-                // which the producer may overwrite them)
-                Gl = scal[s].Gl;
                 fence_proxy_async_smem();
                 tc_fence_before();
                 if (lane == 0 && (warp == 4 || warp == 6)) TRACE(c, warp == 4 ? 11 : 17);
@@ -1044,9 +1035,13 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
                 TRACE(c, 14);
                 ok = wait_or_abort(&bar[B_FULLL0 + s], (c >> 1) & 1, abort_flag, ST_MMA);
                 tc_fence_after();
-                if (ok) issue_carry3<NS>(tmem, st, u2_tile, tb);  // U~(c) is consumed
+                if (ok) issue_carry3<NS>(tmem, st, ut, tb);  // U~(c) is consumed
                 tc_commit(&bar[B_SDONE]);
                 TRACE(c, 9);
+                // P U of chunk c (its output is written while U of chunk c+1 is formed)
+                if (ok) issue_carry2<NS>(tmem, st, ut, ta);
+                tc_commit(&bar[B_CDONE]);
+                tc_commit(&bar[B_EMPTYL0 + s]);  // the late group of chunk c is read
                 if (c + 1 < nch && !u_next) {
                     landed = wait_or_abort(&bar[B_FULLE0 + (s ^ 1)], ((c + 1) >> 1) & 1,
                                            abort_flag, ST_MMA);
@@ -1057,17 +1052,17 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
                         TRACE(c + 1, 5);
                     }
                 }
-                if (ok) issue_carry2<NS>(tmem, st, u_tile, ta);
-                tc_commit(&bar[B_CDONE]);
-                tc_commit(&bar[B_EMPTYL0 + s]);
                 if (!ok) landed = false;  // the late group never landed: stop at the top
                 TRACE(c, 4);
             }
             if (!issuer) {
-                // S1 = Gamma_last S0 + K^T U' for state row L
-                ok = wait_or_abort(&bar[B_SDONE], c & 1, abort_flag, ST_CARRY);
+                // S1 = Gamma_last S0 + K~^T U for state row L (the late group holds
+                // Gamma_last; it stays until P U of this chunk completes)
+                ok = wait_or_abort(&bar[B_SDONE], c & 1, abort_flag, ST_CARRY) &&
+                     wait_or_abort(&bar[B_FULLL0 + s], (c >> 1) & 1, abort_flag, ST_CARRY);
                 if (ok) {
                     if (warp == 4 && lane == 0) TRACE(c, 15);
+                    const float Gl = scal[s].Gl;
                     tc_fence_after();
 #pragma unroll
                     for (int p = 0; p < NP; ++p) {
@@ -1186,13 +1181,13 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream, int* la
                                  (int)CarryCfg<64>::SMEM);
         if (e != cudaSuccess) return e;
         carry_tc_kernel<64><<<dim3(2, a.Hv, a.B), CARRY_THREADS, CarryCfg<64>::SMEM, stream>>>(
-            mk, mv, t);
+            mv, t);
     } else {
         e = cudaFuncSetAttribute(carry_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)CarryCfg<128>::SMEM);
         if (e != cudaSuccess) return e;
         carry_tc_kernel<128><<<dim3(1, a.Hv, a.B), CARRY_THREADS, CarryCfg<128>::SMEM, stream>>>(
-            mk, mv, t);
+            mv, t);
     }
     e = cudaGetLastError();
     if (e == cudaSuccess) *launched = 2;
