@@ -94,6 +94,22 @@ gdn_status gdn_prefill(const void* q, const void* k, const void* v,
                        void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * gdn_prefill_noalloc -- gdn_prefill without a caller workspace: the scratch is a
+ * fixed 128 MiB device array inside the library (allocated when the library's module is
+ * loaded), so the call allocates nothing. Arguments, results and errors as gdn_prefill.
+ * On the tensor-core path (bf16, Dk = Dv = 128) the sequence is processed in segments of
+ * whole 64-token chunks that fit the scratch (2016 (batch, head, chunk) units), the state
+ * carrying over from one segment to the next; the result equals gdn_prefill's.
+ * GDN_EUNSUPPORTED if B * Hv exceeds 2016. The scratch is shared by every caller in the
+ * process: calls must not run concurrently (issue them on one stream, or synchronise).
+ */
+gdn_status gdn_prefill_noalloc(const void* q, const void* k, const void* v,
+                               const float* g_log, const float* beta, float scale,
+                               gdn_dtype dtype, int B, int Hk, int Hv, int S, int Dk,
+                               int Dv, float* state, int state_is_input, void* out,
+                               void* stream);
+
+/*
  * gdn_decode_step -- one fused decode token ("GDN TKG Kernel API Reference":
  * Background, parameters, returns, Notes and Dimensions).
  *

@@ -4,6 +4,7 @@ A C-ABI CUDA library (include/gdn.h, built into ``libgdn.so`` by ``build.py``) w
 thin Python binding of the same names:
 
 * ``gdn_prefill``      -- chunked prefill ("GDN CTE Kernel API Reference").
+* ``gdn_prefill_noalloc`` -- the same, with the library's own static scratch.
 * ``gdn_decode_step``  -- fused single-token decode step ("GDN TKG Kernel API Reference").
 """
 from .gdn import (  # noqa: F401
@@ -21,6 +22,7 @@ from .gdn import (  # noqa: F401
     gdn_last_error,
     gdn_launch_count,
     gdn_prefill,
+    gdn_prefill_noalloc,
     gdn_prefill_workspace_bytes,
     load_library,
 )

@@ -1,6 +1,7 @@
 // gdn_api.cu -- the extern "C" entry points declared in include/gdn.h: argument
 // validation, kernel selection and error reporting. No arithmetic of the method lives
 // here; every step runs in the kernels.
+#include <algorithm>
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
@@ -14,6 +15,11 @@ namespace {
 
 thread_local std::string g_last_error;
 std::atomic<unsigned long long> g_launches{0};
+
+// Scratch of gdn_prefill_noalloc: device memory of the library's own module, so that the
+// call itself allocates nothing.
+constexpr size_t kStaticScratchBytes = size_t(128) << 20;
+__device__ __align__(256) unsigned char g_prefill_scratch[kStaticScratchBytes];
 
 gdn_status fail(gdn_status st, const char* fmt, ...) {
     char buf[512];
@@ -83,11 +89,53 @@ gdn_status gdn_prefill(const void* q, const void* k, const void* v, const float*
     int launched = 0;
     const bool bf16 = dtype == GDN_DTYPE_BF16;
     const cudaError_t e = gdn::prefill_tc_supported(a, bf16)
-                              ? gdn::launch_prefill_tc(a, s, &launched)
+                              ? gdn::launch_prefill_tc(a, 0, (S + 63) / 64, s, &launched)
                               : gdn::launch_prefill_simt(a, bf16, s, &launched);
     g_launches += (unsigned long long)launched;
     if (e != cudaSuccess)
         return fail(GDN_ECUDA, "gdn_prefill: launch failed: %s", cudaGetErrorString(e));
+    return GDN_OK;
+}
+
+gdn_status gdn_prefill_noalloc(const void* q, const void* k, const void* v, const float* g_log,
+                               const float* beta, float scale, gdn_dtype dtype, int B, int Hk,
+                               int Hv, int S, int Dk, int Dv, float* state, int state_is_input,
+                               void* out, void* stream) {
+    const size_t need = gdn_prefill_workspace_bytes(B, Hk, Hv, S, Dk, Dv, dtype);
+    if (need == (size_t)-1 || need == 0)  // a shape error, or a path without scratch
+        return gdn_prefill(q, k, v, g_log, beta, scale, dtype, B, Hk, Hv, S, Dk, Dv, state,
+                           state_is_input, out, nullptr, 0, stream);
+    const bool tok = S > 0;
+    if (!ptr_ok(q, tok) || !ptr_ok(k, tok) || !ptr_ok(v, tok) || !ptr_ok(g_log, tok) ||
+        !ptr_ok(beta, tok) || !ptr_ok(out, tok) || !ptr_ok(state, true))
+        return fail(GDN_EINVAL, "gdn_prefill_noalloc: q, k, v, g_log, beta, out and state must "
+                    "be non-NULL, 16-byte aligned device pointers");
+    // the sequence in segments of `seg` chunks, each using the whole static scratch; the
+    // state carries over from one segment to the next
+    const size_t units = kStaticScratchBytes / gdn::prefill_tc_unit_bytes();
+    const size_t heads = (size_t)B * (size_t)Hv;
+    if (heads > units)
+        return fail(GDN_EUNSUPPORTED, "gdn_prefill_noalloc: B*Hv = %zu exceeds the %zu "
+                    "(batch, head) pairs its static scratch holds", heads, units);
+    void* scratch = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&scratch, g_prefill_scratch);
+    if (e != cudaSuccess)
+        return fail(GDN_ECUDA, "gdn_prefill_noalloc: scratch address: %s", cudaGetErrorString(e));
+    const int nch = (S + 63) / 64;
+    const int seg = (int)std::min<size_t>(units / heads, (size_t)nch);
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    for (int c0 = 0; c0 < nch; c0 += seg) {
+        gdn::PrefillArgs a{q,     k,     v,  g_log, beta,  scale,
+                           B,     Hk,    Hv, S,     Dk,    Dv,
+                           state, (c0 == 0 && !state_is_input) ? 0 : 1,
+                           out,   scratch, kStaticScratchBytes};
+        int launched = 0;
+        e = gdn::launch_prefill_tc(a, c0, std::min(seg, nch - c0), s, &launched);
+        g_launches += (unsigned long long)launched;
+        if (e != cudaSuccess)
+            return fail(GDN_ECUDA, "gdn_prefill_noalloc: launch failed: %s",
+                        cudaGetErrorString(e));
+    }
     return GDN_OK;
 }
 

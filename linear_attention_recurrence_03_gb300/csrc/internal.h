@@ -59,7 +59,11 @@ cudaError_t launch_prefill_simt(const PrefillArgs& a, bool bf16, cudaStream_t st
 // carry kernel runs the sequential part. *launched receives the kernels enqueued.
 bool prefill_tc_supported(const PrefillArgs& a, bool bf16);
 size_t prefill_tc_workspace_bytes(int B, int Hv, int S);
-cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream, int* launched);
+size_t prefill_tc_unit_bytes();
+// Processes chunks c0 .. c0 + nseg - 1 of the sequence (64 tokens each) with a workspace of
+// B * Hv * nseg units; the state carries over between consecutive calls.
+cudaError_t launch_prefill_tc(const PrefillArgs& a, int c0, int nseg, cudaStream_t stream,
+                              int* launched);
 
 // Fused decode step.
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);

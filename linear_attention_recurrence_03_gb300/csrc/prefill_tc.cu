@@ -194,11 +194,14 @@ enum {
 // status bits
 constexpr uint32_t ST_PRODUCER = 1u, ST_MMA = 2u, ST_CARRY = 4u, ST_PREP = 8u;
 
+// One launch pair processes chunks c0 .. c0 + nseg - 1 of every (batch, head); the
+// workspace holds nseg units per head, indexed by the chunk's position in the launch.
 struct TcArgs {
     const float* g;
     const float* beta;
     float scale;
     int B, Hk, Hv, S;
+    int c0, nseg;
     float* state;
     int state_is_input;
     __nv_bfloat16* out;
@@ -493,10 +496,11 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
     };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int cl = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int c = a.c0 + cl;           // the chunk's position in the sequence
     const int kh = h / (a.Hv / a.Hk);  // value head h reads key head h // (Hv/Hk)
     const int S = a.S;
-    const int nch = (S + C - 1) / C;
+    const int nch = a.nseg;
 
     const int zq = b * a.Hk + kh, zv = b * a.Hv + h;
     // g and beta of the chunk are loaded first and the copies of Q and K started at
@@ -617,7 +621,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
             // the workspace (the Q slots are reused next); 16-byte chunk j of the two
             // blocks, same swizzled position
             {
-                uint8_t* wsu = a.ws + ws_offset(b, h, c, a.Hv, nch);
+                uint8_t* wsu = a.ws + ws_offset(b, h, cl, a.Hv, nch);
                 const CarryScalars& cs = *reinterpret_cast<const CarryScalars*>(sm + P_CS);
 #pragma unroll
                 for (int it = 0; it < 8; ++it) {
@@ -776,7 +780,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
                 bar_sync(2, 256);
                 if (P == 0) {
                     TRACE_PREP(28);
-                    uint8_t* ws = a.ws + ws_offset(b, h, c, a.Hv, nch);
+                    uint8_t* ws = a.ws + ws_offset(b, h, cl, a.Hv, nch);
                     bulk_s2g(ws + WS_TU, sb + P_TU, 8192);
                     bulk_s2g(ws + WS_P, sb + P_P, 8192);
                     bulk_s2g(ws + WS_W, sb + PQ_Q, 8192);
@@ -823,7 +827,7 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n0 = blockIdx.x * NS, h = blockIdx.y, b = blockIdx.z;
     const int S = a.S;
-    const int nch = (S + C - 1) / C;
+    const int nch = a.nseg;  // chunks of this launch: a.c0 .. a.c0 + nch - 1
 
     if (tid == 0) {
         for (int i = 0; i < B_COUNT; ++i) mbar_init(&bar[i], 1);
@@ -864,7 +868,8 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
                     bulk_g2s(sb + OFF_Q, wsc + WS_QT + blk * 8192, 8192, fe);
                 }
                 for (int blk = 0; blk < Cfg::NB; ++blk)
-                    tma_load_3d(st + OFF_V + blk * 8192, &mv, fe, n0 + blk * 64, c * C, zv);
+                    tma_load_3d(st + OFF_V + blk * 8192, &mv, fe, n0 + blk * 64, (a.c0 + c) * C,
+                                zv);
                 bulk_g2s(st + Cfg::OFF_TU, wsc + WS_TU, 8192, fe);
                 // late group of chunk c: K~, P, scalars
                 if (c >= 2 && !wait_or_abort(&bar[B_EMPTYL0 + s], ((c >> 1) + 1) & 1, abort_flag,
@@ -880,7 +885,7 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
                 // chunk c + 2 goes to L2 now
                 if (c + 2 < nch) {
                     for (int blk = 0; blk < Cfg::NB; ++blk)
-                        tma_prefetch_l2_3d(&mv, n0 + blk * 64, (c + 2) * C, zv);
+                        tma_prefetch_l2_3d(&mv, n0 + blk * 64, (a.c0 + c + 2) * C, zv);
                     bulk_prefetch_l2(wsc + 2 * WS_UNIT, WS_UNIT);
                 }
             }
@@ -932,7 +937,7 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
 
         // out = scale (Q~ S0 + P U) of chunk cc for token L - 64 (quadrants 2, 3)
         auto write_out = [&](int cc) {
-            const int t = cc * C + (L - 64);
+            const int t = (a.c0 + cc) * C + (L - 64);
             const uint32_t ta = Cfg::TMA + (uint32_t)NS * (uint32_t)(cc & 1);
 #pragma unroll
             for (int p = 0; p < NP; ++p) {
@@ -1152,9 +1157,13 @@ size_t prefill_tc_workspace_bytes(int B, int Hv, int S) {
     return (size_t)B * (size_t)Hv * nch * WS_UNIT;
 }
 
-cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream, int* launched) {
+size_t prefill_tc_unit_bytes() { return WS_UNIT; }
+
+cudaError_t launch_prefill_tc(const PrefillArgs& a, int c0, int nseg, cudaStream_t stream,
+                              int* launched) {
     *launched = 0;
-    if (a.workspace == nullptr || a.workspace_bytes < prefill_tc_workspace_bytes(a.B, a.Hv, a.S))
+    if (a.workspace == nullptr || nseg < 1 ||
+        a.workspace_bytes < (size_t)a.B * (size_t)a.Hv * (size_t)nseg * WS_UNIT)
         return cudaErrorInvalidValue;
     CUtensorMap mq, mk, mv;
     if (!encode_3d(&mq, a.q, a.S, a.B * a.Hk) || !encode_3d(&mk, a.k, a.S, a.B * a.Hk) ||
@@ -1163,10 +1172,9 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream, int* la
     cudaError_t e = cudaFuncSetAttribute(prep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)PREP_SMEM);
     if (e != cudaSuccess) return e;
-    TcArgs t{a.g, a.beta, a.scale, a.B, a.Hk, a.Hv, a.S, a.state, a.state_is_input,
+    TcArgs t{a.g,  a.beta, a.scale, a.B, a.Hk, a.Hv, a.S, c0, nseg, a.state, a.state_is_input,
              static_cast<__nv_bfloat16*>(a.out), static_cast<uint8_t*>(a.workspace)};
-    const int nch = (a.S + C - 1) / C;
-    prep_tc_kernel<<<dim3(nch, a.Hv, a.B), PREP_THREADS, PREP_SMEM, stream>>>(mq, mk, t);
+    prep_tc_kernel<<<dim3(nseg, a.Hv, a.B), PREP_THREADS, PREP_SMEM, stream>>>(mq, mk, t);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     *launched = 1;

@@ -24,8 +24,8 @@ STATUS_NAMES = {0: "GDN_OK", 1: "GDN_EINVAL", 2: "GDN_EUNSUPPORTED", 3: "GDN_ECU
                 4: "GDN_ETIMEOUT"}
 
 # Every symbol include/gdn.h declares.
-EXPORTS = ("gdn_prefill_workspace_bytes", "gdn_prefill", "gdn_decode_step",
-           "gdn_last_error", "gdn_get_device_status", "gdn_launch_count")
+EXPORTS = ("gdn_prefill_workspace_bytes", "gdn_prefill", "gdn_prefill_noalloc",
+           "gdn_decode_step", "gdn_last_error", "gdn_get_device_status", "gdn_launch_count")
 
 _lock = threading.Lock()
 _lib = None
@@ -54,6 +54,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gdn_prefill.argtypes = [vp, vp, vp, vp, vp, f, i, i, i, i, i, i, i, vp, i, vp,
                                     vp, sz, vp]
         lib.gdn_prefill.restype = i
+        lib.gdn_prefill_noalloc.argtypes = [vp, vp, vp, vp, vp, f, i, i, i, i, i, i, i, vp, i,
+                                            vp, vp]
+        lib.gdn_prefill_noalloc.restype = i
         lib.gdn_decode_step.argtypes = [vp] * 12 + [i] * 4 + [vp]
         lib.gdn_decode_step.restype = i
         lib.gdn_last_error.argtypes = []
@@ -149,6 +152,33 @@ def gdn_prefill(q, k, v, g_log, beta, scale, state=None, out=None, workspace=Non
         _ptr(q), _ptr(k), _ptr(v), _ptr(g_log), _ptr(beta), float(scale), code, B, Hk, Hv, S,
         Dk, Dv, _ptr(state), int(state_is_input), _ptr(out), _ptr(workspace), wbytes,
         _stream(stream)))
+    return out, state
+
+
+def gdn_prefill_noalloc(q, k, v, g_log, beta, scale, state=None, out=None, stream=None):
+    """As gdn_prefill, through the entry point that uses the library's own static scratch
+    instead of a workspace (calls must not run concurrently)."""
+    B, Hk, S, Dk = q.shape
+    Hv, Dv = v.shape[1], v.shape[3]
+    dev, dt = q.device, q.dtype
+    if dt not in (torch.float32, torch.bfloat16):
+        raise ValueError("q must be float32 or bfloat16")
+    _need(q, "q", dt, (B, Hk, S, Dk), dev)
+    _need(k, "k", dt, (B, Hk, S, Dk), dev)
+    _need(v, "v", dt, (B, Hv, S, Dv), dev)
+    _need(g_log, "g_log", torch.float32, (B, Hv, S), dev)
+    _need(beta, "beta", torch.float32, (B, Hv, S), dev)
+    state_is_input = state is not None
+    if state is None:
+        state = torch.empty((B, Hv, Dk, Dv), dtype=torch.float32, device=dev)
+    _need(state, "state", torch.float32, (B, Hv, Dk, Dv), dev)
+    if out is None:
+        out = torch.empty((B, Hv, S, Dv), dtype=dt, device=dev)
+    _need(out, "out", dt, (B, Hv, S, Dv), dev)
+    code = GDN_DTYPE_BF16 if dt == torch.bfloat16 else GDN_DTYPE_F32
+    _check(load_library().gdn_prefill_noalloc(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g_log), _ptr(beta), float(scale), code, B, Hk, Hv, S,
+        Dk, Dv, _ptr(state), int(state_is_input), _ptr(out), _stream(stream)))
     return out, state
 
 

@@ -68,8 +68,25 @@ def test_prefill_rejects_bad_arguments(lib, kw, msg):
 
 def test_workspace_query(lib):
     assert lib.gdn_prefill_workspace_bytes(1, 3, 4, 64, 128, 128, 1) == ctypes.c_size_t(-1).value
-    n = lib.gdn_prefill_workspace_bytes(1, 16, 32, 8192, 128, 128, 1)
-    assert n != ctypes.c_size_t(-1).value
+    # tensor-core path: 66560 bytes per (batch, value head, 64-token chunk), ragged tail
+    # rounded up; the fp32 and other-head-dim paths need none
+    assert lib.gdn_prefill_workspace_bytes(1, 16, 32, 8192, 128, 128, 1) == 32 * 128 * 66560
+    assert lib.gdn_prefill_workspace_bytes(2, 1, 3, 65, 128, 128, 1) == 2 * 3 * 2 * 66560
+    assert lib.gdn_prefill_workspace_bytes(1, 16, 32, 8192, 128, 128, 0) == 0
+    assert lib.gdn_prefill_workspace_bytes(1, 16, 32, 8192, 64, 128, 1) == 0
+
+
+def test_prefill_requires_its_workspace(lib):
+    assert _prefill(lib) == gdn.GDN_EINVAL
+    assert "workspace" in lib.gdn_last_error().decode()
+
+
+def test_noalloc_rejects_more_heads_than_its_scratch(lib):
+    vp = ctypes.c_void_p
+    rc = lib.gdn_prefill_noalloc(vp(16), vp(16), vp(16), vp(16), vp(16), 1.0, 1, 1, 1, 4096,
+                                 64, 128, 128, vp(16), 0, vp(16), None)
+    assert rc == gdn.GDN_EUNSUPPORTED
+    assert "static scratch" in lib.gdn_last_error().decode()
 
 
 @pytest.mark.parametrize("kw,msg", [
