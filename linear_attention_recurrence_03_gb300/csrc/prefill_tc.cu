@@ -188,7 +188,7 @@ struct CarryCfg {
 // FULLE/EMPTYE: the early copy group of stage s; FULLL/EMPTYL: the late group
 enum {
     B_FULLE0 = 0, B_FULLE1, B_FULLL0, B_FULLL1, B_EMPTYE0, B_EMPTYE1, B_EMPTYL0, B_EMPTYL1,
-    B_ADONE, B_SDONE, B_CDONE, B_DRAIN, B_COUNT
+    B_ADONE, B_SDONE, B_CDONE, B_DRAIN, B_UREADY, B_SREADY, B_COUNT
 };
 
 // status bits
@@ -830,7 +830,8 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
     const int nch = a.nseg;  // chunks of this launch: a.c0 .. a.c0 + nch - 1
 
     if (tid == 0) {
-        for (int i = 0; i < B_COUNT; ++i) mbar_init(&bar[i], 1);
+        for (int i = 0; i < B_COUNT; ++i)
+            mbar_init(&bar[i], (i == B_UREADY || i == B_SREADY) ? 8 : 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -931,9 +932,7 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
             }
 #pragma unroll
             for (int p = 0; p < NP; ++p) write_row32(s_base + 16384u * pblk(p), L, pch(p), Sr + 32 * p);
-            fence_proxy_async_smem();
         }
-        tc_fence_before();
 
         // out = scale (Q~ S0 + P U) of chunk cc for token L - 64 (quadrants 2, 3)
         auto write_out = [&](int cc) {
@@ -959,37 +958,43 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
         };
 
         int mmas = 0, done = 0;
-        bool landed = true;   // leader: chunk c has landed and U~(c) is issued
-        bool u_next = false;  // leader: U~(c+1) already issued
+        // SIMT warp -> issuer hand-offs (mbarriers, one arrival per SIMT warp):
+        //   SREADY #c: the state tile of chunk c is written (#0: the initial state) and the
+        //              output of chunk c-2 is read out of its TMEM buffer
+        //   UREADY #c: U of chunk c is in its tile and the output of chunk c-1 is written
+        auto warp_arrive = [&](int bi) {
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[bi]);
+        };
+        if (!issuer) warp_arrive(B_SREADY);
+        bool ok = true;
         if (leader) {
-            landed = wait_or_abort(&bar[B_FULLE0], 0, abort_flag, ST_MMA);
-            if (landed) {
+            bool u_next = false;  // U~(c+1) already issued
+            ok = wait_or_abort(&bar[B_FULLE0], 0, abort_flag, ST_MMA);
+            if (ok) {
                 tc_fence_after();
                 issue_u<NS>(tmem, sbase, Cfg::TMB);
                 mmas = 1;
             }
-        }
-        for (int c = 0; c < nch; ++c) {
-            const int s = c & 1;
-            const uint32_t st = sbase + s * Cfg::STAGE;
-            const uint32_t ta = Cfg::TMA + (uint32_t)NS * (uint32_t)s;
-            const uint32_t tb = Cfg::TMB + (uint32_t)NS * (uint32_t)s;
-            const uint32_t ut = u_tile + Cfg::UT * (uint32_t)s;  // U tile of chunk c
-            // the state tile is complete: MMA1 [W; Q~] S0. (A thread that gives up sets the
-            // abort flag before it arrives, so every thread reads the same flag after the
-            // barrier.)
-            if (!landed && !*abort_flag) record_failure(abort_flag, ST_MMA);
-            bar_sync(1, 288);
-            if (*abort_flag) break;
-            if (leader) {
+            for (int c = 0; ok && c < nch; ++c) {
+                const int s = c & 1;
+                const uint32_t st = sbase + s * Cfg::STAGE;
+                const uint32_t ta = Cfg::TMA + (uint32_t)NS * (uint32_t)s;
+                const uint32_t tb = Cfg::TMB + (uint32_t)NS * (uint32_t)s;
+                // MMA1 [W; Q~] S0 once the state tile of chunk c is complete
+                if (!wait_or_abort(&bar[B_SREADY], c & 1, abort_flag, ST_MMA)) break;
                 TRACE(c, 12);
                 tc_fence_after();
                 issue_carry1<NS>(tmem, st, s_base, ta);
-                tc_commit(&bar[B_ADONE]);        // also covers U~(c), issued earlier
+                // ADONE also covers U~(c) and P U(c-1), issued earlier (U of chunk c may
+                // overwrite the U tile P U(c-2) read)
+                tc_commit(&bar[B_ADONE]);
                 tc_commit(&bar[B_EMPTYE0 + s]);  // the early group of chunk c is read
                 TRACE(c, 3);
-                // U~(c+1) now if chunk c+1 has landed; its buffer was last read by the
-                // state update of chunk c-1
+                // U~(c+1) now if chunk c+1 has landed (it then runs while U is formed); its
+                // buffer was last read by the state update of chunk c-1
                 u_next = c + 1 < nch &&
                          mbar_test_wait(&bar[B_FULLE0 + (s ^ 1)], ((c + 1) >> 1) & 1);
                 if (u_next) {
@@ -997,96 +1002,93 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
                                 Cfg::TMB + (uint32_t)NS * (uint32_t)(s ^ 1));
                     TRACE(c + 1, 5);
                 }
+                // K~^T U once U of chunk c is formed, then P U
+                ok = wait_or_abort(&bar[B_UREADY], c & 1, abort_flag, ST_MMA) &&
+                     wait_or_abort(&bar[B_FULLL0 + s], (c >> 1) & 1, abort_flag, ST_MMA);
+                if (!ok) break;
+                TRACE(c, 14);
+                tc_fence_after();
+                const uint32_t ut = u_tile + Cfg::UT * (uint32_t)s;
+                issue_carry3<NS>(tmem, st, ut, tb);  // U~(c) is consumed
+                tc_commit(&bar[B_SDONE]);
+                TRACE(c, 9);
+                if (c + 1 < nch && !u_next) {
+                    ok = wait_or_abort(&bar[B_FULLE0 + (s ^ 1)], ((c + 1) >> 1) & 1, abort_flag,
+                                       ST_MMA);
+                    if (!ok) break;
+                    issue_u<NS>(tmem, sbase + (s ^ 1) * Cfg::STAGE,
+                                Cfg::TMB + (uint32_t)NS * (uint32_t)(s ^ 1));
+                    TRACE(c + 1, 5);
+                }
+                issue_carry2<NS>(tmem, st, ut, ta);
+                tc_commit(&bar[B_CDONE]);
+                tc_commit(&bar[B_EMPTYL0 + s]);  // the late group of chunk c is read
+                TRACE(c, 4);
+                done = c + 1;
             }
-            bool ok = true;
-            if (!issuer) {
+        } else if (!issuer) {
+            for (int c = 0; c < nch; ++c) {
+                const int s = c & 1;
+                const uint32_t ta = Cfg::TMA + (uint32_t)NS * (uint32_t)s;
+                const uint32_t tb = Cfg::TMB + (uint32_t)NS * (uint32_t)s;
+                // Gamma_last of the chunk (late group) is read before this warp's UREADY:
+                // the stage's late group is reloaded only after P U, which follows it
+                ok = wait_or_abort(&bar[B_FULLL0 + s], (c >> 1) & 1, abort_flag, ST_CARRY);
+                if (!ok) break;
+                const float Gl = scal[s].Gl;
                 if (q >= 2) {
                     // the output of chunk c-1, once its P U is complete
-                    ok = c == 0 ||
-                         wait_or_abort(&bar[B_CDONE], (c - 1) & 1, abort_flag, ST_CARRY);
-                    if (ok && c > 0) {
+                    if (c > 0) {
+                        ok = wait_or_abort(&bar[B_CDONE], (c - 1) & 1, abort_flag, ST_CARRY);
+                        if (!ok) break;
                         tc_fence_after();
                         write_out(c - 1);
                     }
                 } else {
                     ok = wait_or_abort(&bar[B_ADONE], c & 1, abort_flag, ST_CARRY);
-                    if (ok) {
-                        if (warp == 4 && lane == 0) TRACE(c, 13);
-                        tc_fence_after();
-                        // U = U~ - W S0 for token L
-#pragma unroll
-                        for (int p = 0; p < NP; ++p) {
-                            float ws[32], uv[32];
-                            tmem_ld32x2(tmem + lane_off + ta + 32 * p, tmem + lane_off + tb + 32 * p,
-                                        ws, uv);
-                            uint32_t u[16];
-#pragma unroll
-                            for (int j = 0; j < 16; ++j)
-                                u[j] = pack_bf16(uv[2 * j] - ws[2 * j], uv[2 * j + 1] - ws[2 * j + 1]);
-                            write_row32_packed(ut + 8192u * pblk(p), L, pch(p), u);
-                        }
-                    }
-                }
-                fence_proxy_async_smem();
-                tc_fence_before();
-                if (lane == 0 && (warp == 4 || warp == 6)) TRACE(c, warp == 4 ? 11 : 17);
-                if (lane == 0) TRACE(c, 26 + (warp - 4));
-            }
-            if (leader) TRACE(c, 34);
-            if (!ok && !*abort_flag) record_failure(abort_flag, ST_CARRY);
-            bar_sync(1, 288);
-            if (*abort_flag) break;
-            if (leader) {
-                TRACE(c, 14);
-                ok = wait_or_abort(&bar[B_FULLL0 + s], (c >> 1) & 1, abort_flag, ST_MMA);
-                tc_fence_after();
-                if (ok) issue_carry3<NS>(tmem, st, ut, tb);  // U~(c) is consumed
-                tc_commit(&bar[B_SDONE]);
-                TRACE(c, 9);
-                // P U of chunk c (its output is written while U of chunk c+1 is formed)
-                if (ok) issue_carry2<NS>(tmem, st, ut, ta);
-                tc_commit(&bar[B_CDONE]);
-                tc_commit(&bar[B_EMPTYL0 + s]);  // the late group of chunk c is read
-                if (c + 1 < nch && !u_next) {
-                    landed = wait_or_abort(&bar[B_FULLE0 + (s ^ 1)], ((c + 1) >> 1) & 1,
-                                           abort_flag, ST_MMA);
-                    TRACE(c, 8);
-                    if (landed) {
-                        issue_u<NS>(tmem, sbase + (s ^ 1) * Cfg::STAGE,
-                                    Cfg::TMB + (uint32_t)NS * (uint32_t)(s ^ 1));
-                        TRACE(c + 1, 5);
-                    }
-                }
-                if (!ok) landed = false;  // the late group never landed: stop at the top
-                TRACE(c, 4);
-            }
-            if (!issuer) {
-                // S1 = Gamma_last S0 + K~^T U for state row L (the late group holds
-                // Gamma_last; it stays until P U of this chunk completes)
-                ok = wait_or_abort(&bar[B_SDONE], c & 1, abort_flag, ST_CARRY) &&
-                     wait_or_abort(&bar[B_FULLL0 + s], (c >> 1) & 1, abort_flag, ST_CARRY);
-                if (ok) {
-                    if (warp == 4 && lane == 0) TRACE(c, 15);
-                    const float Gl = scal[s].Gl;
+                    if (!ok) break;
+                    if (warp == 4 && lane == 0) TRACE(c, 13);
                     tc_fence_after();
+                    // U = U~ - W S0 for token L
+                    const uint32_t ut = u_tile + Cfg::UT * (uint32_t)s;
 #pragma unroll
                     for (int p = 0; p < NP; ++p) {
-                        float d[32];
-                        tmem_ld32(tmem + lane_off + tb + 32 * p, d);
+                        float ws[32], uv[32];
+                        tmem_ld32x2(tmem + lane_off + ta + 32 * p, tmem + lane_off + tb + 32 * p,
+                                    ws, uv);
+                        uint32_t u[16];
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) Sr[32 * p + j] = fmaf(Gl, Sr[32 * p + j], d[j]);
-                        write_row32(s_base + 16384u * pblk(p), L, pch(p), Sr + 32 * p);
+                        for (int j = 0; j < 16; ++j)
+                            u[j] = pack_bf16(uv[2 * j] - ws[2 * j], uv[2 * j + 1] - ws[2 * j + 1]);
+                        write_row32_packed(ut + 8192u * pblk(p), L, pch(p), u);
                     }
-                    fence_proxy_async_smem();
-                    if (warp == 4 && lane == 0) TRACE(c, 16);
                 }
-                tc_fence_before();
+                if (lane == 0 && (warp == 4 || warp == 6)) TRACE(c, warp == 4 ? 11 : 17);
+                warp_arrive(B_UREADY);
+                // S1 = Gamma_last S0 + K~^T U for state row L
+                ok = wait_or_abort(&bar[B_SDONE], c & 1, abort_flag, ST_CARRY);
+                if (!ok) break;
+                if (warp == 4 && lane == 0) TRACE(c, 15);
+                tc_fence_after();
+#pragma unroll
+                for (int p = 0; p < NP; ++p) {
+                    float d[32];
+                    tmem_ld32(tmem + lane_off + tb + 32 * p, d);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) Sr[32 * p + j] = fmaf(Gl, Sr[32 * p + j], d[j]);
+                    write_row32(s_base + 16384u * pblk(p), L, pch(p), Sr + 32 * p);
+                }
+                if (warp == 4 && lane == 0) TRACE(c, 16);
+                warp_arrive(B_SREADY);
+                done = c + 1;
             }
-            done = c + 1;
         }
-        if (done < nch && !*abort_flag) record_failure(abort_flag, ST_CARRY);
+        // every role of the carry group decides the epilogue together (lanes 1-31 of the
+        // issuer warp only take part in this barrier)
+        if ((leader || !issuer) && (!ok || done < nch) && !*abort_flag)
+            record_failure(abort_flag, ST_CARRY);
         bar_sync(1, 288);
-        bool ok = !*abort_flag;
+        ok = !*abort_flag;
         if (ok && !issuer && q >= 2) {
             // the output of the last chunk
             ok = wait_or_abort(&bar[B_CDONE], (nch - 1) & 1, abort_flag, ST_CARRY);
