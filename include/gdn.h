@@ -52,8 +52,8 @@ typedef enum gdn_dtype {
 /*
  * gdn_prefill_workspace_bytes -- scratch (device memory) gdn_prefill needs for this
  * shape. Returns 0 when no workspace is needed, or (size_t)-1 if the shape is invalid.
- * The bf16 path with Dk = Dv = 128 (the tensor-core kernels) needs 32768 bytes per
- * (batch, value head, 64-token chunk): B * Hv * ceil(S / 64) * 32768; every other
+ * The bf16 path with Dk = Dv = 128 (the tensor-core kernels) needs 66560 bytes per
+ * (batch, value head, 64-token chunk): B * Hv * ceil(S / 64) * 66560; every other
  * shape needs none.
  */
 size_t gdn_prefill_workspace_bytes(int B, int Hk, int Hv, int S, int Dk, int Dv,

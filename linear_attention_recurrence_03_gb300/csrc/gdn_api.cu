@@ -89,7 +89,7 @@ gdn_status gdn_prefill(const void* q, const void* k, const void* v, const float*
     int launched = 0;
     const bool bf16 = dtype == GDN_DTYPE_BF16;
     const cudaError_t e = gdn::prefill_tc_supported(a, bf16)
-                              ? gdn::launch_prefill_tc(a, 0, (S + 63) / 64, s, &launched)
+                              ? gdn::launch_prefill_tc_overlapped(a, s, &launched)
                               : gdn::launch_prefill_simt(a, bf16, s, &launched);
     g_launches += (unsigned long long)launched;
     if (e != cudaSuccess)

@@ -55,7 +55,7 @@ cudaError_t launch_prefill_simt(const PrefillArgs& a, bool bf16, cudaStream_t st
                                 int* launched);
 
 // tcgen05 chunked prefill (bf16, Dk = Dv = 128, S > 0): a parallel prep kernel writes
-// 32 KB of operand tiles per (batch, value head, 64-token chunk) to the workspace, then a
+// 65 KB of operand tiles per (batch, value head, 64-token chunk) to the workspace, then a
 // carry kernel runs the sequential part. *launched receives the kernels enqueued.
 bool prefill_tc_supported(const PrefillArgs& a, bool bf16);
 size_t prefill_tc_workspace_bytes(int B, int Hv, int S);
@@ -64,6 +64,13 @@ size_t prefill_tc_unit_bytes();
 // B * Hv * nseg units; the state carries over between consecutive calls.
 cudaError_t launch_prefill_tc(const PrefillArgs& a, int c0, int nseg, cudaStream_t stream,
                               int* launched);
+// The whole sequence with a workspace of B * Hv * ceil(S / 64) units, in segments of
+// prefill_tc_segment_chunks(...) chunks when the carry leaves SMs free: the prep of
+// segment j + 1 (helper stream, low priority) then runs beside the carry of segment j
+// (helper stream, high priority), forked from and joined back to `stream` by events.
+cudaError_t launch_prefill_tc_overlapped(const PrefillArgs& a, cudaStream_t stream,
+                                         int* launched);
+int prefill_tc_segment_chunks(int B, int Hv, int nch, int sms);
 
 // Fused decode step.
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);

@@ -39,6 +39,7 @@
 // its own copies and MMAs, frees TMEM and returns.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "internal.h"
@@ -89,6 +90,14 @@ using namespace ptx;
 
 constexpr int C = 64;    // chunk length
 constexpr uint64_t kWaitNs = 2000000000ull;
+
+// Overlapped schedule (the prep of the next segment of the sequence runs beside the carry
+// of the current one): at most this many segments, of at least kMinSegmentChunks chunks.
+#ifndef GDN_OVERLAP_SEGMENTS
+#define GDN_OVERLAP_SEGMENTS 2
+#endif
+constexpr int kOverlapSegments = GDN_OVERLAP_SEGMENTS;
+constexpr int kMinSegmentChunks = 8;
 
 // ---- workspace: per (batch, value head, chunk) unit, eight bf16 tiles of 64 rows x 64
 // columns in the 128-byte swizzled layout, T_U | P | W[:, 0:64] | W[:, 64:128] |
@@ -1161,47 +1170,181 @@ size_t prefill_tc_workspace_bytes(int B, int Hv, int S) {
 
 size_t prefill_tc_unit_bytes() { return WS_UNIT; }
 
+namespace {
+
+// The two kernels of one segment of the sequence (chunks c0 .. c0 + nseg - 1), whose
+// B Hv nseg workspace units start at `ws`.
+struct SegmentLaunch {
+    CUtensorMap mq, mk, mv;
+    const PrefillArgs* a;
+    int sms;
+
+    TcArgs args(int c0, int nseg, uint8_t* ws) const {
+        const int sin = (c0 > 0 || a->state_is_input) ? 1 : 0;
+        return TcArgs{a->g,     a->beta, a->scale, a->B, a->Hk,  a->Hv,
+                      a->S,     c0,      nseg,     a->state, sin,
+                      static_cast<__nv_bfloat16*>(a->out), ws};
+    }
+    // two carry CTAs per head (64-column state slices) while that still fits the GPU in
+    // one wave, else one CTA per head (128 columns: half the MMA instructions per head)
+    bool split() const { return 2 * a->B * a->Hv <= sms; }
+
+    cudaError_t prep(int c0, int nseg, uint8_t* ws, cudaStream_t st) const {
+        prep_tc_kernel<<<dim3(nseg, a->Hv, a->B), PREP_THREADS, PREP_SMEM, st>>>(
+            mq, mk, args(c0, nseg, ws));
+        return cudaGetLastError();
+    }
+    cudaError_t carry(int c0, int nseg, uint8_t* ws, cudaStream_t st) const {
+        if (split())
+            carry_tc_kernel<64><<<dim3(2, a->Hv, a->B), CARRY_THREADS, CarryCfg<64>::SMEM, st>>>(
+                mv, args(c0, nseg, ws));
+        else
+            carry_tc_kernel<128>
+                <<<dim3(1, a->Hv, a->B), CARRY_THREADS, CarryCfg<128>::SMEM, st>>>(
+                    mv, args(c0, nseg, ws));
+        return cudaGetLastError();
+    }
+};
+
+cudaError_t set_attributes() {
+    static cudaError_t e = [] {
+        cudaError_t r = cudaFuncSetAttribute(
+            prep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PREP_SMEM);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(carry_tc_kernel<64>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)CarryCfg<64>::SMEM);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(carry_tc_kernel<128>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)CarryCfg<128>::SMEM);
+        return r;
+    }();
+    return e;
+}
+
+// Per-device streams and events of the overlapped schedule: the prep kernels run on a
+// low-priority stream, the carry kernels on a high-priority one, both forked from and
+// joined back to the caller's stream with events.
+struct Overlap {
+    std::mutex mu;
+    bool ready = false;
+    cudaStream_t prep = nullptr, carry = nullptr;
+    cudaEvent_t fork = nullptr, prepped = nullptr, joined = nullptr;
+};
+
+Overlap* overlap_for(int dev) {
+    constexpr int kMaxDevices = 64;
+    static Overlap tab[kMaxDevices];
+    return (dev >= 0 && dev < kMaxDevices) ? &tab[dev] : nullptr;
+}
+
+cudaError_t overlap_init(Overlap& o) {
+    if (o.ready) return cudaSuccess;
+    int least = 0, greatest = 0;
+    cudaError_t e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
+    if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&o.prep, cudaStreamNonBlocking, least);
+    if (e == cudaSuccess)
+        e = cudaStreamCreateWithPriority(&o.carry, cudaStreamNonBlocking, greatest);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&o.fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&o.prepped, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&o.joined, cudaEventDisableTiming);
+    o.ready = e == cudaSuccess;
+    return e;
+}
+
+cudaError_t prepare(SegmentLaunch& L, const PrefillArgs& a) {
+    L.a = &a;
+    if (!encode_3d(&L.mq, a.q, a.S, a.B * a.Hk) || !encode_3d(&L.mk, a.k, a.S, a.B * a.Hk) ||
+        !encode_3d(&L.mv, a.v, a.S, a.B * a.Hv))
+        return cudaErrorInvalidValue;
+    cudaError_t e = set_attributes();
+    if (e != cudaSuccess) return e;
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&L.sms, cudaDevAttrMultiProcessorCount, dev);
+    return e;
+}
+
+}  // namespace
+
+int prefill_tc_segment_chunks(int B, int Hv, int nch, int sms) {
+    // The carry of a segment occupies 2 B Hv SMs (one CTA each) for the whole segment;
+    // the prep of the next segment runs meanwhile on the SMs left over. Without enough
+    // of those, or with too few chunks, one segment.
+    const int carry_sms = 2 * B * Hv;
+    if (carry_sms > sms || sms - carry_sms < sms / 4 || nch < 2 * kMinSegmentChunks) return nch;
+    const int g = std::min(kOverlapSegments, nch / kMinSegmentChunks);
+    return (nch + g - 1) / g;
+}
+
 cudaError_t launch_prefill_tc(const PrefillArgs& a, int c0, int nseg, cudaStream_t stream,
                               int* launched) {
     *launched = 0;
     if (a.workspace == nullptr || nseg < 1 ||
         a.workspace_bytes < (size_t)a.B * (size_t)a.Hv * (size_t)nseg * WS_UNIT)
         return cudaErrorInvalidValue;
-    CUtensorMap mq, mk, mv;
-    if (!encode_3d(&mq, a.q, a.S, a.B * a.Hk) || !encode_3d(&mk, a.k, a.S, a.B * a.Hk) ||
-        !encode_3d(&mv, a.v, a.S, a.B * a.Hv))
-        return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(prep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)PREP_SMEM);
+    SegmentLaunch L{};
+    cudaError_t e = prepare(L, a);
     if (e != cudaSuccess) return e;
-    TcArgs t{a.g,  a.beta, a.scale, a.B, a.Hk, a.Hv, a.S, c0, nseg, a.state, a.state_is_input,
-             static_cast<__nv_bfloat16*>(a.out), static_cast<uint8_t*>(a.workspace)};
-    prep_tc_kernel<<<dim3(nseg, a.Hv, a.B), PREP_THREADS, PREP_SMEM, stream>>>(mq, mk, t);
-    e = cudaGetLastError();
+    uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+    e = L.prep(c0, nseg, ws, stream);
     if (e != cudaSuccess) return e;
     *launched = 1;
-    // two CTAs per head (64-column state slices) while that still fits the GPU in one
-    // wave, else one CTA per head (128 columns: half the MMA instructions per head)
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const bool split = 2 * a.B * a.Hv <= sms;
-    if (split) {
-        e = cudaFuncSetAttribute(carry_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)CarryCfg<64>::SMEM);
-        if (e != cudaSuccess) return e;
-        carry_tc_kernel<64><<<dim3(2, a.Hv, a.B), CARRY_THREADS, CarryCfg<64>::SMEM, stream>>>(
-            mv, t);
-    } else {
-        e = cudaFuncSetAttribute(carry_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)CarryCfg<128>::SMEM);
-        if (e != cudaSuccess) return e;
-        carry_tc_kernel<128><<<dim3(1, a.Hv, a.B), CARRY_THREADS, CarryCfg<128>::SMEM, stream>>>(
-            mv, t);
-    }
-    e = cudaGetLastError();
+    e = L.carry(c0, nseg, ws, stream);
     if (e == cudaSuccess) *launched = 2;
     return e;
+}
+
+cudaError_t launch_prefill_tc_overlapped(const PrefillArgs& a, cudaStream_t stream,
+                                         int* launched) {
+    *launched = 0;
+    const int nch = (a.S + C - 1) / C;
+    if (a.workspace == nullptr || nch < 1 ||
+        a.workspace_bytes < (size_t)a.B * (size_t)a.Hv * (size_t)nch * WS_UNIT)
+        return cudaErrorInvalidValue;
+    SegmentLaunch L{};
+    cudaError_t e = prepare(L, a);
+    if (e != cudaSuccess) return e;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int seg = prefill_tc_segment_chunks(a.B, a.Hv, nch, L.sms);
+    Overlap* o = overlap_for(dev);
+    uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+    if (seg >= nch || o == nullptr) {
+        e = L.prep(0, nch, ws, stream);
+        if (e != cudaSuccess) return e;
+        *launched = 1;
+        e = L.carry(0, nch, ws, stream);
+        if (e == cudaSuccess) *launched = 2;
+        return e;
+    }
+    std::lock_guard<std::mutex> lock(o->mu);
+    e = overlap_init(*o);
+    if (e != cudaSuccess) return e;
+    // fork: both helper streams start after the caller's earlier work
+    e = cudaEventRecord(o->fork, stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(o->prep, o->fork, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(o->carry, o->fork, 0);
+    if (e != cudaSuccess) return e;
+    // prep of segment j+1 overlaps the carry of segment j; each carry waits for its prep
+    // (a wait takes the event's latest record at the time it is enqueued)
+    cudaError_t le = cudaSuccess;
+    for (int c0 = 0; c0 < nch && le == cudaSuccess; c0 += seg) {
+        const int n = std::min(seg, nch - c0);
+        uint8_t* wsj = ws + (size_t)a.B * (size_t)a.Hv * (size_t)c0 * WS_UNIT;
+        le = L.prep(c0, n, wsj, o->prep);
+        if (le != cudaSuccess) break;
+        ++*launched;
+        le = cudaEventRecord(o->prepped, o->prep);
+        if (le == cudaSuccess) le = cudaStreamWaitEvent(o->carry, o->prepped, 0);
+        if (le == cudaSuccess) le = L.carry(c0, n, wsj, o->carry);
+        if (le == cudaSuccess) ++*launched;
+    }
+    // join, also after a failed launch, so that no work is left outside the caller's stream
+    e = cudaEventRecord(o->joined, o->carry);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, o->joined, 0);
+    return le != cudaSuccess ? le : e;
 }
 
 }  // namespace gdn

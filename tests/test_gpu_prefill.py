@@ -166,6 +166,28 @@ def test_prefill_noalloc_equals_prefill_one_segment():
     assert torch.equal(o1, o2) and torch.equal(s1, s2)
 
 
+def test_prefill_overlapped_segments_equal_one_pass():
+    """Few heads and a long sequence: gdn_prefill runs the sequence as several segments,
+    the prep of each beside the carry of the one before (two helper streams). The state
+    crosses segments in fp32, so the result equals the one-segment run (the static
+    scratch of gdn_prefill_noalloc holds this whole sequence) bit for bit, and matches the
+    oracle on sampled heads."""
+    w = syn.shrink(syn.PREFILL_BF16_GQA2, B=1, Hk=4, Hv=8, S=64 * 40 - 17, state_std=0.05)
+    x = syn.prefill_inputs(w)
+    args = [x[n].to(DEV) for n in ("q", "k", "v", "g_log", "beta")]
+    st0 = x["state"].to(DEV)
+    n0 = gdn.gdn_launch_count()
+    o1, s1 = gdn.gdn_prefill(*args, x["scale"], state=st0.clone())
+    assert gdn.gdn_launch_count() - n0 > 2  # more than one segment
+    o2, s2 = gdn.gdn_prefill_noalloc(*args, x["scale"], state=st0.clone())
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(s1, s2)
+    ref = oracle_prefill_heads(x, [(0, 0), (0, 5)])
+    for (b, h), (o_ref, s_ref) in ref.items():
+        assert rel(to_np(o1[b, h]), o_ref) <= TOL_BF16["out"]
+        assert rel(to_np(s1[b, h]), s_ref) <= TOL_BF16["state"]
+
+
 def test_prefill_noalloc_many_segments():
     """B*Hv = 1024 leaves room for one 64-token chunk per (batch, head) in the static
     scratch, so S = 320 runs as five segments with the state carried between them: the
