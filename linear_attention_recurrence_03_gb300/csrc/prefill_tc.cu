@@ -796,7 +796,9 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
                     bulk_s2g(ws + WS_W + 8192, sb + PQ_STRIDE + PQ_Q, 8192);
                     bulk_s2g(ws + WS_CS, sb + P_CS, sizeof(CarryScalars));
                     bulk_commit();
-                    bulk_wait_all();
+                    // the CTA may exit once the tiles are read out of shared memory: the
+                    // carry, a later kernel, sees the global writes completed
+                    bulk_wait_read_all();
                 }
             }
         }
