@@ -48,6 +48,10 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-batched", action="store_true",
                    help="skip the extra B=8, S=4096 prefill measurement")
+    p.add_argument("--no-multi", action="store_true",
+                   help="skip the multi-token decode measurement (T = 2, 4, 8 tokens per call)")
+    p.add_argument("--no-conv", action="store_true",
+                   help="skip the conv1d decode measurement (B = 256, 8192 channels)")
     p.add_argument("--spinup-seconds", type=float, default=1.0,
                    help="untimed load before the warm-up, so clock samples see the GPU busy")
     return p.parse_args()
@@ -441,6 +445,95 @@ def run_gdn(args):
             "tensor_tflops": bf_ / (b_ms * 1e-3) / 1e12, "frac_of_roofline": rb / (b_ms * 1e-3),
             "l2": "working set 0.85 GB > L2"}
         del PB, b_state, b_out
+
+    # multi-token decode: T tokens of the BH = 8192 rows per call, state read and written
+    # once per call (in place)
+    if not args.no_multi:
+        multi = {}
+        m_state = D["state"]
+        for T in (2, 4, 8):
+            xm = syn.decode_multi_inputs(wd, T, seed=1)
+            M = {n: xm[n].to(dev) for n in ("q", "k", "v", "b", "a", "z")}
+            margs = [vp(M[n].data_ptr()) for n in ("q", "k", "v", "b", "a")] + [
+                vp(D["A_log"].data_ptr()), vp(D["dt_bias"].data_ptr()), vp(M["z"].data_ptr()),
+                vp(D["norm_weight"].data_ptr()), vp(m_state.data_ptr()),
+                vp(m_state.data_ptr())]
+            m_out = torch.empty((T, wd.BH, wd.V), dtype=torch.bfloat16, device=dev)
+
+            def decode_m():
+                rc = lib.gdn_decode_multi(*margs, vp(m_out.data_ptr()), T, wd.BH,
+                                          wd.num_v_heads, wd.K, wd.V, sptr)
+                if rc != 0:
+                    raise RuntimeError(gdn.gdn_last_error())
+
+            for _ in range(args.warmup):
+                decode_m()
+            torch.cuda.synchronize()
+            em0 = torch.cuda.Event(enable_timing=True)
+            em1 = torch.cuda.Event(enable_timing=True)
+            em0.record(stream)
+            for _ in range(K):
+                decode_m()
+            em1.record(stream)
+            torch.cuda.synchronize()
+            m_ms = reduce_max([em0.elapsed_time(em1) / K], ws)[0]
+            sb_, db_ = decode_bytes(wd)
+            mb = sb_ + T * (db_ - sb_)  # the state once, the per-token rows T times
+            multi[f"T{T}"] = {"ms": m_ms, "row_tokens_per_s": T * wd.BH / (m_ms * 1e-3),
+                              "achieved_gbs": mb / (m_ms * 1e-3) / 1e9,
+                              "frac_hbm": mb / (m_ms * 1e-3) / 1e9 / hbm,
+                              "speedup_vs_T_single_steps": T * d_ms / m_ms}
+            del M, m_out
+        result["decode_multi"] = {"workload": wd.name, "kernel": "decode.cu",
+                                  "api": "gdn_decode_multi", **multi}
+
+    # conv1d decode token in front of the decode step: B = 256, 8192 q|k|v channels,
+    # K_win = 4, window in place
+    if not args.no_conv:
+        wc = syn.CONV1D_B256
+        xc = syn.conv1d_inputs(wc)
+        CX = {n: xc[n].to(dev) for n in ("x", "conv_weight", "conv_state")}
+        cq = torch.empty((wc.B * wc.num_v_heads, wc.head_k_dim), dtype=torch.bfloat16,
+                         device=dev)
+        ck = torch.empty_like(cq)
+        cv = torch.empty((wc.B * wc.num_v_heads, wc.head_v_dim), dtype=torch.bfloat16,
+                         device=dev)
+        cargs = [vp(CX["x"].data_ptr()), vp(CX["conv_weight"].data_ptr()),
+                 vp(CX["conv_state"].data_ptr()), vp(CX["conv_state"].data_ptr()),
+                 vp(cq.data_ptr()), vp(ck.data_ptr()), vp(cv.data_ptr())]
+
+        def conv_c():
+            rc = lib.gdn_conv1d_decode(*cargs, wc.B, wc.num_k_heads, wc.num_v_heads,
+                                       wc.head_k_dim, wc.head_v_dim, wc.K_win, sptr)
+            if rc != 0:
+                raise RuntimeError(gdn.gdn_last_error())
+
+        for _ in range(args.warmup):
+            conv_c()
+        torch.cuda.synchronize()
+        # each call timed alone after a write of 256 MB (twice L2) so it reads HBM
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        evs = []
+        for _ in range(K):
+            flush.zero_()
+            ec0 = torch.cuda.Event(enable_timing=True)
+            ec1 = torch.cuda.Event(enable_timing=True)
+            ec0.record(stream)
+            conv_c()
+            ec1.record(stream)
+            evs.append((ec0, ec1))
+        torch.cuda.synchronize()
+        c_ms = reduce_max([sum(a.elapsed_time(b) for a, b in evs) / K], ws)[0]
+        del flush
+        cb = (wc.B * wc.conv_dim * 2 + wc.conv_dim * wc.K_win * 4
+              + 2 * wc.B * wc.conv_dim * wc.K_win * 2
+              + wc.B * wc.num_v_heads * (2 * wc.head_k_dim + wc.head_v_dim) * 2)
+        result["conv1d_decode"] = {
+            "workload": wc.name, "kernel": "conv1d.cu", "api": "gdn_conv1d_decode",
+            "ms": c_ms, "algorithmic_bytes": cb, "achieved_gbs": cb / (c_ms * 1e-3) / 1e9,
+            "frac_hbm": cb / (c_ms * 1e-3) / 1e9 / hbm,
+            "l2": "L2 flushed (256 MB written) before each timed call"}
+        del CX, cq, ck, cv
 
     # end to end through the binding, host buffers: H2D inputs, prefill, D2H out + state
     if not args.no_e2e:

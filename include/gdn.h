@@ -11,7 +11,10 @@
  * Sources (AWS Neuron NKI library API pages):
  *   "GDN CTE Kernel API Reference"  -- the chunked prefill (gdn_prefill).
  *   "GDN TKG Kernel API Reference"  -- the fused single-token decode step
- *                                      (gdn_decode_step).
+ *                                      (gdn_decode_step; gdn_decode_multi runs T
+ *                                      of them with the state kept on chip).
+ *   "GDN Block TKG Kernel API Reference" -- the conv1d decode token in front of the
+ *                                      decode step (gdn_conv1d_decode).
  *
  * Conventions for every call:
  *   - Pointers marked "device" are CUDA device pointers; the caller owns all memory.
@@ -142,6 +145,61 @@ gdn_status gdn_decode_step(const void* q, const void* k, const void* v, const vo
                            const void* z, const float* norm_weight, const float* state_in,
                            float* state_out, void* out, int BH, int num_v_heads, int K,
                            int V, void* stream);
+
+/*
+ * gdn_decode_multi -- T consecutive fused decode tokens of the same BH rows in one call:
+ * token t applies exactly the gdn_decode_step formulas to the state left by token t-1.
+ * Not on the pages (an extension of the "GDN TKG Kernel API Reference" step): the state
+ * is read once and written once, so its HBM traffic is shared by the T tokens.
+ *
+ *   q, k         device, [T, BH, K] bf16 raw (token-major: token t's rows at t * BH).
+ *   v, z         device, [T, BH, V] bf16.
+ *   b, a         device, [T, BH] bf16.
+ *   out          device, [T, BH, V] bf16.
+ *   A_log, dt_bias, norm_weight, state_in, state_out: as gdn_decode_step (state_out may
+ *                equal state_in). T == 1 is gdn_decode_step; T == 0 or BH == 0 enqueues
+ *                nothing.
+ *
+ * Errors: as gdn_decode_step, plus GDN_EINVAL for T < 0.
+ */
+gdn_status gdn_decode_multi(const void* q, const void* k, const void* v, const void* b,
+                            const void* a, const float* A_log, const float* dt_bias,
+                            const void* z, const float* norm_weight, const float* state_in,
+                            float* state_out, void* out, int T, int BH, int num_v_heads, int K,
+                            int V, void* stream);
+
+/*
+ * gdn_conv1d_decode -- the step in front of the decode step: one token of the q|k|v
+ * in_proj output through the depthwise causal convolution with its sliding window,
+ * SiLU, then the split into q | k | v with q and k repeated over the value heads
+ * ("GDN Block TKG Kernel API Reference": gdn_conv1d_decode -- conv + silu + slide-window
+ * state -- and "split conv_out + GQA-repeat q,k"; shapes from its parameters and
+ * Dimensions).
+ *
+ *   x              device, [B, conv_dim] bf16, conv_dim = 2 key_dim + value_dim with
+ *                  key_dim = num_k_heads * head_k_dim, value_dim = num_v_heads * head_v_dim
+ *                  (channels q | k | v, head-major within each).
+ *   conv_weight    device, [conv_dim, K_win] fp32 depthwise taps, oldest tap first.
+ *   conv_state_in  device, [B, conv_dim, K_win] bf16, the K_win latest inputs, oldest first.
+ *   conv_state_out device, [B, conv_dim, K_win] bf16, the window after this token. May
+ *                  equal conv_state_in (in place); must not otherwise overlap it.
+ *   q_out, k_out   device, [B * num_v_heads, head_k_dim] bf16 (row b * num_v_heads + h
+ *                  holds key head h / (num_v_heads / num_k_heads)): raw, not normalised --
+ *                  the form gdn_decode_step takes.
+ *   v_out          device, [B * num_v_heads, head_v_dim] bf16.
+ *   1 <= head_k_dim, head_v_dim <= 128; 1 <= K_win <= 16; B == 0 enqueues nothing.
+ *
+ * Per batch and channel: window' = (state[1..K_win-1], x); y = silu(sum_w weight[w]
+ * window'[w]) in fp32, rounded to bf16; state' = window'. The page gives the operation
+ * and shapes only: the window order and the absence of a bias are readings.
+ *
+ * Errors: GDN_EINVAL for a bad shape, a NULL/misaligned pointer or a partial overlap of
+ * the windows; GDN_ECUDA if the launch fails.
+ */
+gdn_status gdn_conv1d_decode(const void* x, const float* conv_weight, const void* conv_state_in,
+                             void* conv_state_out, void* q_out, void* k_out, void* v_out, int B,
+                             int num_k_heads, int num_v_heads, int head_k_dim, int head_v_dim,
+                             int K_win, void* stream);
 
 /* Message describing the calling thread's last non-GDN_OK status ("" if none). The
  * pointer stays valid until the thread's next call into the library. */

@@ -6,6 +6,9 @@ thin Python binding of the same names:
 * ``gdn_prefill``      -- chunked prefill ("GDN CTE Kernel API Reference").
 * ``gdn_prefill_noalloc`` -- the same, with the library's own static scratch.
 * ``gdn_decode_step``  -- fused single-token decode step ("GDN TKG Kernel API Reference").
+* ``gdn_decode_multi`` -- T consecutive decode tokens in one call (state read once).
+* ``gdn_conv1d_decode`` -- the conv1d decode token feeding the decode step ("GDN Block
+  TKG Kernel API Reference").
 """
 from .gdn import (  # noqa: F401
     EXPORTS,
@@ -17,6 +20,8 @@ from .gdn import (  # noqa: F401
     GDN_EUNSUPPORTED,
     GDN_OK,
     GDNError,
+    gdn_conv1d_decode,
+    gdn_decode_multi,
     gdn_decode_step,
     gdn_get_device_status,
     gdn_last_error,

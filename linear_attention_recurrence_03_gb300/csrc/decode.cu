@@ -17,6 +17,10 @@
 // columns (4l..4l+3 as one 16-byte vector when V == 128, else l, l+32, l+64, l+96).
 // Cross-warp sums go through shared memory in a fixed order, so results are bitwise
 // reproducible and do not depend on the grid ("LNC1 is byte-identical", Notes).
+//
+// Multi-token form (T consecutive steps of the same rows in one call; an extension, not
+// on the pages): the state stays in registers across the T tokens, so its 2 x 64 KB of
+// HBM traffic is paid once per call; token t's inputs sit at offset t * BH rows.
 #include "internal.h"
 
 namespace gdn {
@@ -61,6 +65,7 @@ __global__ void __launch_bounds__(NT, 2) decode_kernel(DecodeArgs a) {
     const int K = a.K, V = a.V;
     const float* S0 = a.state_in + (size_t)bh * K * V;
     float* S1 = a.state_out + (size_t)bh * K * V;
+    const size_t BH = (size_t)a.BH;
 
     // 1. issue the state loads first: 16 rows x 4 columns per thread
     float st[ROWS][4];
@@ -80,18 +85,39 @@ __global__ void __launch_bounds__(NT, 2) decode_kernel(DecodeArgs a) {
         }
     }
 
-    // 2. small per-row inputs
-    for (int i = tid; i < kMaxHeadDim; i += NT) {
-        s.qn[i] = i < K ? __bfloat162float(a.q[(size_t)bh * K + i]) : 0.f;
-        s.kn[i] = i < K ? __bfloat162float(a.k[(size_t)bh * K + i]) : 0.f;
-        s.v[i] = i < V ? __bfloat162float(a.v[(size_t)bh * V + i]) : 0.f;
-        s.z[i] = i < V ? __bfloat162float(a.z[(size_t)bh * V + i]) : 0.f;
+    // 2. small per-row inputs, token by token; thread i < 128 holds element i of the
+    // next token's q, k, v, z (and thread 0 its b, a) in registers, loaded one token
+    // ahead so that their latency hides behind the current token
+    float nq = 0.f, nk = 0.f, nv = 0.f, nz = 0.f, nb = 0.f, na = 0.f;
+    auto fetch = [&](int tok) {
+        const size_t row = (size_t)tok * BH + (size_t)bh;
+        if (tid < kMaxHeadDim) {
+            nq = tid < K ? __bfloat162float(a.q[row * K + tid]) : 0.f;
+            nk = tid < K ? __bfloat162float(a.k[row * K + tid]) : 0.f;
+            nv = tid < V ? __bfloat162float(a.v[row * V + tid]) : 0.f;
+            nz = tid < V ? __bfloat162float(a.z[row * V + tid]) : 0.f;
+        }
+        if (tid == 0) {
+            nb = __bfloat162float(a.b[row]);
+            na = __bfloat162float(a.a[row]);
+        }
+    };
+    fetch(0);
+    for (int tok = 0; tok < a.T; ++tok) {
+    if (tok > 0) __syncthreads();  // the previous token's shared inputs are read
+    const size_t row = (size_t)tok * BH + (size_t)bh;  // this token's input row
+    if (tid < kMaxHeadDim) {
+        s.qn[tid] = nq;
+        s.kn[tid] = nk;
+        s.v[tid] = nv;
+        s.z[tid] = nz;
     }
     if (tid == 0) {
-        s.scal[3] = sigmoid_f(__bfloat162float(a.b[bh]));
-        const float gg = -expf(a.A_log[h]) * softplus_f(__bfloat162float(a.a[bh]) + a.dt_bias[h]);
+        s.scal[3] = sigmoid_f(nb);
+        const float gg = -expf(a.A_log[h]) * softplus_f(na + a.dt_bias[h]);
         s.scal[4] = expf(gg);
     }
+    if (tok + 1 < a.T) fetch(tok + 1);
     __syncthreads();
     // 3. l2 norms of q and k (warps 0 and 1), then normalise
     if (w < 2) {
@@ -157,25 +183,31 @@ __global__ void __launch_bounds__(NT, 2) decode_kernel(DecodeArgs a) {
         ms /= (float)V;
         const float zj = s.z[tid];
         const float y = o * (1.f / sqrtf(ms + kEpsRms)) * a.norm_weight[tid] * (zj * sigmoid_f(zj));
-        a.out[(size_t)bh * V + tid] = __float2bfloat16_rn(y);
+        a.out[row * V + tid] = __float2bfloat16_rn(y);
     }
-    // 7. S' = alpha S + k^ u^T from registers
+    // 7. S' = alpha S + k^ u^T in registers (rows beyond K stay zero)
+#pragma unroll
+    for (int m = 0; m < ROWS; ++m) {
+        const int i = w + NWARP * m;
+        const float ki = s.kn[i];  // zero beyond K
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            st[m][c] = fmaf(alpha, st[m][c], ki * s.u[col_of<VEC4>(lane, c)]);
+    }
+    }  // tokens
+    // 8. the state, written once
 #pragma unroll
     for (int m = 0; m < ROWS; ++m) {
         const int i = w + NWARP * m;
         if (i >= K) continue;
-        const float ki = s.kn[i];
-        float r[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) r[c] = fmaf(alpha, st[m][c], ki * s.u[col_of<VEC4>(lane, c)]);
         if (VEC4) {
             __stcs(reinterpret_cast<float4*>(S1 + (size_t)i * V) + lane,
-                   make_float4(r[0], r[1], r[2], r[3]));
+                   make_float4(st[m][0], st[m][1], st[m][2], st[m][3]));
         } else {
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const int j = col_of<false>(lane, c);
-                if (j < V) __stcs(S1 + (size_t)i * V + j, r[c]);
+                if (j < V) __stcs(S1 + (size_t)i * V + j, st[m][c]);
             }
         }
     }
@@ -184,7 +216,7 @@ __global__ void __launch_bounds__(NT, 2) decode_kernel(DecodeArgs a) {
 }  // namespace
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
-    if (a.BH == 0) return cudaSuccess;
+    if (a.BH == 0 || a.T == 0) return cudaSuccess;
     if (a.V == kMaxHeadDim)
         decode_kernel<true><<<a.BH, NT, 0, stream>>>(a);
     else

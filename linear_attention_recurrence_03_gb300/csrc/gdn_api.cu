@@ -139,41 +139,111 @@ gdn_status gdn_prefill_noalloc(const void* q, const void* k, const void* v, cons
     return GDN_OK;
 }
 
-gdn_status gdn_decode_step(const void* q, const void* k, const void* v, const void* b,
-                           const void* a, const float* A_log, const float* dt_bias,
-                           const void* z, const float* norm_weight, const float* state_in,
-                           float* state_out, void* out, int BH, int num_v_heads, int K, int V,
-                           void* stream) {
-    if (BH < 0 || num_v_heads < 1 || BH % num_v_heads != 0)
-        return fail(GDN_EINVAL, "gdn_decode_step: need BH >= 0 and BH %% num_v_heads == 0 "
-                    "(got BH=%d num_v_heads=%d)", BH, num_v_heads);
+}  // extern "C"
+
+namespace {
+
+// The decode step, T tokens in a row: validation, then one launch.
+gdn_status decode_impl(const char* fn, const void* q, const void* k, const void* v,
+                       const void* b, const void* a, const float* A_log, const float* dt_bias,
+                       const void* z, const float* norm_weight, const float* state_in,
+                       float* state_out, void* out, int T, int BH, int num_v_heads, int K,
+                       int V, void* stream) {
+    if (T < 0 || BH < 0 || num_v_heads < 1 || BH % num_v_heads != 0)
+        return fail(GDN_EINVAL, "%s: need T >= 0, BH >= 0 and BH %% num_v_heads == 0 "
+                    "(got T=%d BH=%d num_v_heads=%d)", fn, T, BH, num_v_heads);
     if (K < 1 || K > gdn::kMaxHeadDim || V < 1 || V > gdn::kMaxHeadDim)
-        return fail(GDN_EINVAL, "gdn_decode_step: need 1 <= K, V <= %d (got K=%d V=%d)",
+        return fail(GDN_EINVAL, "%s: need 1 <= K, V <= %d (got K=%d V=%d)", fn,
                     gdn::kMaxHeadDim, K, V);
-    const bool rows = BH > 0;
+    const bool rows = BH > 0 && T > 0;
     if (!ptr_ok(q, rows) || !ptr_ok(k, rows) || !ptr_ok(v, rows) || !ptr_ok(b, rows) ||
         !ptr_ok(a, rows) || !ptr_ok(z, rows) || !ptr_ok(state_in, rows) ||
         !ptr_ok(state_out, rows) || !ptr_ok(out, rows) || !ptr_ok(A_log, true) ||
         !ptr_ok(dt_bias, true) || !ptr_ok(norm_weight, true))
-        return fail(GDN_EINVAL, "gdn_decode_step: every pointer must be a non-NULL, "
-                    "16-byte aligned device pointer");
+        return fail(GDN_EINVAL, "%s: every pointer must be a non-NULL, 16-byte aligned "
+                    "device pointer", fn);
     if (state_in != state_out && rows) {
         const uintptr_t i0 = reinterpret_cast<uintptr_t>(state_in);
         const uintptr_t o0 = reinterpret_cast<uintptr_t>(state_out);
         const uintptr_t n = (uintptr_t)BH * K * V * sizeof(float);
         if (i0 < o0 + n && o0 < i0 + n)
-            return fail(GDN_EINVAL, "gdn_decode_step: state_out overlaps state_in without "
-                        "being equal to it");
+            return fail(GDN_EINVAL, "%s: state_out overlaps state_in without being equal "
+                        "to it", fn);
     }
     gdn::DecodeArgs d{static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
                       static_cast<const __nv_bfloat16*>(v), static_cast<const __nv_bfloat16*>(b),
                       static_cast<const __nv_bfloat16*>(a), A_log, dt_bias,
                       static_cast<const __nv_bfloat16*>(z), norm_weight, state_in, state_out,
-                      static_cast<__nv_bfloat16*>(out), BH, num_v_heads, K, V};
+                      static_cast<__nv_bfloat16*>(out), BH, num_v_heads, K, V, T};
     const cudaError_t e = gdn::launch_decode(d, static_cast<cudaStream_t>(stream));
-    if (BH > 0) g_launches += 1;
+    if (rows) g_launches += 1;
     if (e != cudaSuccess)
-        return fail(GDN_ECUDA, "gdn_decode_step: launch failed: %s", cudaGetErrorString(e));
+        return fail(GDN_ECUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
+    return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_decode_step(const void* q, const void* k, const void* v, const void* b,
+                           const void* a, const float* A_log, const float* dt_bias,
+                           const void* z, const float* norm_weight, const float* state_in,
+                           float* state_out, void* out, int BH, int num_v_heads, int K, int V,
+                           void* stream) {
+    return decode_impl("gdn_decode_step", q, k, v, b, a, A_log, dt_bias, z, norm_weight,
+                       state_in, state_out, out, 1, BH, num_v_heads, K, V, stream);
+}
+
+gdn_status gdn_decode_multi(const void* q, const void* k, const void* v, const void* b,
+                            const void* a, const float* A_log, const float* dt_bias,
+                            const void* z, const float* norm_weight, const float* state_in,
+                            float* state_out, void* out, int T, int BH, int num_v_heads, int K,
+                            int V, void* stream) {
+    return decode_impl("gdn_decode_multi", q, k, v, b, a, A_log, dt_bias, z, norm_weight,
+                       state_in, state_out, out, T, BH, num_v_heads, K, V, stream);
+}
+
+gdn_status gdn_conv1d_decode(const void* x, const float* conv_weight, const void* conv_state_in,
+                             void* conv_state_out, void* q_out, void* k_out, void* v_out, int B,
+                             int num_k_heads, int num_v_heads, int head_k_dim, int head_v_dim,
+                             int K_win, void* stream) {
+    if (B < 0 || num_k_heads < 1 || num_v_heads < 1 || num_v_heads % num_k_heads != 0)
+        return fail(GDN_EINVAL, "gdn_conv1d_decode: need B >= 0 and num_v_heads a multiple of "
+                    "num_k_heads (got B=%d num_k_heads=%d num_v_heads=%d)", B, num_k_heads,
+                    num_v_heads);
+    if (head_k_dim < 1 || head_k_dim > gdn::kMaxHeadDim || head_v_dim < 1 ||
+        head_v_dim > gdn::kMaxHeadDim)
+        return fail(GDN_EINVAL, "gdn_conv1d_decode: need 1 <= head_k_dim, head_v_dim <= %d",
+                    gdn::kMaxHeadDim);
+    if (K_win < 1 || K_win > gdn::kMaxConvWidth)
+        return fail(GDN_EINVAL, "gdn_conv1d_decode: need 1 <= K_win <= %d (got %d)",
+                    gdn::kMaxConvWidth, K_win);
+    const bool rows = B > 0;
+    if (!ptr_ok(x, rows) || !ptr_ok(conv_weight, true) || !ptr_ok(conv_state_in, rows) ||
+        !ptr_ok(conv_state_out, rows) || !ptr_ok(q_out, rows) || !ptr_ok(k_out, rows) ||
+        !ptr_ok(v_out, rows))
+        return fail(GDN_EINVAL, "gdn_conv1d_decode: every pointer must be a non-NULL, "
+                    "16-byte aligned device pointer");
+    const size_t C = 2 * (size_t)num_k_heads * head_k_dim + (size_t)num_v_heads * head_v_dim;
+    if (conv_state_in != conv_state_out && rows) {
+        const uintptr_t i0 = reinterpret_cast<uintptr_t>(conv_state_in);
+        const uintptr_t o0 = reinterpret_cast<uintptr_t>(conv_state_out);
+        const uintptr_t n = (uintptr_t)B * C * K_win * 2;
+        if (i0 < o0 + n && o0 < i0 + n)
+            return fail(GDN_EINVAL, "gdn_conv1d_decode: conv_state_out overlaps conv_state_in "
+                        "without being equal to it");
+    }
+    gdn::Conv1dArgs d{static_cast<const __nv_bfloat16*>(x), conv_weight,
+                      static_cast<const __nv_bfloat16*>(conv_state_in),
+                      static_cast<__nv_bfloat16*>(conv_state_out),
+                      static_cast<__nv_bfloat16*>(q_out), static_cast<__nv_bfloat16*>(k_out),
+                      static_cast<__nv_bfloat16*>(v_out), B, num_k_heads, num_v_heads,
+                      head_k_dim, head_v_dim, K_win};
+    const cudaError_t e = gdn::launch_conv1d_decode(d, static_cast<cudaStream_t>(stream));
+    if (rows) g_launches += 1;
+    if (e != cudaSuccess)
+        return fail(GDN_ECUDA, "gdn_conv1d_decode: launch failed: %s", cudaGetErrorString(e));
     return GDN_OK;
 }
 

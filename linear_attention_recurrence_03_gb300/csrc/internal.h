@@ -34,19 +34,20 @@ struct PrefillArgs {
 };
 
 struct DecodeArgs {
-    const __nv_bfloat16* q;   // [BH, K]
-    const __nv_bfloat16* k;   // [BH, K]
-    const __nv_bfloat16* v;   // [BH, V]
-    const __nv_bfloat16* b;   // [BH]
-    const __nv_bfloat16* a;   // [BH]
+    const __nv_bfloat16* q;   // [T, BH, K]
+    const __nv_bfloat16* k;   // [T, BH, K]
+    const __nv_bfloat16* v;   // [T, BH, V]
+    const __nv_bfloat16* b;   // [T, BH]
+    const __nv_bfloat16* a;   // [T, BH]
     const float* A_log;       // [H]
     const float* dt_bias;     // [H]
-    const __nv_bfloat16* z;   // [BH, V]
+    const __nv_bfloat16* z;   // [T, BH, V]
     const float* norm_weight; // [V]
     const float* state_in;    // [BH, K, V]
     float* state_out;         // [BH, K, V]
-    __nv_bfloat16* out;       // [BH, V]
+    __nv_bfloat16* out;       // [T, BH, V]
     int BH, H, K, V;
+    int T;                    // consecutive tokens per call (1: the single decode step)
 };
 
 // SIMT fp32 chunked prefill (any Dk, Dv <= 128; q/k/v fp32 or bf16). *launched
@@ -72,7 +73,22 @@ cudaError_t launch_prefill_tc_overlapped(const PrefillArgs& a, cudaStream_t stre
                                          int* launched);
 int prefill_tc_segment_chunks(int B, int Hv, int nch, int sms);
 
-// Fused decode step.
+// Depthwise causal conv1d decode token + silu + window shift, split into q | k | v with
+// q and k repeated over the value heads.
+constexpr int kMaxConvWidth = 16;
+struct Conv1dArgs {
+    const __nv_bfloat16* x;         // [B, conv_dim], conv_dim = 2 Hk Dk + Hv Dv
+    const float* weight;            // [conv_dim, K_win]
+    const __nv_bfloat16* state_in;  // [B, conv_dim, K_win]
+    __nv_bfloat16* state_out;       // [B, conv_dim, K_win] (may equal state_in)
+    __nv_bfloat16* q;               // [B * Hv, Dk]
+    __nv_bfloat16* k;               // [B * Hv, Dk]
+    __nv_bfloat16* v;               // [B * Hv, Dv]
+    int B, Hk, Hv, Dk, Dv, K_win;
+};
+cudaError_t launch_conv1d_decode(const Conv1dArgs& a, cudaStream_t stream);
+
+// Fused decode step, T tokens in a row (the state read and written once).
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 
 // Device status word of each translation unit that has bounded waits: returns the

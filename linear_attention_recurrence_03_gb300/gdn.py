@@ -25,7 +25,8 @@ STATUS_NAMES = {0: "GDN_OK", 1: "GDN_EINVAL", 2: "GDN_EUNSUPPORTED", 3: "GDN_ECU
 
 # Every symbol include/gdn.h declares.
 EXPORTS = ("gdn_prefill_workspace_bytes", "gdn_prefill", "gdn_prefill_noalloc",
-           "gdn_decode_step", "gdn_last_error", "gdn_get_device_status", "gdn_launch_count")
+           "gdn_decode_step", "gdn_decode_multi", "gdn_conv1d_decode", "gdn_last_error",
+           "gdn_get_device_status", "gdn_launch_count")
 
 _lock = threading.Lock()
 _lib = None
@@ -59,6 +60,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gdn_prefill_noalloc.restype = i
         lib.gdn_decode_step.argtypes = [vp] * 12 + [i] * 4 + [vp]
         lib.gdn_decode_step.restype = i
+        lib.gdn_decode_multi.argtypes = [vp] * 12 + [i] * 5 + [vp]
+        lib.gdn_decode_multi.restype = i
+        lib.gdn_conv1d_decode.argtypes = [vp] * 7 + [i] * 6 + [vp]
+        lib.gdn_conv1d_decode.restype = i
         lib.gdn_last_error.argtypes = []
         lib.gdn_last_error.restype = ctypes.c_char_p
         lib.gdn_get_device_status.argtypes = [vp]
@@ -209,3 +214,59 @@ def gdn_decode_step(q, k, v, b, a, A_log, dt_bias, z, norm_weight, state_in, num
         _ptr(norm_weight), _ptr(state_in), _ptr(state_out), _ptr(out), BH, num_v_heads, K, V,
         _stream(stream)))
     return out, state_out
+
+
+def gdn_decode_multi(q, k, v, b, a, A_log, dt_bias, z, norm_weight, state_in, num_v_heads,
+                     state_out=None, out=None, stream=None):
+    """T consecutive fused decode tokens in one call. q,k [T,BH,K], v,z [T,BH,V], b,a
+    [T,BH] bf16; the rest as gdn_decode_step. Returns (out [T,BH,V] bf16, state_out)."""
+    T, BH, K = q.shape
+    V = v.shape[2]
+    dev, bf = q.device, torch.bfloat16
+    for t, n, sh in ((q, "q", (T, BH, K)), (k, "k", (T, BH, K)), (v, "v", (T, BH, V)),
+                     (z, "z", (T, BH, V)), (b, "b", (T, BH)), (a, "a", (T, BH))):
+        _need(t, n, bf, sh, dev)
+    _need(A_log, "A_log", torch.float32, (num_v_heads,), dev)
+    _need(dt_bias, "dt_bias", torch.float32, (num_v_heads,), dev)
+    _need(norm_weight, "norm_weight", torch.float32, (V,), dev)
+    _need(state_in, "state_in", torch.float32, (BH, K, V), dev)
+    if state_out is None:
+        state_out = torch.empty_like(state_in)
+    _need(state_out, "state_out", torch.float32, (BH, K, V), dev)
+    if out is None:
+        out = torch.empty((T, BH, V), dtype=bf, device=dev)
+    _need(out, "out", bf, (T, BH, V), dev)
+    _check(load_library().gdn_decode_multi(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(b), _ptr(a), _ptr(A_log), _ptr(dt_bias), _ptr(z),
+        _ptr(norm_weight), _ptr(state_in), _ptr(state_out), _ptr(out), T, BH, num_v_heads, K,
+        V, _stream(stream)))
+    return out, state_out
+
+
+def gdn_conv1d_decode(x, conv_weight, conv_state_in, num_k_heads, num_v_heads, head_k_dim,
+                      head_v_dim, conv_state_out=None, stream=None):
+    """One token through the depthwise causal conv + SiLU + window shift, split into
+    q | k | v with q, k repeated over the value heads. x [B, conv_dim] bf16,
+    conv_weight [conv_dim, K_win] fp32, conv_state_in [B, conv_dim, K_win] bf16.
+    ``conv_state_out`` may be ``conv_state_in`` (in place). Returns (q, k, v,
+    conv_state_out): q, k [B*num_v_heads, head_k_dim], v [B*num_v_heads, head_v_dim]."""
+    B, C = x.shape
+    K_win = conv_weight.shape[1]
+    dev, bf = x.device, torch.bfloat16
+    if C != 2 * num_k_heads * head_k_dim + num_v_heads * head_v_dim:
+        raise ValueError("x: conv_dim must be 2 * num_k_heads * head_k_dim + "
+                         "num_v_heads * head_v_dim")
+    _need(x, "x", bf, (B, C), dev)
+    _need(conv_weight, "conv_weight", torch.float32, (C, K_win), dev)
+    _need(conv_state_in, "conv_state_in", bf, (B, C, K_win), dev)
+    if conv_state_out is None:
+        conv_state_out = torch.empty_like(conv_state_in)
+    _need(conv_state_out, "conv_state_out", bf, (B, C, K_win), dev)
+    q = torch.empty((B * num_v_heads, head_k_dim), dtype=bf, device=dev)
+    k = torch.empty_like(q)
+    v = torch.empty((B * num_v_heads, head_v_dim), dtype=bf, device=dev)
+    _check(load_library().gdn_conv1d_decode(
+        _ptr(x), _ptr(conv_weight), _ptr(conv_state_in), _ptr(conv_state_out), _ptr(q),
+        _ptr(k), _ptr(v), B, num_k_heads, num_v_heads, head_k_dim, head_v_dim, K_win,
+        _stream(stream)))
+    return q, k, v, conv_state_out

@@ -17,6 +17,8 @@ from __future__ import annotations
 
 from dataclasses import dataclass, replace
 
+import math
+
 import torch
 
 
@@ -136,3 +138,65 @@ def decode_inputs(w: DecodeWorkload, seed: int | None = None) -> dict:
     state = torch.randn((w.BH, w.K, w.V), generator=gen, dtype=torch.float32) * w.state_std
     return dict(q=q, k=k, v=v, z=z, b=b, a=a, A_log=A_log, dt_bias=dt_bias,
                 norm_weight=norm_weight, state=state, num_v_heads=w.num_v_heads)
+
+
+def decode_multi_inputs(w: DecodeWorkload, T: int, seed: int | None = None) -> dict:
+    """CPU tensors for T consecutive decode tokens: per token, in token order, q, k, v,
+    z, b, a drawn as in decode_inputs (stacked on a leading T axis), then A_log, dt_bias,
+    norm_weight and the state once."""
+    gen = torch.Generator().manual_seed(w.seed if seed is None else seed)
+    G = w.num_v_heads // w.num_k_heads
+    bf = torch.bfloat16
+    per = {n: [] for n in ("q", "k", "v", "z", "b", "a")}
+    for _ in range(T):
+        for n in ("q", "k"):
+            x = torch.randn((w.B, w.num_k_heads, w.K), generator=gen, dtype=torch.float32)
+            per[n].append(x.repeat_interleave(G, dim=1).reshape(w.BH, w.K))
+        for n in ("v", "z"):
+            per[n].append(torch.randn((w.BH, w.V), generator=gen, dtype=torch.float32))
+        for n in ("b", "a"):
+            per[n].append(torch.randn((w.BH,), generator=gen, dtype=torch.float32))
+    out = {n: torch.stack(xs).to(bf) if xs else torch.empty((0,), dtype=bf)
+           for n, xs in per.items()}
+    out["A_log"] = _uniform(gen, (w.num_v_heads,), -2.0, 1.0)
+    out["dt_bias"] = _uniform(gen, (w.num_v_heads,), -1.0, 1.0)
+    out["norm_weight"] = _uniform(gen, (w.V,), 0.5, 1.5)
+    out["state"] = torch.randn((w.BH, w.K, w.V), generator=gen, dtype=torch.float32) * w.state_std
+    out["num_v_heads"] = w.num_v_heads
+    return out
+
+
+
+@dataclass(frozen=True)
+class Conv1dWorkload:
+    """One conv1d decode token in front of the decode step (the q|k|v channels of a
+    Qwen3.5-style GDN layer: conv_dim = 2 num_k_heads head_k_dim + num_v_heads head_v_dim)."""
+    name: str
+    B: int
+    num_k_heads: int
+    num_v_heads: int
+    head_k_dim: int
+    head_v_dim: int
+    K_win: int = 4
+    seed: int = 0
+
+    @property
+    def conv_dim(self) -> int:
+        return 2 * self.num_k_heads * self.head_k_dim + self.num_v_heads * self.head_v_dim
+
+
+CONV1D_B256 = Conv1dWorkload("conv1d_decode_b256_hk16_hv32_d128_k4", B=256, num_k_heads=16,
+                             num_v_heads=32, head_k_dim=128, head_v_dim=128)
+
+
+def conv1d_inputs(w: Conv1dWorkload, seed: int | None = None) -> dict:
+    """CPU tensors drawn in the order x, conv_weight, conv_state: x ~ N(0,1) and the window
+    ~ N(0,1) (bf16, earlier tokens of the same activations), conv_weight ~ U(-1/sqrt(K_win),
+    1/sqrt(K_win)) fp32 (the usual random init of a depthwise conv)."""
+    gen = torch.Generator().manual_seed(w.seed if seed is None else seed)
+    x = torch.randn((w.B, w.conv_dim), generator=gen, dtype=torch.float32).to(torch.bfloat16)
+    bound = 1.0 / math.sqrt(w.K_win)
+    weight = _uniform(gen, (w.conv_dim, w.K_win), -bound, bound)
+    state = torch.randn((w.B, w.conv_dim, w.K_win), generator=gen,
+                        dtype=torch.float32).to(torch.bfloat16)
+    return dict(x=x, conv_weight=weight, conv_state=state)

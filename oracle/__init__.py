@@ -7,6 +7,9 @@ from .oracle import (  # noqa: F401
     Oracle,
     default,
     build,
+    conv1d_decode,
+    conv1d_split,
+    decode_multi,
     decode_step,
     prefill,
     prefill_chunked,

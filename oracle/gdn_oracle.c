@@ -33,6 +33,10 @@
  *       closed forms. The RMSNormGated epilogue's eps and its norm-then-gate order
  *       are not stated on the pages: for those two choices, parity unpinned
  *       (closed forms pin the formula as read, not the reading itself).
+ *   gdn_oracle_conv1d_decode       -- the depthwise causal conv1d decode token
+ *       ("GDN Block TKG Kernel API Reference"); pinned by impulse responses, the
+ *       shift register and pass-through cases. Its window order and the absence of a
+ *       bias are readings (the page gives shapes only).
  *
  * Everything is fp64. Inputs arrive as double (bf16/fp32 -> double is exact).
  */
@@ -367,5 +371,37 @@ int gdn_oracle_decode_step(const double* q, const double* k, const double* v, co
     decode_ctx c = {q, k, v, b, a, A_log, dt_bias, z, norm_weight, state_in,
                     BH, num_v_heads, K, V, eps_l2, eps_rms, out, state_out};
     for_each_unit(decode_unit, &c, (long)BH, nthreads);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* gdn_oracle_conv1d_decode -- one decode token through the depthwise causal    */
+/* convolution ("GDN Block TKG Kernel API Reference": gdn_conv1d_decode, conv +  */
+/* silu + slide-window state; conv_weight [conv_dim, K_win], conv_state          */
+/* [B, conv_dim, K_win]).                                                        */
+/*                                                                              */
+/* The page names the operation and the shapes only. Reading (plainest causal   */
+/* depthwise convolution of width K_win over a window of the K_win latest       */
+/* inputs): per batch b and channel c,                                          */
+/*     window' = (state[1], ..., state[K_win-1], x)     (oldest first)          */
+/*     y       = silu( sum_w weight[c][w] * window'[w] ),  silu(s) = s / (1+e^-s)*/
+/*     state'  = window'                                                         */
+/* No bias. Pinned by impulse responses, shift-register and pass-through cases.  */
+/* ------------------------------------------------------------------------ */
+int gdn_oracle_conv1d_decode(const double* x, const double* weight, const double* state_in,
+                             int B, int C, int K_win, double* y, double* state_out) {
+    if (B < 0 || C <= 0 || K_win <= 0) return -1;
+    if (state_in == state_out) return -1;
+    for (long b = 0; b < B; ++b) {
+        for (long c = 0; c < C; ++c) {
+            const double* s = state_in + ((size_t)b * C + c) * K_win;
+            double* so = state_out + ((size_t)b * C + c) * K_win;
+            for (int w = 0; w + 1 < K_win; ++w) so[w] = s[w + 1];
+            so[K_win - 1] = x[(size_t)b * C + c];
+            double acc = 0.0;
+            for (int w = 0; w < K_win; ++w) acc += weight[(size_t)c * K_win + w] * so[w];
+            y[(size_t)b * C + c] = acc / (1.0 + exp(-acc));
+        }
+    }
     return 0;
 }

@@ -54,6 +54,8 @@ def _bind(path):
     lib.gdn_oracle_unit_lower_inverse.restype = None
     lib.gdn_oracle_decode_step.argtypes = [_dp] * 10 + [i] * 4 + [d, d] + [_dp, _dp, i]
     lib.gdn_oracle_decode_step.restype = i
+    lib.gdn_oracle_conv1d_decode.argtypes = [_dp] * 3 + [i] * 3 + [_dp, _dp]
+    lib.gdn_oracle_conv1d_decode.restype = i
     return lib
 
 
@@ -141,6 +143,54 @@ class Oracle:
         return out, st
 
 
+    def decode_multi(self, q, k, v, b, a, A_log, dt_bias, z, norm_weight, state_in,
+                     num_v_heads, eps_l2=EPS_L2, eps_rms=EPS_RMS, nthreads=None):
+        """T consecutive decode tokens: token t is decode_step applied to the state token
+        t-1 left (the multi-token extension is defined as exactly that). q,k [T,BH,K];
+        v,z [T,BH,V]; b,a [T,BH]; the rest as decode_step. Returns (out [T,BH,V] fp64,
+        state_out [BH,K,V])."""
+        q, k, v, b, a, z = map(_f64, (q, k, v, b, a, z))
+        T = q.shape[0]
+        st = _f64(state_in)
+        outs = []
+        for t in range(T):
+            o, st = self.decode_step(q[t], k[t], v[t], b[t], a[t], A_log, dt_bias, z[t],
+                                     norm_weight, st, num_v_heads, eps_l2, eps_rms, nthreads)
+            outs.append(o)
+        out = np.stack(outs) if outs else np.empty((0,) + v.shape[1:])
+        return out, st
+
+
+    def conv1d_decode(self, x, weight, state_in):
+        """One token through the depthwise causal conv: x [B, C], weight [C, K_win],
+        state_in [B, C, K_win] (oldest first). Returns (y = silu(conv) [B, C],
+        state_out [B, C, K_win])."""
+        x, w, s0 = map(_f64, (x, weight, state_in))
+        B, C, K_win = s0.shape
+        y = np.empty((B, C))
+        st = np.empty((B, C, K_win))
+        rc = self.lib.gdn_oracle_conv1d_decode(_ptr(x), _ptr(w), _ptr(s0), B, C, K_win,
+                                               _ptr(y), _ptr(st))
+        if rc != 0:
+            raise ValueError("oracle conv1d_decode: bad shapes")
+        return y, st
+
+    def conv1d_split(self, y, num_k_heads, num_v_heads, head_k_dim, head_v_dim):
+        """Split the conv output [B, conv_dim] into q | k | v and repeat q, k over the
+        value heads (value head h reads key head h // (num_v_heads // num_k_heads)).
+        Returns q, k [B * num_v_heads, head_k_dim] and v [B * num_v_heads, head_v_dim]."""
+        y = _f64(y)
+        B = y.shape[0]
+        kd = num_k_heads * head_k_dim
+        G = num_v_heads // num_k_heads
+        q = y[:, :kd].reshape(B, num_k_heads, head_k_dim)
+        k = y[:, kd:2 * kd].reshape(B, num_k_heads, head_k_dim)
+        v = y[:, 2 * kd:].reshape(B * num_v_heads, head_v_dim)
+        idx = np.arange(num_v_heads) // G
+        return (q[:, idx].reshape(B * num_v_heads, head_k_dim),
+                k[:, idx].reshape(B * num_v_heads, head_k_dim), v)
+
+
 def default() -> Oracle:
     """The oracle built from ``gdn_oracle.c`` (compiled on first use)."""
     global _lib
@@ -164,3 +214,15 @@ def unit_lower_inverse(A):
 
 def decode_step(*args, **kw):
     return default().decode_step(*args, **kw)
+
+
+def decode_multi(*args, **kw):
+    return default().decode_multi(*args, **kw)
+
+
+def conv1d_decode(*args, **kw):
+    return default().conv1d_decode(*args, **kw)
+
+
+def conv1d_split(*args, **kw):
+    return default().conv1d_split(*args, **kw)

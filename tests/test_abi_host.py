@@ -21,7 +21,7 @@ def lib():
 def header_functions():
     src = open(os.path.join(ROOT, "include", "gdn.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(gdn_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(gdn_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_header_declares_the_binding_exports():
@@ -103,6 +103,45 @@ def test_decode_rejects_bad_arguments(lib, kw, msg):
     rc = lib.gdn_decode_step(*(vp(a[n]) for n in ("q", "k", "v", "b", "a", "A_log", "dt_bias",
                                                   "z", "w", "state_in", "state_out", "out")),
                              a["BH"], a["H"], a["K"], a["V"], None)
+    assert rc == gdn.GDN_EINVAL
+    assert msg in lib.gdn_last_error().decode()
+
+
+@pytest.mark.parametrize("kw,msg", [
+    (dict(T=-1), "T >= 0"),
+    (dict(BH=10, H=4), "BH % num_v_heads"),
+    (dict(V=0), "K, V"),
+    (dict(z=None), "non-NULL"),
+])
+def test_decode_multi_rejects_bad_arguments(lib, kw, msg):
+    a = dict(q=16, k=16, v=16, b=16, a=16, A_log=16, dt_bias=16, z=16, w=16, state_in=16,
+             state_out=16, out=16, T=3, BH=8, H=4, K=128, V=128)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    rc = lib.gdn_decode_multi(*(vp(a[n]) for n in ("q", "k", "v", "b", "a", "A_log",
+                                                   "dt_bias", "z", "w", "state_in",
+                                                   "state_out", "out")),
+                              a["T"], a["BH"], a["H"], a["K"], a["V"], None)
+    assert rc == gdn.GDN_EINVAL
+    assert msg in lib.gdn_last_error().decode()
+
+
+@pytest.mark.parametrize("kw,msg", [
+    (dict(Hk=3, Hv=4), "multiple of num_k_heads"),
+    (dict(Dk=129), "head_k_dim"),
+    (dict(K=0), "K_win"),
+    (dict(K=17), "K_win"),
+    (dict(x=None), "non-NULL"),
+    (dict(q=24), "non-NULL"),
+    (dict(so=16 + 64), "overlaps"),
+])
+def test_conv1d_rejects_bad_arguments(lib, kw, msg):
+    a = dict(x=16, w=16, si=16, so=1 << 40, q=16, k=16, v=16, B=2, Hk=2, Hv=4, Dk=128,
+             Dv=128, K=4)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    rc = lib.gdn_conv1d_decode(*(vp(a[n]) for n in ("x", "w", "si", "so", "q", "k", "v")),
+                               a["B"], a["Hk"], a["Hv"], a["Dk"], a["Dv"], a["K"], None)
     assert rc == gdn.GDN_EINVAL
     assert msg in lib.gdn_last_error().decode()
 

@@ -85,3 +85,68 @@ def test_decode_empty_batch():
     y, st = gpu_decode(x)
     assert y.shape == (0, 128) and st.shape == (0, 128, 128)
     assert gdn.gdn_get_device_status() == gdn.GDN_OK
+
+
+# ---------------------------------------------------------------- multi-token decode
+MULTI_NAMES = ("q", "k", "v", "b", "a", "A_log", "dt_bias", "z", "norm_weight", "state")
+
+
+def _gpu_multi(x, in_place=False):
+    args = [x[n].to("cuda") for n in MULTI_NAMES]
+    out, st = gdn.gdn_decode_multi(*args, x["num_v_heads"],
+                                   state_out=args[-1] if in_place else None)
+    torch.cuda.synchronize()
+    return out.cpu(), st.cpu()
+
+
+@pytest.mark.parametrize("K,V,T", [(128, 128, 6), (64, 96, 3), (8, 8, 9)])
+def test_decode_multi_matches_oracle(K, V, T):
+    """T tokens in one call against T chained oracle steps (out per token, final state)."""
+    w = syn.DecodeWorkload("t", B=3, num_k_heads=2, num_v_heads=4, K=K, V=V)
+    x = syn.decode_multi_inputs(w, T)
+    y, st = _gpu_multi(x)
+    y_ref, s_ref = oracle.decode_multi(*(x[n] for n in MULTI_NAMES), x["num_v_heads"])
+    for t in range(T):
+        assert rel(to_np(y[t]), y_ref[t]) <= TOL_BF16["out"], f"token {t}"
+    assert rel(to_np(st), s_ref) <= TOL_BF16["state"]
+
+
+def test_decode_multi_one_token_is_the_step():
+    """T = 1 is gdn_decode_step bit for bit; T = 0 leaves everything untouched."""
+    w = syn.DecodeWorkload("t", B=4, num_k_heads=2, num_v_heads=8, K=128, V=128)
+    x = syn.decode_multi_inputs(w, 1)
+    y, st = _gpu_multi(x)
+    one = {n: (x[n][0] if n in ("q", "k", "v", "b", "a", "z") else x[n]) for n in MULTI_NAMES}
+    one["num_v_heads"] = x["num_v_heads"]
+    y1, s1 = gpu_decode(one)
+    assert torch.equal(y[0], y1) and torch.equal(st, s1)
+    x0 = syn.decode_multi_inputs(w, 0)
+    args = [x0[n].to("cuda") for n in MULTI_NAMES]
+    state = args[-1].clone()
+    q0 = torch.empty((0, w.BH, w.K), dtype=torch.bfloat16, device="cuda")
+    v0 = torch.empty((0, w.BH, w.V), dtype=torch.bfloat16, device="cuda")
+    r0 = torch.empty((0, w.BH), dtype=torch.bfloat16, device="cuda")
+    out, st0 = gdn.gdn_decode_multi(q0, q0, v0, r0, r0, args[5], args[6], v0, args[8], state,
+                                    x0["num_v_heads"], state_out=state)
+    torch.cuda.synchronize()
+    assert out.shape == (0, w.BH, w.V) and torch.equal(st0, args[-1])
+
+
+def test_decode_multi_in_place_and_full_rows():
+    """BH = 8192 (the decode workload's rows), T = 4, state updated in place: sampled rows
+    against the oracle, finite everywhere, and equal to the out-of-place call."""
+    x = syn.decode_multi_inputs(syn.DECODE_BH8192, 4)
+    y1, s1 = _gpu_multi(x, in_place=False)
+    y2, s2 = _gpu_multi(x, in_place=True)
+    assert torch.equal(y1, y2) and torch.equal(s1, s2)
+    rng = np.random.default_rng(1)
+    rows = np.sort(rng.choice(x["q"].shape[1], size=48, replace=False))
+    sel = torch.as_tensor(rows)
+    H = x["num_v_heads"]
+    sub = {n: x[n][:, sel] for n in ("q", "k", "v", "b", "a", "z")}
+    y_ref, s_ref = oracle.decode_multi(sub["q"], sub["k"], sub["v"], sub["b"], sub["a"],
+                                       x["A_log"][sel % H], x["dt_bias"][sel % H], sub["z"],
+                                       x["norm_weight"], x["state"][sel], len(rows))
+    assert rel(to_np(y1[:, sel]), y_ref) <= TOL_BF16["out"]
+    assert rel(to_np(s1[sel]), s_ref) <= TOL_BF16["state"]
+    assert torch.isfinite(y1.float()).all() and torch.isfinite(s1).all()

@@ -336,6 +336,36 @@ def test_decode_steps_equal_one_prefill(oracle_mod):
     np.testing.assert_allclose(st, st_p[:, 0], rtol=1e-12, atol=1e-14)
 
 
+def test_decode_multi_equals_prefill(oracle_mod):
+    """The multi-token decode (T tokens in one call) carries the state like one T-token
+    prefill on the gated, l2-normalised inputs, and its first token is the single
+    step."""
+    rng = np.random.default_rng(23)
+    BH, H, K, V, T = 6, 3, 8, 8, 4
+    d0 = rand_decode(rng, BH, H, K, V)
+    toks = [rand_decode(rng, BH, H, K, V) for _ in range(T)]
+    seq = {n: np.stack([d[n] for d in toks]) for n in ("q", "k", "v", "b", "a", "z")}
+    out, st = oracle_mod.decode_multi(seq["q"], seq["k"], seq["v"], seq["b"], seq["a"],
+                                      d0["A_log"], d0["dt_bias"], seq["z"], d0["norm_weight"],
+                                      d0["state_in"], H, eps_l2=0.0)
+    gs, betas = [], []
+    for d in toks:
+        d.update(A_log=d0["A_log"], dt_bias=d0["dt_bias"], num_v_heads=H)
+        beta, g = _gates(d)
+        gs.append(g), betas.append(beta)
+    q = np.stack([_unit(d["q"]) for d in toks], 1)[:, None]
+    k = np.stack([_unit(d["k"]) for d in toks], 1)[:, None]
+    v = np.stack([d["v"] for d in toks], 1)[:, None]
+    _, st_p = oracle_mod.prefill(q, k, v, np.stack(gs, 1)[:, None],
+                                 np.stack(betas, 1)[:, None], K ** -0.5,
+                                 d0["state_in"][:, None])
+    np.testing.assert_allclose(st, st_p[:, 0], rtol=1e-12, atol=1e-14)
+    y1, _ = oracle_mod.decode_step(seq["q"][0], seq["k"][0], seq["v"][0], seq["b"][0],
+                                   seq["a"][0], d0["A_log"], d0["dt_bias"], seq["z"][0],
+                                   d0["norm_weight"], d0["state_in"], H, eps_l2=0.0)
+    np.testing.assert_array_equal(out[0], y1)
+
+
 def test_decode_gates_closed_forms(oracle_mod):
     """Read beta and alpha = exp(g) off the state and check closed forms:
     sigmoid(0) = 1/2; softplus(0) = ln 2 so A_log = ln 2 gives alpha = 2^-2;
@@ -402,3 +432,72 @@ def test_decode_hand_worked_example(oracle_mod):
     y, st = oracle_mod.decode_step(**d)  # default eps readings (1e-6)
     np.testing.assert_allclose(y.ravel(), gd["out"], rtol=1e-13, atol=1e-15)
     np.testing.assert_allclose(st.ravel(), gd["state_out"], rtol=1e-13, atol=1e-15)
+
+
+# ------------------------------------------------------------- conv1d decode token
+def _silu(x):
+    return x * expit(x)
+
+
+def test_conv1d_impulse_response(oracle_mod):
+    """A depthwise causal filter is fixed by its impulse response: an impulse of height a
+    entered at step 0 into a zero window comes out at step t as silu(a w[c][K-1-t])."""
+    rng = np.random.default_rng(30)
+    B, C, K = 2, 5, 4
+    w = rng.standard_normal((C, K))
+    a = rng.standard_normal((B, C))
+    st = np.zeros((B, C, K))
+    for t in range(K + 1):
+        x = a if t == 0 else np.zeros((B, C))
+        y, st = oracle_mod.conv1d_decode(x, w, st)
+        want = _silu(a * w[None, :, K - 1 - t]) if t < K else np.zeros((B, C))
+        np.testing.assert_allclose(y, want, rtol=1e-14, atol=0)
+
+
+def test_conv1d_window_is_a_shift_register(oracle_mod):
+    """After K tokens the window holds exactly those tokens, oldest first; the next token
+    drops the oldest."""
+    rng = np.random.default_rng(31)
+    B, C, K = 3, 4, 5
+    w = rng.standard_normal((C, K))
+    st = rng.standard_normal((B, C, K))
+    xs = [rng.standard_normal((B, C)) for _ in range(K + 1)]
+    for x in xs[:K]:
+        _, st = oracle_mod.conv1d_decode(x, w, st)
+    np.testing.assert_array_equal(st, np.stack(xs[:K], axis=2))
+    _, st = oracle_mod.conv1d_decode(xs[K], w, st)
+    np.testing.assert_array_equal(st, np.stack(xs[1:], axis=2))
+
+
+def test_conv1d_pass_through_and_delay(oracle_mod):
+    """A one-hot filter on the newest tap passes silu(x) through; on tap j it returns
+    silu of the input j + 1 tokens older than the newest (state[j + 1])."""
+    rng = np.random.default_rng(32)
+    B, C, K = 2, 3, 4
+    st = rng.standard_normal((B, C, K))
+    x = rng.standard_normal((B, C))
+    w = np.zeros((C, K))
+    w[:, K - 1] = 1.0
+    y, _ = oracle_mod.conv1d_decode(x, w, st)
+    np.testing.assert_allclose(y, _silu(x), rtol=1e-15)
+    for j in range(K - 1):
+        w = np.zeros((C, K))
+        w[:, j] = 1.0
+        y, _ = oracle_mod.conv1d_decode(x, w, st)
+        np.testing.assert_allclose(y, _silu(st[:, :, j + 1]), rtol=1e-15)
+
+
+def test_conv1d_split_is_repeat_interleave(oracle_mod):
+    """q | k | v split of the conv channels, q and k repeated over the value heads the
+    way torch.repeat_interleave does it (value head h reads key head h // G)."""
+    import torch
+    rng = np.random.default_rng(33)
+    B, Hk, Hv, Dk, Dv = 2, 2, 6, 3, 4
+    y = rng.standard_normal((B, 2 * Hk * Dk + Hv * Dv))
+    q, k, v = oracle_mod.conv1d_split(y, Hk, Hv, Dk, Dv)
+    t = torch.from_numpy(y)
+    qr = t[:, :Hk * Dk].reshape(B, Hk, Dk).repeat_interleave(Hv // Hk, dim=1)
+    kr = t[:, Hk * Dk:2 * Hk * Dk].reshape(B, Hk, Dk).repeat_interleave(Hv // Hk, dim=1)
+    np.testing.assert_array_equal(q, qr.reshape(B * Hv, Dk).numpy())
+    np.testing.assert_array_equal(k, kr.reshape(B * Hv, Dk).numpy())
+    np.testing.assert_array_equal(v, t[:, 2 * Hk * Dk:].reshape(B * Hv, Dv).numpy())
