@@ -52,6 +52,8 @@ def parse_args():
                    help="skip the multi-token decode measurement (T = 2, 4, 8 tokens per call)")
     p.add_argument("--no-conv", action="store_true",
                    help="skip the conv1d decode measurement (B = 256, 8192 channels)")
+    p.add_argument("--no-varlen", action="store_true",
+                   help="skip the variable-length prefill measurement (16 packed sequences)")
     p.add_argument("--spinup-seconds", type=float, default=1.0,
                    help="untimed load before the warm-up, so clock samples see the GPU busy")
     return p.parse_args()
@@ -486,6 +488,50 @@ def run_gdn(args):
             del M, m_out
         result["decode_multi"] = {"workload": wd.name, "kernel": "decode.cu",
                                   "api": "gdn_decode_multi", **multi}
+
+    # variable-length prefill: 16 sequences of 256..4096 tokens packed along the token axis
+    if not args.no_varlen:
+        wv = syn.PREFILL_BF16_VARLEN
+        xv = syn.varlen_inputs(wv)
+        VX = {n: xv[n].to(dev) for n in ("q", "k", "v", "g_log", "beta", "cu_seqlens")}
+        Tv = VX["q"].shape[1]
+        v_out = torch.empty((wv.base.Hv, Tv, wv.base.Dv), dtype=torch.bfloat16, device=dev)
+        v_state = torch.empty((wv.N, wv.base.Hv, wv.base.Dk, wv.base.Dv), dtype=torch.float32,
+                              device=dev)
+        v_wsb = lib.gdn_prefill_varlen_workspace_bytes(wv.N, wv.base.Hk, wv.base.Hv, Tv,
+                                                       wv.base.Dk, wv.base.Dv, gdn.GDN_DTYPE_BF16)
+        v_ws = torch.empty(max(v_wsb, 16), dtype=torch.uint8, device=dev)
+        vargs = [vp(VX[n].data_ptr()) for n in ("q", "k", "v", "g_log", "beta")]
+
+        def prefill_v():
+            rc = lib.gdn_prefill_varlen(*vargs, float(xv["scale"]), gdn.GDN_DTYPE_BF16,
+                                        vp(VX["cu_seqlens"].data_ptr()), wv.N, wv.base.Hk,
+                                        wv.base.Hv, Tv, wv.base.Dk, wv.base.Dv,
+                                        vp(v_state.data_ptr()), 0, vp(v_out.data_ptr()),
+                                        vp(v_ws.data_ptr()), v_wsb, sptr)
+            if rc != 0:
+                raise RuntimeError(gdn.gdn_last_error())
+
+        for _ in range(args.warmup):
+            prefill_v()
+        torch.cuda.synchronize()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(K):
+            prefill_v()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        v_ms = reduce_max([ev0.elapsed_time(ev1) / K], ws)[0]
+        wvd = syn.shrink(wv.base, B=1, S=Tv, state_std=None)
+        vb, vf = prefill_bytes(wvd), prefill_flops(wvd)
+        vb += (wv.N - 1) * wv.base.Hv * wv.base.Dk * wv.base.Dv * 4  # one state per sequence
+        rv = max(vb / (hbm * 1e9), vf / (bf16 * 1e12))
+        result["prefill_varlen"] = {
+            "workload": wv.name, "tokens": Tv, "sequences": wv.N, "ms": v_ms,
+            "tokens_per_s": ws * Tv / (v_ms * 1e-3), "achieved_gbs": vb / (v_ms * 1e-3) / 1e9,
+            "frac_of_roofline": rv / (v_ms * 1e-3), "api": "gdn_prefill_varlen"}
+        del VX, v_out, v_state, v_ws
 
     # conv1d decode token in front of the decode step: B = 256, 8192 q|k|v channels,
     # K_win = 4, window in place

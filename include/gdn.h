@@ -97,6 +97,47 @@ gdn_status gdn_prefill(const void* q, const void* k, const void* v,
                        void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * gdn_prefill_varlen_workspace_bytes -- device scratch gdn_prefill_varlen needs for N
+ * sequences packed into T tokens: on the bf16 Dk = Dv = 128 path (tensor cores)
+ * Hv * (ceil(T / 64) + N) * 66560 bytes rounded up to 256, plus 4 * (N + 2); on every
+ * other path 4 * (N + 2) rounded up to 16. (size_t)-1 for an invalid shape.
+ */
+size_t gdn_prefill_varlen_workspace_bytes(int N, int Hk, int Hv, int T, int Dk, int Dv,
+                                          gdn_dtype dtype);
+
+/*
+ * gdn_prefill_varlen -- gdn_prefill over a variable-length batch: N independent
+ * sequences packed back to back along the token axis, sequence n holding tokens
+ * cu_seqlens[n] .. cu_seqlens[n+1] - 1 (the "GDN CTE Kernel API Reference" recurrence
+ * per sequence, each from its own state; the pages' kernel takes a dense batch with
+ * S % 64 == 0 -- per-sequence offsets are this library's extension).
+ *
+ *   q, k         device, [Hk, T, Dk] in the compute dtype (one batch row, tokens packed).
+ *   v            device, [Hv, T, Dv].
+ *   g_log, beta  device, [Hv, T] fp32.
+ *   cu_seqlens   device, [N + 1] int32: 0 = cu[0] <= cu[1] <= ... <= cu[N] <= T.
+ *                Sequences may be empty; tokens past cu[N] are ignored.
+ *   state        device, [N, Hv, Dk, Dv] fp32, one state per sequence, with
+ *                state_is_input as in gdn_prefill (an empty sequence leaves its state
+ *                unchanged, or writes zeros when state_is_input == 0).
+ *   out          device, [Hv, T, Dv]; rows of tokens past cu[N] are not written.
+ *   workspace    device scratch of gdn_prefill_varlen_workspace_bytes(...) bytes.
+ *   0 <= N <= 65535; N == 0 enqueues nothing.
+ *
+ * Each sequence's chunks start at its first token, so sequence n gets bit for bit what
+ * gdn_prefill returns for it alone (B = 1, S = its length). A malformed cu_seqlens is
+ * found on the device: every sequence is then treated as empty and
+ * gdn_get_device_status() returns GDN_EINVAL.
+ *
+ * Errors: as gdn_prefill, plus GDN_EINVAL for N out of range.
+ */
+gdn_status gdn_prefill_varlen(const void* q, const void* k, const void* v, const float* g_log,
+                              const float* beta, float scale, gdn_dtype dtype,
+                              const int* cu_seqlens, int N, int Hk, int Hv, int T, int Dk,
+                              int Dv, float* state, int state_is_input, void* out,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * gdn_prefill_noalloc -- gdn_prefill without a caller workspace: the scratch is a
  * fixed 128 MiB device array inside the library (allocated when the library's module is
  * loaded), so the call allocates nothing. Arguments, results and errors as gdn_prefill.

@@ -5,6 +5,7 @@ thin Python binding of the same names:
 
 * ``gdn_prefill``      -- chunked prefill ("GDN CTE Kernel API Reference").
 * ``gdn_prefill_noalloc`` -- the same, with the library's own static scratch.
+* ``gdn_prefill_varlen`` -- the same over sequences packed by ``cu_seqlens``.
 * ``gdn_decode_step``  -- fused single-token decode step ("GDN TKG Kernel API Reference").
 * ``gdn_decode_multi`` -- T consecutive decode tokens in one call (state read once).
 * ``gdn_conv1d_decode`` -- the conv1d decode token feeding the decode step ("GDN Block
@@ -28,6 +29,8 @@ from .gdn import (  # noqa: F401
     gdn_launch_count,
     gdn_prefill,
     gdn_prefill_noalloc,
+    gdn_prefill_varlen,
+    gdn_prefill_varlen_workspace_bytes,
     gdn_prefill_workspace_bytes,
     load_library,
 )

@@ -33,6 +33,9 @@ gdn_status fail(gdn_status st, const char* fmt, ...) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Sequences of one variable-length call (the carry grid's third dimension).
+constexpr int kMaxSequences = 65535;
+
 // Checks that p is non-NULL and 16-byte aligned (or NULL allowed when unused).
 bool ptr_ok(const void* p, bool required) {
     if (p == nullptr) return !required;
@@ -94,6 +97,55 @@ gdn_status gdn_prefill(const void* q, const void* k, const void* v, const float*
     g_launches += (unsigned long long)launched;
     if (e != cudaSuccess)
         return fail(GDN_ECUDA, "gdn_prefill: launch failed: %s", cudaGetErrorString(e));
+    return GDN_OK;
+}
+
+size_t gdn_prefill_varlen_workspace_bytes(int N, int Hk, int Hv, int T, int Dk, int Dv,
+                                          gdn_dtype dtype) {
+    if (N < 0 || N > kMaxSequences || check_prefill_shape(1, Hk, Hv, T, Dk, Dv, dtype) != GDN_OK)
+        return (size_t)-1;
+    gdn::PrefillArgs a{};
+    a.B = 1, a.Hk = Hk, a.Hv = Hv, a.S = T, a.Dk = Dk, a.Dv = Dv;
+    if (gdn::prefill_tc_supported(a, dtype == GDN_DTYPE_BF16))
+        return gdn::prefill_tc_varlen_workspace_bytes(N, Hv, T);
+    return (gdn::varlen_table_ints(N) * sizeof(int) + 15) / 16 * 16;
+}
+
+gdn_status gdn_prefill_varlen(const void* q, const void* k, const void* v, const float* g_log,
+                              const float* beta, float scale, gdn_dtype dtype,
+                              const int* cu_seqlens, int N, int Hk, int Hv, int T, int Dk,
+                              int Dv, float* state, int state_is_input, void* out,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+    gdn_status st = check_prefill_shape(1, Hk, Hv, T, Dk, Dv, dtype);
+    if (st != GDN_OK) return st;
+    if (N < 0 || N > kMaxSequences)
+        return fail(GDN_EINVAL, "gdn_prefill_varlen: need 0 <= N <= %d (got N=%d)",
+                    kMaxSequences, N);
+    if (N == 0) return GDN_OK;
+    const bool tok = T > 0;
+    if (!ptr_ok(q, tok) || !ptr_ok(k, tok) || !ptr_ok(v, tok) || !ptr_ok(g_log, tok) ||
+        !ptr_ok(beta, tok) || !ptr_ok(out, tok) || !ptr_ok(state, true) ||
+        !ptr_ok(cu_seqlens, true))
+        return fail(GDN_EINVAL, "gdn_prefill_varlen: q, k, v, g_log, beta, out, state and "
+                    "cu_seqlens must be non-NULL, 16-byte aligned device pointers");
+    const size_t need = gdn_prefill_varlen_workspace_bytes(N, Hk, Hv, T, Dk, Dv, dtype);
+    if (workspace_bytes < need || !ptr_ok(workspace, true))
+        return fail(GDN_EINVAL, "gdn_prefill_varlen: workspace of %zu bytes needed, %zu given",
+                    need, workspace_bytes);
+    gdn::PrefillArgs a{q, k, v, g_log, beta, scale, 1, Hk, Hv, T, Dk, Dv,
+                       state, state_is_input ? 1 : 0, out, workspace, workspace_bytes};
+    a.cu_seqlens = cu_seqlens;
+    a.N = N;
+    a.table = static_cast<int*>(workspace);  // the fp32 path's table opens the workspace
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int launched = 0;
+    const bool bf16 = dtype == GDN_DTYPE_BF16;
+    const cudaError_t e = gdn::prefill_tc_supported(a, bf16)
+                              ? gdn::launch_prefill_tc_varlen(a, s, &launched)
+                              : gdn::launch_prefill_simt(a, bf16, s, &launched);
+    g_launches += (unsigned long long)launched;
+    if (e != cudaSuccess)
+        return fail(GDN_ECUDA, "gdn_prefill_varlen: launch failed: %s", cudaGetErrorString(e));
     return GDN_OK;
 }
 
@@ -256,6 +308,9 @@ gdn_status gdn_get_device_status(void* stream) {
     if (e != cudaSuccess)
         return fail(GDN_ECUDA, "gdn_get_device_status: %s", cudaGetErrorString(e));
     const uint32_t bits = gdn::prefill_tc_take_status();
+    if (bits & gdn::kStatusBadSeqlens)
+        return fail(GDN_EINVAL, "gdn_prefill_varlen: cu_seqlens was not 0 = cu[0] <= ... <= "
+                    "cu[N] <= T; every sequence was treated as empty");
     if (bits != 0)
         return fail(GDN_ETIMEOUT, "a kernel gave up a bounded wait (status bits 0x%x)", bits);
     return GDN_OK;

@@ -31,7 +31,21 @@ struct PrefillArgs {
     void* out;          // [B, Hv, S, Dv]
     void* workspace;
     size_t workspace_bytes;
+    // Variable-length batch (cu_seqlens != NULL): B == 1, the N sequences are packed
+    // along S (sequence n: tokens cu_seqlens[n] .. cu_seqlens[n+1] - 1), state is
+    // [N, Hv, Dk, Dv]; `table` is device scratch of varlen_table_ints(N) ints that the
+    // setup kernel fills (chunk bases, then a validity flag).
+    const int* cu_seqlens = nullptr;
+    int N = 0;
+    int* table = nullptr;
 };
+
+// Ints of the variable-length batch's table: N + 1 chunk bases and a validity flag.
+inline size_t varlen_table_ints(int N) { return (size_t)N + 2; }
+// Fills the table from cu_seqlens (one CTA): chunk bases of 64-token chunks and the flag
+// (0 when cu_seqlens is not 0 = cu[0] <= cu[1] <= ... <= cu[N] <= S; the status word
+// then gets its input bit and every sequence is treated as empty).
+cudaError_t launch_varlen_setup(const PrefillArgs& a, cudaStream_t stream);
 
 struct DecodeArgs {
     const __nv_bfloat16* q;   // [T, BH, K]
@@ -61,6 +75,12 @@ cudaError_t launch_prefill_simt(const PrefillArgs& a, bool bf16, cudaStream_t st
 bool prefill_tc_supported(const PrefillArgs& a, bool bf16);
 size_t prefill_tc_workspace_bytes(int B, int Hv, int S);
 size_t prefill_tc_unit_bytes();
+// Variable-length batch on the tensor cores: the workspace holds Hv * (ceil(S/64) + N)
+// units, then the table.
+size_t prefill_tc_varlen_workspace_bytes(int N, int Hv, int S);
+cudaError_t launch_prefill_tc_varlen(const PrefillArgs& a, cudaStream_t stream, int* launched);
+// Status bit of a malformed cu_seqlens (prefill_tc_take_status).
+constexpr uint32_t kStatusBadSeqlens = 16u;
 // Processes chunks c0 .. c0 + nseg - 1 of the sequence (64 tokens each) with a workspace of
 // B * Hv * nseg units; the state carries over between consecutive calls.
 cudaError_t launch_prefill_tc(const PrefillArgs& a, int c0, int nseg, cudaStream_t stream,

@@ -21,7 +21,8 @@
 // Grid: (ceil(Dv/32) value-column slices, Hv, B); the columns of S evolve
 // independently (left-multiplication by (I - beta k k^T) never mixes them), so each
 // CTA carries its own 32 columns of the state through the whole sequence in shared
-// memory.
+// memory. A variable-length batch (B == 1, sequences packed along S by cu_seqlens) puts
+// sequence n on grid row n; its chunks start at its first token.
 #include "internal.h"
 
 namespace gdn {
@@ -60,18 +61,32 @@ __global__ void __launch_bounds__(NT) prefill_simt_kernel(PrefillArgs a) {
     extern __shared__ float4 smem_raw[];
     Smem& s = *reinterpret_cast<Smem*>(smem_raw);
     const int tid = threadIdx.x;
-    const int n0 = blockIdx.x * NS, h = blockIdx.y, b = blockIdx.z;
+    const int n0 = blockIdx.x * NS, h = blockIdx.y;
     const int Dk = a.Dk, Dv = a.Dv, S = a.S;
     const int nw = min(NS, Dv - n0);
     const int kh = h / (a.Hv / a.Hk);  // value head h reads key head h // (Hv/Hk)
+    // this CTA's sequence: batch b (tensor row b, tokens 0 .. S-1), or packed sequence n
+    // (tensor row 0, tokens cu[n] .. cu[n+1]-1; a malformed cu leaves every sequence empty)
+    int b = blockIdx.z, t0 = 0, len = S, srow = blockIdx.z;
+    if (a.cu_seqlens != nullptr) {
+        const int n = blockIdx.z;
+        const bool valid = a.table[a.N + 1] != 0;
+        b = 0;
+        t0 = valid ? a.cu_seqlens[n] : 0;
+        len = valid ? a.cu_seqlens[n + 1] - t0 : 0;
+    }
 
-    const Tin* q = static_cast<const Tin*>(a.q) + ((size_t)b * a.Hk + kh) * (size_t)S * Dk;
-    const Tin* k = static_cast<const Tin*>(a.k) + ((size_t)b * a.Hk + kh) * (size_t)S * Dk;
-    const Tin* v = static_cast<const Tin*>(a.v) + ((size_t)b * a.Hv + h) * (size_t)S * Dv;
-    const float* g = a.g + ((size_t)b * a.Hv + h) * (size_t)S;
-    const float* be = a.beta + ((size_t)b * a.Hv + h) * (size_t)S;
-    Tin* out = static_cast<Tin*>(a.out) + ((size_t)b * a.Hv + h) * (size_t)S * Dv;
-    float* st = a.state + ((size_t)b * a.Hv + h) * (size_t)Dk * Dv;
+    const Tin* q = static_cast<const Tin*>(a.q) + ((size_t)b * a.Hk + kh) * (size_t)S * Dk +
+                   (size_t)t0 * Dk;
+    const Tin* k = static_cast<const Tin*>(a.k) + ((size_t)b * a.Hk + kh) * (size_t)S * Dk +
+                   (size_t)t0 * Dk;
+    const Tin* v = static_cast<const Tin*>(a.v) + ((size_t)b * a.Hv + h) * (size_t)S * Dv +
+                   (size_t)t0 * Dv;
+    const float* g = a.g + ((size_t)b * a.Hv + h) * (size_t)S + t0;
+    const float* be = a.beta + ((size_t)b * a.Hv + h) * (size_t)S + t0;
+    Tin* out = static_cast<Tin*>(a.out) + ((size_t)b * a.Hv + h) * (size_t)S * Dv +
+               (size_t)t0 * Dv;
+    float* st = a.state + ((size_t)srow * a.Hv + h) * (size_t)Dk * Dv;
 
     // Initial state: the supplied one, else zero with no load.
     for (int idx = tid; idx < kMaxHeadDim * NS; idx += NT) {
@@ -79,8 +94,8 @@ __global__ void __launch_bounds__(NT) prefill_simt_kernel(PrefillArgs a) {
         s.S[i][n] = (a.state_is_input && i < Dk && n < nw) ? st[(size_t)i * Dv + n0 + n] : 0.f;
     }
 
-    for (int c0 = 0; c0 < S; c0 += C) {
-        const int L = min(C, S - c0);
+    for (int c0 = 0; c0 < len; c0 += C) {
+        const int L = min(C, len - c0);
         __syncthreads();
         for (int idx = tid; idx < C * Dk; idx += NT) {
             const int r = idx / Dk, i = idx % Dk;
@@ -198,7 +213,14 @@ __global__ void __launch_bounds__(NT) prefill_simt_kernel(PrefillArgs a) {
 cudaError_t launch_prefill_simt(const PrefillArgs& a, bool bf16, cudaStream_t stream,
                                 int* launched) {
     *launched = 0;
-    const dim3 grid((a.Dv + NS - 1) / NS, a.Hv, a.B);
+    const int rows = a.cu_seqlens ? a.N : a.B;
+    if (rows == 0) return cudaSuccess;
+    if (a.cu_seqlens) {
+        const cudaError_t e = launch_varlen_setup(a, stream);
+        if (e != cudaSuccess) return e;
+        *launched = 1;
+    }
+    const dim3 grid((a.Dv + NS - 1) / NS, a.Hv, rows);
     const size_t smem = sizeof(Smem);
     cudaError_t e;
     if (bf16) {
@@ -212,7 +234,7 @@ cudaError_t launch_prefill_simt(const PrefillArgs& a, bool bf16, cudaStream_t st
         if (e != cudaSuccess) return e;
         prefill_simt_kernel<float><<<grid, NT, smem, stream>>>(a);
     }
-    *launched = 1;
+    *launched += 1;
     return cudaGetLastError();
 }
 

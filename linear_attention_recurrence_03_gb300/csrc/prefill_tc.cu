@@ -215,10 +215,27 @@ struct TcArgs {
     int state_is_input;
     __nv_bfloat16* out;
     uint8_t* ws;
+    // variable-length batch (NULL cu: the dense [B, H, S] layout): sequence n holds the
+    // packed tokens cu[n] .. cu[n+1] - 1 of the [H, S] tensors and the chunks
+    // cb[n] .. cb[n+1] - 1 of the grid, nseg = an upper bound of cb[N] chunks
+    const int* cu;
+    const int* cb;
+    int N;
 };
 
 __device__ __forceinline__ size_t ws_offset(int b, int h, int c, int Hv, int nch) {
     return ((size_t)(b * Hv + h) * (size_t)nch + (size_t)c) * WS_UNIT;
+}
+
+// Sequence n of a variable-length batch for chunk cl of the grid: cb[n] <= cl < cb[n+1]
+// (binary search over the N + 1 chunk bases).
+__device__ __forceinline__ int seq_of_chunk(const int* cb, int N, int cl) {
+    int lo = 0, hi = N;  // invariant: cb[lo] <= cl < cb[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (cb[mid] <= cl) lo = mid; else hi = mid;
+    }
+    return lo;
 }
 
 __device__ __forceinline__ void bar_sync(uint32_t id, uint32_t n) {
@@ -505,23 +522,36 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
     };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int cl = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int c = a.c0 + cl;           // the chunk's position in the sequence
+    const int cl = blockIdx.x, h = blockIdx.y;
     const int kh = h / (a.Hv / a.Hk);  // value head h reads key head h // (Hv/Hk)
     const int S = a.S;
     const int nch = a.nseg;
+    // the chunk: its first token `tc` and token bound `tend` in the [heads][S] tensors
+    // (a variable-length batch packs its sequences along S; the grid then covers an upper
+    // bound of their chunks and the surplus CTAs leave at once)
+    int b = blockIdx.z, tc, tend;
+    if (a.cu == nullptr) {
+        tc = (a.c0 + cl) * C;
+        tend = S;
+    } else {
+        if (cl >= a.cb[a.N]) return;
+        const int n = seq_of_chunk(a.cb, a.N, cl);
+        tc = a.cu[n] + (cl - a.cb[n]) * C;
+        tend = a.cu[n + 1];
+        b = 0;
+    }
 
     const int zq = b * a.Hk + kh, zv = b * a.Hv + h;
     // g and beta of the chunk are loaded first and the copies of Q and K started at
-    // once, so that their latency overlaps the setup (padding tokens: g = beta = 0,
-    // an exact no-op)
+    // once, so that their latency overlaps the setup (padding tokens -- past the end of
+    // the sequence -- get g = beta = 0, an exact no-op)
     float x0 = 0.f, x1 = 0.f, be0 = 0.f, be1 = 0.f;
     if (warp == 0) {
         const float* gp = a.g + (size_t)zv * S;
         const float* bp = a.beta + (size_t)zv * S;
-        const int t0 = c * C + lane, t1 = t0 + 32;
-        if (t0 < S) x0 = gp[t0], be0 = bp[t0];
-        if (t1 < S) x1 = gp[t1], be1 = bp[t1];
+        const int t0 = tc + lane, t1 = t0 + 32;
+        if (t0 < tend) x0 = gp[t0], be0 = bp[t0];
+        if (t1 < tend) x1 = gp[t1], be1 = bp[t1];
     }
     if (tid == 0) {
         for (int i = 0; i < PB_COUNT; ++i) mbar_init(&bar[i], i == PB_FULL ? 2 : 1);
@@ -529,8 +559,8 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
         fence_mbar_init();
         mbar_arrive_expect_tx(&bar[PB_FULL], 2 * 16384);
         for (int blk = 0; blk < 2; ++blk) {
-            tma_load_3d(sm + blk * PQ_STRIDE + PQ_Q, &mq, &bar[PB_FULL], blk * 64, c * C, zq);
-            tma_load_3d(sm + blk * PQ_STRIDE + PQ_K, &mk, &bar[PB_FULL], blk * 64, c * C, zq);
+            tma_load_3d(sm + blk * PQ_STRIDE + PQ_Q, &mq, &bar[PB_FULL], blk * 64, tc, zq);
+            tma_load_3d(sm + blk * PQ_STRIDE + PQ_K, &mk, &bar[PB_FULL], blk * 64, tc, zq);
         }
         TRACE_PREP(20);
     }
@@ -836,9 +866,28 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
     CarryScalars* scal = reinterpret_cast<CarryScalars*>(sm + Cfg::SCAL);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int n0 = blockIdx.x * NS, h = blockIdx.y, b = blockIdx.z;
+    const int n0 = blockIdx.x * NS, h = blockIdx.y;
     const int S = a.S;
-    const int nch = a.nseg;  // chunks of this launch: a.c0 .. a.c0 + nch - 1
+    // The sequence of this CTA: its chunks (the workspace units u0 .. u0 + nch - 1 of
+    // head row `wb`), first token `tbase`, token bound `tend`, state row `sb`. Dense
+    // layout: batch b, chunks a.c0 .. a.c0 + a.nseg - 1. Variable-length batch: sequence
+    // blockIdx.z, its packed tokens cu[n] .. cu[n+1] - 1.
+    int wb, u0, nch, tbase, tend, sb;
+    if (a.cu == nullptr) {
+        wb = blockIdx.z, u0 = 0, nch = a.nseg, tbase = a.c0 * C, tend = S;
+        sb = blockIdx.z * a.Hv + h;
+    } else {
+        const int n = blockIdx.z;
+        wb = 0, u0 = a.cb[n], nch = a.cb[n + 1] - a.cb[n], tbase = a.cu[n], tend = a.cu[n + 1];
+        sb = n * a.Hv + h;
+    }
+    if (nch == 0) {
+        // an empty sequence: the state passes through (zero when none was supplied)
+        if (!a.state_is_input)
+            for (int i = tid; i < 128 * NS; i += CARRY_THREADS)
+                a.state[((size_t)sb * 128 + i / NS) * 128 + n0 + i % NS] = 0.f;
+        return;
+    }
 
     if (tid == 0) {
         for (int i = 0; i < B_COUNT; ++i)
@@ -859,8 +908,8 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------- loads (one thread)
         if (lane == 0) {
-            const int zv = b * a.Hv + h;
-            const uint8_t* wsh = a.ws + ws_offset(b, h, 0, a.Hv, nch);
+            const int zv = wb * a.Hv + h;
+            const uint8_t* wsh = a.ws + ws_offset(wb, h, u0, a.Hv, a.nseg);
             int issued = 0;
             for (int c = 0; c < nch; ++c) {
                 const int s = c & 1;
@@ -880,7 +929,7 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
                     bulk_g2s(sb + OFF_Q, wsc + WS_QT + blk * 8192, 8192, fe);
                 }
                 for (int blk = 0; blk < Cfg::NB; ++blk)
-                    tma_load_3d(st + OFF_V + blk * 8192, &mv, fe, n0 + blk * 64, (a.c0 + c) * C,
+                    tma_load_3d(st + OFF_V + blk * 8192, &mv, fe, n0 + blk * 64, tbase + c * C,
                                 zv);
                 bulk_g2s(st + Cfg::OFF_TU, wsc + WS_TU, 8192, fe);
                 // late group of chunk c: K~, P, scalars
@@ -897,7 +946,7 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
                 // chunk c + 2 goes to L2 now
                 if (c + 2 < nch) {
                     for (int blk = 0; blk < Cfg::NB; ++blk)
-                        tma_prefetch_l2_3d(&mv, n0 + blk * 64, (a.c0 + c + 2) * C, zv);
+                        tma_prefetch_l2_3d(&mv, n0 + blk * 64, tbase + (c + 2) * C, zv);
                     bulk_prefetch_l2(wsc + 2 * WS_UNIT, WS_UNIT);
                 }
             }
@@ -919,8 +968,8 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
         const int col0 = CPT * hc;  // first state column of this thread within the slice
         const uint32_t lane_off = ((uint32_t)(32 * q) << 16) + (uint32_t)col0;
         const uint32_t s_base = sbase + Cfg::SM_S, u_tile = sbase + Cfg::U;
-        float* gstate = a.state + ((size_t)(b * a.Hv + h) * 128 + L) * 128 + n0 + col0;
-        __nv_bfloat16* gout = a.out + (size_t)(b * a.Hv + h) * S * 128 + n0 + col0;
+        float* gstate = a.state + ((size_t)sb * 128 + L) * 128 + n0 + col0;
+        __nv_bfloat16* gout = a.out + (size_t)(wb * a.Hv + h) * S * 128 + n0 + col0;
         // 32-column piece p of this thread: tile block and 16-byte chunk within the block
         auto pblk = [&](int p) { return (uint32_t)((col0 + 32 * p) >> 6); };
         auto pch = [&](int p) { return ((col0 + 32 * p) & 63) >> 3; };
@@ -947,13 +996,13 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
 
         // out = scale (Q~ S0 + P U) of chunk cc for token L - 64 (quadrants 2, 3)
         auto write_out = [&](int cc) {
-            const int t = (a.c0 + cc) * C + (L - 64);
+            const int t = tbase + cc * C + (L - 64);
             const uint32_t ta = Cfg::TMA + (uint32_t)NS * (uint32_t)(cc & 1);
 #pragma unroll
             for (int p = 0; p < NP; ++p) {
                 float o[32];
                 tmem_ld32(tmem + lane_off + ta + 32 * p, o);
-                if (t < S) {
+                if (t < tend) {
                     uint4* dst = reinterpret_cast<uint4*>(gout + (size_t)t * 128 + 32 * p);
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -1130,6 +1179,62 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
     }
 }
 
+// ---------------------------------------------------------------- variable-length batch
+
+// One CTA: table[0..N] = chunk bases of the sequences cu[n] .. cu[n+1] - 1 in 64-token
+// chunks (block-wide scan in tiles of 1024), table[N+1] = 1. A malformed cu (cu[0] != 0,
+// a decreasing step or cu[N] > S) zeroes the table -- every sequence then counts as
+// empty -- and sets the status bit instead.
+__global__ void __launch_bounds__(1024) varlen_setup_kernel(const int* cu, int N, int S,
+                                                            int* table) {
+    __shared__ int wsum[32];
+    __shared__ int carry, bad;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    if (tid == 0) {
+        carry = 0;
+        bad = (cu[0] != 0 || cu[N] > S) ? 1 : 0;
+        table[0] = 0;
+    }
+    __syncthreads();
+    for (int base = 0; base < N; base += 1024) {
+        const int n = base + tid;
+        int x = 0;
+        if (n < N) {
+            const int len = cu[n + 1] - cu[n];
+            if (len < 0) atomicOr(&bad, 1);
+            x = len > 0 ? (len + C - 1) / C : 0;
+        }
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, off);
+            if (lane >= off) x += y;
+        }
+        if (lane == 31) wsum[w] = x;
+        __syncthreads();
+        if (w == 0) {
+            int v = wsum[lane];
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, v, off);
+                if (lane >= off) v += y;
+            }
+            wsum[lane] = v;
+        }
+        __syncthreads();
+        const int incl = x + (w > 0 ? wsum[w - 1] : 0);
+        if (n < N) table[n + 1] = carry + incl;
+        __syncthreads();
+        if (tid == 1023) carry += incl;
+        __syncthreads();
+    }
+    if (bad) {
+        for (int n = tid; n <= N + 1; n += 1024) table[n] = 0;
+        if (tid == 0) atomicOr(&g_tc_status, kStatusBadSeqlens);
+    } else if (tid == 0) {
+        table[N + 1] = 1;
+    }
+}
+
 // ---------------------------------------------------------------- host side
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -1173,6 +1278,22 @@ size_t prefill_tc_workspace_bytes(int B, int Hv, int S) {
 size_t prefill_tc_unit_bytes() { return WS_UNIT; }
 
 namespace {
+size_t varlen_units_bytes(int N, int Hv, int S) {
+    const size_t nmax = ((size_t)S + C - 1) / C + (size_t)N;
+    return ((size_t)Hv * nmax * WS_UNIT + 255) / 256 * 256;
+}
+}  // namespace
+
+size_t prefill_tc_varlen_workspace_bytes(int N, int Hv, int S) {
+    return varlen_units_bytes(N, Hv, S) + varlen_table_ints(N) * sizeof(int);
+}
+
+cudaError_t launch_varlen_setup(const PrefillArgs& a, cudaStream_t stream) {
+    varlen_setup_kernel<<<1, 1024, 0, stream>>>(a.cu_seqlens, a.N, a.S, a.table);
+    return cudaGetLastError();
+}
+
+namespace {
 
 // The two kernels of one segment of the sequence (chunks c0 .. c0 + nseg - 1), whose
 // B Hv nseg workspace units start at `ws`.
@@ -1185,11 +1306,13 @@ struct SegmentLaunch {
         const int sin = (c0 > 0 || a->state_is_input) ? 1 : 0;
         return TcArgs{a->g,     a->beta, a->scale, a->B, a->Hk,  a->Hv,
                       a->S,     c0,      nseg,     a->state, sin,
-                      static_cast<__nv_bfloat16*>(a->out), ws};
+                      static_cast<__nv_bfloat16*>(a->out), ws, a->cu_seqlens, a->table, a->N};
     }
+    // sequences of the carry grid: the batch, or the variable-length batch's sequences
+    int rows() const { return a->cu_seqlens ? a->N : a->B; }
     // two carry CTAs per head (64-column state slices) while that still fits the GPU in
     // one wave, else one CTA per head (128 columns: half the MMA instructions per head)
-    bool split() const { return 2 * a->B * a->Hv <= sms; }
+    bool split() const { return 2 * rows() * a->Hv <= sms; }
 
     cudaError_t prep(int c0, int nseg, uint8_t* ws, cudaStream_t st) const {
         prep_tc_kernel<<<dim3(nseg, a->Hv, a->B), PREP_THREADS, PREP_SMEM, st>>>(
@@ -1198,11 +1321,12 @@ struct SegmentLaunch {
     }
     cudaError_t carry(int c0, int nseg, uint8_t* ws, cudaStream_t st) const {
         if (split())
-            carry_tc_kernel<64><<<dim3(2, a->Hv, a->B), CARRY_THREADS, CarryCfg<64>::SMEM, st>>>(
-                mv, args(c0, nseg, ws));
+            carry_tc_kernel<64>
+                <<<dim3(2, a->Hv, rows()), CARRY_THREADS, CarryCfg<64>::SMEM, st>>>(
+                    mv, args(c0, nseg, ws));
         else
             carry_tc_kernel<128>
-                <<<dim3(1, a->Hv, a->B), CARRY_THREADS, CarryCfg<128>::SMEM, st>>>(
+                <<<dim3(1, a->Hv, rows()), CARRY_THREADS, CarryCfg<128>::SMEM, st>>>(
                     mv, args(c0, nseg, ws));
         return cudaGetLastError();
     }
@@ -1295,6 +1419,31 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, int c0, int nseg, cudaStream
     *launched = 1;
     e = L.carry(c0, nseg, ws, stream);
     if (e == cudaSuccess) *launched = 2;
+    return e;
+}
+
+cudaError_t launch_prefill_tc_varlen(const PrefillArgs& a, cudaStream_t stream, int* launched) {
+    *launched = 0;
+    if (a.workspace == nullptr || a.cu_seqlens == nullptr || a.B != 1 ||
+        a.workspace_bytes < prefill_tc_varlen_workspace_bytes(a.N, a.Hv, a.S))
+        return cudaErrorInvalidValue;
+    PrefillArgs v = a;
+    v.table = reinterpret_cast<int*>(static_cast<uint8_t*>(a.workspace) +
+                                     varlen_units_bytes(a.N, a.Hv, a.S));
+    SegmentLaunch L{};
+    cudaError_t e = prepare(L, v);
+    if (e != cudaSuccess) return e;
+    e = launch_varlen_setup(v, stream);
+    if (e != cudaSuccess) return e;
+    *launched = 1;
+    // the prep grid covers the chunk bound ceil(S/64) + N; CTAs past the last chunk leave
+    const int nmax = (a.S + C - 1) / C + a.N;
+    uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+    e = L.prep(0, nmax, ws, stream);
+    if (e != cudaSuccess) return e;
+    *launched = 2;
+    e = L.carry(0, nmax, ws, stream);
+    if (e == cudaSuccess) *launched = 3;
     return e;
 }
 

@@ -25,6 +25,7 @@ STATUS_NAMES = {0: "GDN_OK", 1: "GDN_EINVAL", 2: "GDN_EUNSUPPORTED", 3: "GDN_ECU
 
 # Every symbol include/gdn.h declares.
 EXPORTS = ("gdn_prefill_workspace_bytes", "gdn_prefill", "gdn_prefill_noalloc",
+           "gdn_prefill_varlen_workspace_bytes", "gdn_prefill_varlen",
            "gdn_decode_step", "gdn_decode_multi", "gdn_conv1d_decode", "gdn_last_error",
            "gdn_get_device_status", "gdn_launch_count")
 
@@ -58,6 +59,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gdn_prefill_noalloc.argtypes = [vp, vp, vp, vp, vp, f, i, i, i, i, i, i, i, vp, i,
                                             vp, vp]
         lib.gdn_prefill_noalloc.restype = i
+        lib.gdn_prefill_varlen_workspace_bytes.argtypes = [i] * 7
+        lib.gdn_prefill_varlen_workspace_bytes.restype = sz
+        lib.gdn_prefill_varlen.argtypes = [vp, vp, vp, vp, vp, f, i, vp, i, i, i, i, i, i, vp,
+                                           i, vp, vp, sz, vp]
+        lib.gdn_prefill_varlen.restype = i
         lib.gdn_decode_step.argtypes = [vp] * 12 + [i] * 4 + [vp]
         lib.gdn_decode_step.restype = i
         lib.gdn_decode_multi.argtypes = [vp] * 12 + [i] * 5 + [vp]
@@ -270,3 +276,44 @@ def gdn_conv1d_decode(x, conv_weight, conv_state_in, num_k_heads, num_v_heads, h
         _ptr(k), _ptr(v), B, num_k_heads, num_v_heads, head_k_dim, head_v_dim, K_win,
         _stream(stream)))
     return q, k, v, conv_state_out
+
+
+def gdn_prefill_varlen_workspace_bytes(N, Hk, Hv, T, Dk, Dv, dtype) -> int:
+    dt = GDN_DTYPE_BF16 if dtype == torch.bfloat16 else GDN_DTYPE_F32
+    n = load_library().gdn_prefill_varlen_workspace_bytes(N, Hk, Hv, T, Dk, Dv, dt)
+    if n == ctypes.c_size_t(-1).value:
+        raise GDNError(GDN_EINVAL, "invalid shape")
+    return n
+
+
+def gdn_prefill_varlen(q, k, v, g_log, beta, scale, cu_seqlens, state=None, out=None,
+                       workspace=None, stream=None):
+    """Variable-length prefill: q,k [Hk,T,Dk], v [Hv,T,Dv], g_log, beta [Hv,T], cu_seqlens
+    [N+1] int32 on the device (sequence n = tokens cu[n] .. cu[n+1]-1). ``state`` [N,Hv,Dk,Dv]
+    fp32 is updated in place when given, else zero-initialised and returned. Returns
+    (out [Hv,T,Dv], state)."""
+    Hk, T, Dk = q.shape
+    Hv, Dv = v.shape[0], v.shape[2]
+    N = cu_seqlens.shape[0] - 1
+    dev, dt = q.device, q.dtype
+    code = GDN_DTYPE_BF16 if dt == torch.bfloat16 else GDN_DTYPE_F32
+    _need(k, "k", dt, (Hk, T, Dk), dev)
+    _need(v, "v", dt, (Hv, T, Dv), dev)
+    _need(g_log, "g_log", torch.float32, (Hv, T), dev)
+    _need(beta, "beta", torch.float32, (Hv, T), dev)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, (N + 1,), dev)
+    state_is_input = state is not None
+    if state is None:
+        state = torch.empty((N, Hv, Dk, Dv), dtype=torch.float32, device=dev)
+    _need(state, "state", torch.float32, (N, Hv, Dk, Dv), dev)
+    if out is None:
+        out = torch.empty((Hv, T, Dv), dtype=dt, device=dev)
+    _need(out, "out", dt, (Hv, T, Dv), dev)
+    need = gdn_prefill_varlen_workspace_bytes(N, Hk, Hv, T, Dk, Dv, dt)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    _check(load_library().gdn_prefill_varlen(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g_log), _ptr(beta), float(scale), code,
+        _ptr(cu_seqlens), N, Hk, Hv, T, Dk, Dv, _ptr(state), int(state_is_input), _ptr(out),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out, state

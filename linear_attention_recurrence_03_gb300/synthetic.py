@@ -80,6 +80,42 @@ PREFILL_WORKLOADS = (PREFILL_F32_SMALL, PREFILL_BF16_GQA2, PREFILL_BF16_LAYER,
                      PREFILL_BF16_BATCHED)
 
 
+@dataclass(frozen=True)
+class VarlenWorkload:
+    """A variable-length batch: N sequences packed along the token axis, lengths drawn
+    uniformly from [len_lo, len_hi] (a mix of short and long prompts), the layer's heads
+    and distributions otherwise."""
+    name: str
+    base: PrefillWorkload
+    N: int
+    len_lo: int
+    len_hi: int
+    seed: int = 0
+
+    def lengths(self) -> list[int]:
+        gen = torch.Generator().manual_seed(self.seed + 7)
+        return torch.randint(self.len_lo, self.len_hi + 1, (self.N,), generator=gen).tolist()
+
+
+PREFILL_BF16_VARLEN = VarlenWorkload("prefill_bf16_varlen_n16_len256to4096_hk16_hv32_d128",
+                                     PREFILL_BF16_LAYER, N=16, len_lo=256, len_hi=4096)
+
+
+def varlen_inputs(w: VarlenWorkload) -> dict:
+    """CPU tensors of a packed batch ([H, T, D] q, k, v; [Hv, T] g_log, beta), drawn as
+    prefill_inputs for one row of T = sum(lengths) tokens, then cu_seqlens (int32)."""
+    lengths = w.lengths()
+    T = int(sum(lengths))
+    x = prefill_inputs(replace(w.base, B=1, S=T, state_std=None), seed=w.seed)
+    out = {n: x[n][0] for n in ("q", "k", "v", "g_log", "beta")}
+    cu = [0]
+    for L in lengths:
+        cu.append(cu[-1] + L)
+    out["cu_seqlens"] = torch.tensor(cu, dtype=torch.int32)
+    out["scale"] = x["scale"]
+    return out
+
+
 def shrink(w: PrefillWorkload, **kw) -> PrefillWorkload:
     """Same distributions, other sizes (for small parity cases)."""
     return replace(w, **kw)

@@ -13,6 +13,7 @@ from .oracle import (  # noqa: F401
     decode_step,
     prefill,
     prefill_chunked,
+    prefill_varlen,
     unit_lower_inverse,
     EPS_L2,
     EPS_RMS,

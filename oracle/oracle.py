@@ -114,6 +114,30 @@ class Oracle:
             raise ValueError("oracle prefill_chunked: bad shapes")
         return out, st
 
+    def prefill_varlen(self, q, k, v, g_log, beta, scale, cu_seqlens, state0=None,
+                       nthreads=None):
+        """Variable-length batch: sequence n = tokens cu[n] .. cu[n+1]-1 of q,k [Hk,T,Dk],
+        v [Hv,T,Dv], g_log, beta [Hv,T], each run through ``prefill`` from its own state
+        (state0 [N,Hv,Dk,Dv] or None = zeros). Returns (out [Hv,T,Dv] -- zero past cu[N] --,
+        state [N,Hv,Dk,Dv])."""
+        q, k, v, g, b = map(_f64, (q, k, v, g_log, beta))
+        cu = [int(x) for x in np.asarray(cu_seqlens).reshape(-1)]
+        N = len(cu) - 1
+        Hk, T, Dk = q.shape
+        Hv, Dv = v.shape[0], v.shape[2]
+        out = np.zeros((Hv, T, Dv))
+        st = np.zeros((N, Hv, Dk, Dv)) if state0 is None else _f64(state0).copy()
+        for n in range(N):
+            t0, t1 = cu[n], cu[n + 1]
+            if t1 <= t0:
+                continue
+            o, s1 = self.prefill(q[None, :, t0:t1], k[None, :, t0:t1], v[None, :, t0:t1],
+                                 g[None, :, t0:t1], b[None, :, t0:t1], scale,
+                                 st[n][None], nthreads)
+            out[:, t0:t1] = o[0]
+            st[n] = s1[0]
+        return out, st
+
     def unit_lower_inverse(self, A):
         """(I + A)^-1 for strictly lower-triangular square A (forward substitution)."""
         A = _f64(A)
@@ -210,6 +234,10 @@ def prefill_chunked(*args, **kw):
 
 def unit_lower_inverse(A):
     return default().unit_lower_inverse(A)
+
+
+def prefill_varlen(*args, **kw):
+    return default().prefill_varlen(*args, **kw)
 
 
 def decode_step(*args, **kw):

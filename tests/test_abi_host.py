@@ -146,6 +146,27 @@ def test_conv1d_rejects_bad_arguments(lib, kw, msg):
     assert msg in lib.gdn_last_error().decode()
 
 
+def test_varlen_workspace_query(lib):
+    # tensor-core path: Hv * (ceil(T/64) + N) units of 66560 bytes (to 256), then the
+    # N + 2 ints of the chunk table; fp32 / other head dims: the table alone (to 16)
+    units = 32 * (4096 // 64 + 5) * 66560
+    assert lib.gdn_prefill_varlen_workspace_bytes(5, 16, 32, 4096, 128, 128, 1) == \
+        (units + 255) // 256 * 256 + 4 * 7
+    assert lib.gdn_prefill_varlen_workspace_bytes(5, 2, 2, 100, 64, 64, 0) == 32
+    assert lib.gdn_prefill_varlen_workspace_bytes(-1, 2, 2, 100, 64, 64, 0) == \
+        ctypes.c_size_t(-1).value
+
+
+@pytest.mark.parametrize("N,ws,msg", [(-1, 1 << 20, "N <="), (70000, 1 << 20, "N <="),
+                                      (3, 8, "workspace")])
+def test_varlen_rejects_bad_arguments(lib, N, ws, msg):
+    vp = ctypes.c_void_p
+    rc = lib.gdn_prefill_varlen(vp(16), vp(16), vp(16), vp(16), vp(16), 1.0, 0, vp(16), N, 2, 2,
+                                100, 64, 64, vp(16), 0, vp(16), vp(16), ws, None)
+    assert rc == gdn.GDN_EINVAL
+    assert msg in lib.gdn_last_error().decode()
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError, match="missing"):
         gdn.load_library(str(tmp_path / "libgdn.so"))

@@ -501,3 +501,41 @@ def test_conv1d_split_is_repeat_interleave(oracle_mod):
     np.testing.assert_array_equal(q, qr.reshape(B * Hv, Dk).numpy())
     np.testing.assert_array_equal(k, kr.reshape(B * Hv, Dk).numpy())
     np.testing.assert_array_equal(v, t[:, 2 * Hk * Dk:].reshape(B * Hv, Dv).numpy())
+
+
+# ------------------------------------------------------------ variable-length batches
+def test_varlen_equal_lengths_is_the_dense_batch(oracle_mod):
+    """N sequences of one length L packed along the token axis give the dense batch
+    (B = N, S = L) result, row for row."""
+    rng = np.random.default_rng(40)
+    N, Hk, Hv, L, D = 3, 2, 4, 7, 5
+    q = _unit(rng.standard_normal((N, Hk, L, D)))
+    k = _unit(rng.standard_normal((N, Hk, L, D)))
+    v = rng.standard_normal((N, Hv, L, D))
+    g = rng.uniform(-0.5, -0.01, (N, Hv, L))
+    b = rng.uniform(0.05, 0.95, (N, Hv, L))
+    s0 = rng.standard_normal((N, Hv, D, D)) * 0.1
+    o_d, s_d = oracle_mod.prefill(q, k, v, g, b, 0.5, s0)
+    pack = lambda x: np.concatenate(list(x), axis=1)  # [N, H, L, ...] -> [H, N*L, ...]
+    cu = np.arange(N + 1) * L
+    o_v, s_v = oracle_mod.prefill_varlen(pack(q), pack(k), pack(v), pack(g), pack(b), 0.5, cu,
+                                         s0)
+    np.testing.assert_allclose(o_v, pack(o_d), rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(s_v, s_d, rtol=1e-13, atol=1e-15)
+
+
+def test_varlen_empty_sequences_keep_their_state(oracle_mod):
+    rng = np.random.default_rng(41)
+    Hk, Hv, T, D = 1, 2, 6, 4
+    q = _unit(rng.standard_normal((Hk, T, D)))
+    k = _unit(rng.standard_normal((Hk, T, D)))
+    v = rng.standard_normal((Hv, T, D))
+    g = rng.uniform(-0.5, -0.01, (Hv, T))
+    b = rng.uniform(0.05, 0.95, (Hv, T))
+    s0 = rng.standard_normal((3, Hv, D, D))
+    out, st = oracle_mod.prefill_varlen(q, k, v, g, b, 1.0, [0, 0, 6, 6], s0)
+    np.testing.assert_array_equal(st[0], s0[0])
+    np.testing.assert_array_equal(st[2], s0[2])
+    o1, s1 = oracle_mod.prefill(q[None], k[None], v[None], g[None], b[None], 1.0, s0[1][None])
+    np.testing.assert_array_equal(st[1], s1[0])
+    np.testing.assert_array_equal(out, o1[0])
