@@ -27,6 +27,8 @@ import sys
 import tempfile
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
@@ -52,6 +54,8 @@ def parse_args():
                    help="skip the multi-token decode measurement (T = 2, 4, 8 tokens per call)")
     p.add_argument("--no-conv", action="store_true",
                    help="skip the conv1d decode measurement (B = 256, 8192 channels)")
+    p.add_argument("--no-tril", action="store_true",
+                   help="skip the intra-chunk inverse comparison (substitution vs Neumann)")
     p.add_argument("--no-varlen", action="store_true",
                    help="skip the variable-length prefill measurement (16 packed sequences)")
     p.add_argument("--spinup-seconds", type=float, default=1.0,
@@ -532,6 +536,49 @@ def run_gdn(args):
             "tokens_per_s": ws * Tv / (v_ms * 1e-3), "achieved_gbs": vb / (v_ms * 1e-3) / 1e9,
             "frac_of_roofline": rv / (v_ms * 1e-3), "api": "gdn_prefill_varlen"}
         del VX, v_out, v_state, v_ws
+
+    # the intra-chunk inverse on its own: 4096 chunk matrices (the layer's chunks x heads),
+    # forward substitution against the Neumann product
+    if not args.no_tril:
+        nA = wp.Hv * (wp.S // 64)
+        rng = np.random.default_rng(0)
+        kk = rng.standard_normal((nA, 64, 128)).astype(np.float32)
+        kk /= np.linalg.norm(kk, axis=-1, keepdims=True)
+        bet = rng.uniform(0.05, 0.95, (nA, 64)).astype(np.float32)
+        gam = np.cumsum(rng.uniform(-0.3, -0.005, (nA, 64)), axis=1).astype(np.float32)
+        Ah = np.tril(bet[:, :, None] * np.einsum("nrd,njd->nrj", kk, kk)
+                     * np.exp(gam[:, :, None] - gam[:, None, :]), -1).astype(np.float32)
+        Ad = torch.from_numpy(Ah).to(dev)
+        Td = torch.empty_like(Ad)
+        tri = {"matrices": nA, "C": 64, "kernel": "tril_inverse.cu",
+               "api": "gdn_unit_lower_inverse"}
+        outs = {}
+        for alg, name in ((gdn.GDN_TRIL_SUBSTITUTION, "substitution"),
+                          (gdn.GDN_TRIL_NEUMANN, "neumann")):
+            def tri_run():
+                rc = lib.gdn_unit_lower_inverse(vp(Ad.data_ptr()), vp(Td.data_ptr()), nA, 64,
+                                                alg, sptr)
+                if rc != 0:
+                    raise RuntimeError(gdn.gdn_last_error())
+            for _ in range(args.warmup):
+                tri_run()
+            torch.cuda.synchronize()
+            et0 = torch.cuda.Event(enable_timing=True)
+            et1 = torch.cuda.Event(enable_timing=True)
+            et0.record(stream)
+            for _ in range(K):
+                tri_run()
+            et1.record(stream)
+            torch.cuda.synchronize()
+            t_ms = reduce_max([et0.elapsed_time(et1) / K], ws)[0]
+            outs[name] = Td.clone()
+            flops = 2.0 * nA * (64 ** 3 / 3 if name == "substitution" else 11 * 64 ** 3)
+            tri[name] = {"ms": t_ms, "us_per_matrix": t_ms * 1e3 / nA,
+                         "executed_tflops": flops / (t_ms * 1e-3) / 1e12}
+        tri["neumann_rel_diff_vs_substitution"] = float(
+            (outs["neumann"] - outs["substitution"]).norm() / outs["substitution"].norm())
+        result["tril_inverse"] = tri
+        del Ad, Td, outs
 
     # conv1d decode token in front of the decode step: B = 256, 8192 q|k|v channels,
     # K_win = 4, window in place

@@ -49,6 +49,12 @@ typedef enum gdn_dtype {
     GDN_DTYPE_BF16 = 1
 } gdn_dtype;
 
+/* Intra-chunk inverse methods of gdn_unit_lower_inverse. */
+typedef enum gdn_tril_algorithm {
+    GDN_TRIL_SUBSTITUTION = 0, /* forward substitution, fp32                          */
+    GDN_TRIL_NEUMANN = 1       /* (I+X)(I+X^2)...(I+X^32), X = -A, tf32 tensor cores  */
+} gdn_tril_algorithm;
+
 /* Largest head dimension: "GDN CTE Kernel API Reference", Notes (Dk, Dv <= 128). */
 #define GDN_MAX_HEAD_DIM 128
 
@@ -208,6 +214,29 @@ gdn_status gdn_decode_multi(const void* q, const void* k, const void* v, const v
                             const void* z, const float* norm_weight, const float* state_in,
                             float* state_out, void* out, int T, int BH, int num_v_heads, int K,
                             int V, void* stream);
+
+/*
+ * gdn_unit_lower_inverse -- T = (I + A)^-1 for n strictly lower-triangular C x C fp32
+ * matrices, the chunked prefill's intra-chunk inverse, by the method `algorithm` selects
+ * ("GDN CTE Kernel API Reference", :param algorithm: -- the pages offer a selectable
+ * inverse, "neumann" among them; this call exposes the choice on its own so the two
+ * methods can be compared):
+ *   GDN_TRIL_SUBSTITUTION  forward substitution in fp32 (rounding only);
+ *   GDN_TRIL_NEUMANN       sum_{n<C} X^n with X = -A (nilpotent), as the product
+ *                          (I + X)(I + X^2)...(I + X^(C/2)): log2(C) rounds of tf32
+ *                          tensor-core products (relative error ~1e-3 for |A| <= 1).
+ *
+ *   A  device, [n, C, C] fp32, row-major; entries on and above the diagonal are read
+ *      as zero by neither method's definition, so they must BE zero.
+ *   T  device, [n, C, C] fp32, unit lower triangular. May equal A (in place); must not
+ *      otherwise overlap it.
+ *   C == 64 (GDN_EUNSUPPORTED otherwise); n == 0 enqueues nothing.
+ *
+ * Errors: GDN_EINVAL for n < 0, an unknown algorithm, a NULL/misaligned pointer or a
+ * partial overlap; GDN_ECUDA if the launch fails.
+ */
+gdn_status gdn_unit_lower_inverse(const float* A, float* T, int n, int C, int algorithm,
+                                  void* stream);
 
 /*
  * gdn_conv1d_decode -- the step in front of the decode step: one token of the q|k|v

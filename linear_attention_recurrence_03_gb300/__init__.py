@@ -8,6 +8,8 @@ thin Python binding of the same names:
 * ``gdn_prefill_varlen`` -- the same over sequences packed by ``cu_seqlens``.
 * ``gdn_decode_step``  -- fused single-token decode step ("GDN TKG Kernel API Reference").
 * ``gdn_decode_multi`` -- T consecutive decode tokens in one call (state read once).
+* ``gdn_unit_lower_inverse`` -- the intra-chunk (I + A)^-1 by forward substitution or
+  the Neumann product (the prefill's selectable inverse method, on its own).
 * ``gdn_conv1d_decode`` -- the conv1d decode token feeding the decode step ("GDN Block
   TKG Kernel API Reference").
 """
@@ -20,6 +22,8 @@ from .gdn import (  # noqa: F401
     GDN_ETIMEOUT,
     GDN_EUNSUPPORTED,
     GDN_OK,
+    GDN_TRIL_NEUMANN,
+    GDN_TRIL_SUBSTITUTION,
     GDNError,
     gdn_conv1d_decode,
     gdn_decode_multi,
@@ -32,5 +36,6 @@ from .gdn import (  # noqa: F401
     gdn_prefill_varlen,
     gdn_prefill_varlen_workspace_bytes,
     gdn_prefill_workspace_bytes,
+    gdn_unit_lower_inverse,
     load_library,
 )

@@ -299,6 +299,33 @@ gdn_status gdn_conv1d_decode(const void* x, const float* conv_weight, const void
     return GDN_OK;
 }
 
+gdn_status gdn_unit_lower_inverse(const float* A, float* T, int n, int C, int algorithm,
+                                  void* stream) {
+    if (n < 0 || n > (1 << 30) / (64 * 64))
+        return fail(GDN_EINVAL, "gdn_unit_lower_inverse: need 0 <= n (got %d)", n);
+    if (C != 64)
+        return fail(GDN_EUNSUPPORTED, "gdn_unit_lower_inverse: only C = 64 (got %d)", C);
+    if (algorithm != GDN_TRIL_SUBSTITUTION && algorithm != GDN_TRIL_NEUMANN)
+        return fail(GDN_EINVAL, "gdn_unit_lower_inverse: unknown algorithm %d", algorithm);
+    if (!ptr_ok(A, n > 0) || !ptr_ok(T, n > 0))
+        return fail(GDN_EINVAL, "gdn_unit_lower_inverse: A and T must be non-NULL, 16-byte "
+                    "aligned device pointers");
+    if (A != T && n > 0) {
+        const uintptr_t a0 = reinterpret_cast<uintptr_t>(A), t0 = reinterpret_cast<uintptr_t>(T);
+        const uintptr_t bytes = (uintptr_t)n * 64 * 64 * sizeof(float);
+        if (a0 < t0 + bytes && t0 < a0 + bytes)
+            return fail(GDN_EINVAL, "gdn_unit_lower_inverse: T overlaps A without being "
+                        "equal to it");
+    }
+    const cudaError_t e = gdn::launch_tril_inverse(A, T, n, algorithm,
+                                                   static_cast<cudaStream_t>(stream));
+    if (n > 0) g_launches += 1;
+    if (e != cudaSuccess)
+        return fail(GDN_ECUDA, "gdn_unit_lower_inverse: launch failed: %s",
+                    cudaGetErrorString(e));
+    return GDN_OK;
+}
+
 const char* gdn_last_error(void) { return g_last_error.c_str(); }
 
 unsigned long long gdn_launch_count(void) { return g_launches.load(); }

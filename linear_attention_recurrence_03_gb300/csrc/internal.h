@@ -108,6 +108,11 @@ struct Conv1dArgs {
 };
 cudaError_t launch_conv1d_decode(const Conv1dArgs& a, cudaStream_t stream);
 
+// (I + A)^-1 of n strictly lower-triangular 64 x 64 fp32 matrices: algorithm 0 forward
+// substitution, 1 the Neumann product on the tensor cores.
+cudaError_t launch_tril_inverse(const float* A, float* T, int n, int algorithm,
+                                cudaStream_t stream);
+
 // Fused decode step, T tokens in a row (the state read and written once).
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 

@@ -20,13 +20,15 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgdn.so")
 
 GDN_OK, GDN_EINVAL, GDN_EUNSUPPORTED, GDN_ECUDA, GDN_ETIMEOUT = range(5)
 GDN_DTYPE_F32, GDN_DTYPE_BF16 = 0, 1
+GDN_TRIL_SUBSTITUTION, GDN_TRIL_NEUMANN = 0, 1
 STATUS_NAMES = {0: "GDN_OK", 1: "GDN_EINVAL", 2: "GDN_EUNSUPPORTED", 3: "GDN_ECUDA",
                 4: "GDN_ETIMEOUT"}
 
 # Every symbol include/gdn.h declares.
 EXPORTS = ("gdn_prefill_workspace_bytes", "gdn_prefill", "gdn_prefill_noalloc",
            "gdn_prefill_varlen_workspace_bytes", "gdn_prefill_varlen",
-           "gdn_decode_step", "gdn_decode_multi", "gdn_conv1d_decode", "gdn_last_error",
+           "gdn_decode_step", "gdn_decode_multi", "gdn_conv1d_decode",
+           "gdn_unit_lower_inverse", "gdn_last_error",
            "gdn_get_device_status", "gdn_launch_count")
 
 _lock = threading.Lock()
@@ -70,6 +72,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gdn_decode_multi.restype = i
         lib.gdn_conv1d_decode.argtypes = [vp] * 7 + [i] * 6 + [vp]
         lib.gdn_conv1d_decode.restype = i
+        lib.gdn_unit_lower_inverse.argtypes = [vp, vp, i, i, i, vp]
+        lib.gdn_unit_lower_inverse.restype = i
         lib.gdn_last_error.argtypes = []
         lib.gdn_last_error.restype = ctypes.c_char_p
         lib.gdn_get_device_status.argtypes = [vp]
@@ -317,3 +321,19 @@ def gdn_prefill_varlen(q, k, v, g_log, beta, scale, cu_seqlens, state=None, out=
         _ptr(cu_seqlens), N, Hk, Hv, T, Dk, Dv, _ptr(state), int(state_is_input), _ptr(out),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
     return out, state
+
+
+def gdn_unit_lower_inverse(A, algorithm=GDN_TRIL_SUBSTITUTION, out=None, stream=None):
+    """(I + A)^-1 for a batch of strictly lower-triangular 64x64 fp32 matrices A [n,64,64]
+    (zero on and above the diagonal). ``algorithm``: GDN_TRIL_SUBSTITUTION or
+    GDN_TRIL_NEUMANN. Returns T [n,64,64] fp32."""
+    n, C, C2 = A.shape
+    if C != C2:
+        raise ValueError("A must be [n, C, C]")
+    _need(A, "A", torch.float32, (n, C, C), A.device)
+    if out is None:
+        out = torch.empty_like(A)
+    _need(out, "out", torch.float32, (n, C, C), A.device)
+    _check(load_library().gdn_unit_lower_inverse(_ptr(A), _ptr(out), n, C, int(algorithm),
+                                                 _stream(stream)))
+    return out

@@ -167,6 +167,15 @@ def test_varlen_rejects_bad_arguments(lib, N, ws, msg):
     assert msg in lib.gdn_last_error().decode()
 
 
+@pytest.mark.parametrize("n,C,alg,code,msg", [(-1, 64, 0, gdn.GDN_EINVAL, "n"),
+                                               (4, 32, 0, gdn.GDN_EUNSUPPORTED, "C = 64"),
+                                               (4, 64, 2, gdn.GDN_EINVAL, "algorithm")])
+def test_unit_lower_inverse_rejects_bad_arguments(lib, n, C, alg, code, msg):
+    vp = ctypes.c_void_p
+    assert lib.gdn_unit_lower_inverse(vp(16), vp(1 << 40), n, C, alg, None) == code
+    assert msg in lib.gdn_last_error().decode()
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError, match="missing"):
         gdn.load_library(str(tmp_path / "libgdn.so"))
