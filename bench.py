@@ -35,9 +35,11 @@ sys.path.insert(0, ROOT)
 METRIC = "GDN prefill tokens/s & % roofline; decode-step state HBM GB/s vs peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM traffic per launch of the dominant kernel from one ncu capture, keyed by the
-# sha256 of the kernel's source file at capture time (reported only while it matches).
-NCU_TRAFFIC = {"prefill_tc.cu@f12343c2ba942974": 175342592}
+# DRAM traffic of one layer prefill call (the four launches of prefill_tc.cu's two
+# overlapped segments, dram__bytes_read.sum + dram__bytes_write.sum, one ncu capture),
+# keyed by the sha256 of the kernel source at capture time (reported only while it
+# matches).
+NCU_TRAFFIC = {"prefill_tc.cu@c3f71d89b21a276a": 591617280}
 
 
 def parse_args():
