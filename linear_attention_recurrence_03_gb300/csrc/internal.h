@@ -85,12 +85,14 @@ constexpr uint32_t kStatusBadSeqlens = 16u;
 // B * Hv * nseg units; the state carries over between consecutive calls.
 cudaError_t launch_prefill_tc(const PrefillArgs& a, int c0, int nseg, cudaStream_t stream,
                               int* launched);
-// The whole sequence with a workspace of B * Hv * ceil(S / 64) units, in segments of
-// prefill_tc_segment_chunks(...) chunks when the carry leaves SMs free: the prep of
+// The whole sequence with a workspace of B * Hv * ceil(S / 64) units, in
+// prefill_tc_segments(...) segments when the carry leaves SMs free (the first one of
+// prefill_tc_segment_chunks(...) chunks, the others sharing the rest): the prep of
 // segment j + 1 (helper stream, low priority) then runs beside the carry of segment j
 // (helper stream, high priority), forked from and joined back to `stream` by events.
 cudaError_t launch_prefill_tc_overlapped(const PrefillArgs& a, cudaStream_t stream,
                                          int* launched);
+int prefill_tc_segments(int B, int Hv, int nch, int sms);
 int prefill_tc_segment_chunks(int B, int Hv, int nch, int sms);
 
 // Depthwise causal conv1d decode token + silu + window shift, split into q | k | v with

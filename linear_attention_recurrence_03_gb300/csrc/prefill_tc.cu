@@ -98,6 +98,14 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 #endif
 constexpr int kOverlapSegments = GDN_OVERLAP_SEGMENTS;
 constexpr int kMinSegmentChunks = 8;
+// Share (per mille) of the chunks in the first segment: its prep is exposed, the others
+// run beside the carry of the segment before. The prep of the rest on the SMs the carry
+// leaves (88 of 152 for 64 carry CTAs) takes about as long as the carry of the first
+// when the first holds ~45%.
+#ifndef GDN_FIRST_SEGMENT_PERMILLE
+#define GDN_FIRST_SEGMENT_PERMILLE 450
+#endif
+constexpr int kFirstSegmentPermille = GDN_FIRST_SEGMENT_PERMILLE;
 
 // ---- workspace: per (batch, value head, chunk) unit, eight bf16 tiles of 64 rows x 64
 // columns in the 128-byte swizzled layout, T_U | P | W[:, 0:64] | W[:, 64:128] |
@@ -1394,14 +1402,20 @@ cudaError_t prepare(SegmentLaunch& L, const PrefillArgs& a) {
 
 }  // namespace
 
-int prefill_tc_segment_chunks(int B, int Hv, int nch, int sms) {
+int prefill_tc_segments(int B, int Hv, int nch, int sms) {
     // The carry of a segment occupies 2 B Hv SMs (one CTA each) for the whole segment;
     // the prep of the next segment runs meanwhile on the SMs left over. Without enough
     // of those, or with too few chunks, one segment.
     const int carry_sms = 2 * B * Hv;
-    if (carry_sms > sms || sms - carry_sms < sms / 4 || nch < 2 * kMinSegmentChunks) return nch;
-    const int g = std::min(kOverlapSegments, nch / kMinSegmentChunks);
-    return (nch + g - 1) / g;
+    if (carry_sms > sms || sms - carry_sms < sms / 4 || nch < 2 * kMinSegmentChunks) return 1;
+    return std::max(1, std::min(kOverlapSegments, nch / kMinSegmentChunks));
+}
+
+int prefill_tc_segment_chunks(int B, int Hv, int nch, int sms) {
+    const int g = prefill_tc_segments(B, Hv, nch, sms);
+    if (g == 1) return nch;
+    const int first = (int)(((long)nch * kFirstSegmentPermille + 500) / 1000);
+    return std::max(kMinSegmentChunks, std::min(first, nch - kMinSegmentChunks * (g - 1)));
 }
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a, int c0, int nseg, cudaStream_t stream,
@@ -1460,6 +1474,9 @@ cudaError_t launch_prefill_tc_overlapped(const PrefillArgs& a, cudaStream_t stre
     int dev = 0;
     cudaGetDevice(&dev);
     const int seg = prefill_tc_segment_chunks(a.B, a.Hv, nch, L.sms);
+    const int g = prefill_tc_segments(a.B, a.Hv, nch, L.sms);
+    // the first segment is `seg` chunks, the others share the rest evenly
+    const int rest = g > 1 ? (nch - seg + g - 2) / (g - 1) : 0;
     Overlap* o = overlap_for(dev);
     uint8_t* ws = static_cast<uint8_t*>(a.workspace);
     if (seg >= nch || o == nullptr) {
@@ -1481,8 +1498,8 @@ cudaError_t launch_prefill_tc_overlapped(const PrefillArgs& a, cudaStream_t stre
     // prep of segment j+1 overlaps the carry of segment j; each carry waits for its prep
     // (a wait takes the event's latest record at the time it is enqueued)
     cudaError_t le = cudaSuccess;
-    for (int c0 = 0; c0 < nch && le == cudaSuccess; c0 += seg) {
-        const int n = std::min(seg, nch - c0);
+    for (int c0 = 0, n = 0; c0 < nch && le == cudaSuccess; c0 += n) {
+        n = c0 == 0 ? seg : std::min(rest, nch - c0);
         uint8_t* wsj = ws + (size_t)a.B * (size_t)a.Hv * (size_t)c0 * WS_UNIT;
         le = L.prep(c0, n, wsj, o->prep);
         if (le != cudaSuccess) break;
