@@ -136,11 +136,12 @@ def gdn_prefill_workspace_bytes(B, Hk, Hv, S, Dk, Dv, dtype) -> int:
 
 
 def gdn_prefill(q, k, v, g_log, beta, scale, state=None, out=None, workspace=None,
-                stream=None):
+                stream=None, state_is_input=None):
     """Chunked prefill. q,k [B,Hk,S,Dk], v [B,Hv,S,Dv] (fp32 or bf16, one dtype);
     g_log, beta [B,Hv,S] fp32. ``state`` [B,Hv,Dk,Dv] fp32, if given, is the initial
-    state and is updated in place; if None a zero initial state is used and a new
-    tensor returned. Returns (out [B,Hv,S,Dv], state)."""
+    state and is updated in place (with ``state_is_input=False`` it is only written: zero
+    initial state, no load); if None a zero initial state is used and a new tensor
+    returned. Returns (out [B,Hv,S,Dv], state)."""
     B, Hk, S, Dk = q.shape
     Hv, Dv = v.shape[1], v.shape[3]
     dev, dt = q.device, q.dtype
@@ -151,8 +152,11 @@ def gdn_prefill(q, k, v, g_log, beta, scale, state=None, out=None, workspace=Non
     _need(v, "v", dt, (B, Hv, S, Dv), dev)
     _need(g_log, "g_log", torch.float32, (B, Hv, S), dev)
     _need(beta, "beta", torch.float32, (B, Hv, S), dev)
-    state_is_input = state is not None
+    if state_is_input is None:
+        state_is_input = state is not None
     if state is None:
+        if state_is_input:
+            raise ValueError("state_is_input needs a state")
         state = torch.empty((B, Hv, Dk, Dv), dtype=torch.float32, device=dev)
     _need(state, "state", torch.float32, (B, Hv, Dk, Dv), dev)
     if out is None:
