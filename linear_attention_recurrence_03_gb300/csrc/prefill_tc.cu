@@ -664,31 +664,29 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
             tc_fence_after();
             if (P == 0) TRACE_PREP(23);
 
-            // ---- Q~ = diag(Gamma) Q and K~ = diag(exp(gamma_last - gamma)) K straight to
-            // the workspace (the Q slots are reused next); 16-byte chunk j of the two
-            // blocks, same swizzled position
-            {
-                uint8_t* wsu = a.ws + ws_offset(b, h, cl, a.Hv, nch);
+            // ---- Q~ = diag(Gamma) Q and (later, beside the diagonal solve) K~ =
+            // diag(exp(gamma_last - gamma)) K straight to the workspace; 16-byte chunk j of
+            // the two 64-column blocks, same swizzled position
+            uint8_t* wsu = a.ws + ws_offset(b, h, cl, a.Hv, nch);
+            auto export_rows = [&](int j, bool isq) {
                 const CarryScalars& cs = *reinterpret_cast<const CarryScalars*>(sm + P_CS);
+                const int blk = j >> 9, off = (j & 511) * 16, row = (j & 511) >> 3;
+                const float f = isq ? sc.Gam[row] : cs.kdec[row];
+                const uint4 x = *reinterpret_cast<const uint4*>(
+                    sm + blk * PQ_STRIDE + (isq ? PQ_Q : PQ_K) + off);
+                const uint32_t in[4] = {x.x, x.y, x.z, x.w};
+                uint32_t o[4];
 #pragma unroll
-                for (int it = 0; it < 8; ++it) {
-                    const int j = P + 256 * (it & 3), blk = j >> 9, off = (j & 511) * 16;
-                    const int row = (j & 511) >> 3;
-                    const bool isq = it < 4;
-                    const float f = isq ? sc.Gam[row] : cs.kdec[row];
-                    const uint4 x = *reinterpret_cast<const uint4*>(
-                        sm + blk * PQ_STRIDE + (isq ? PQ_Q : PQ_K) + off);
-                    const uint32_t in[4] = {x.x, x.y, x.z, x.w};
-                    uint32_t o[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&in[e]));
-                        o[e] = pack_bf16(v.x * f, v.y * f);
-                    }
-                    *reinterpret_cast<uint4*>(wsu + (isq ? WS_QT : WS_KT) + blk * 8192 + off) =
-                        make_uint4(o[0], o[1], o[2], o[3]);
+                for (int e = 0; e < 4; ++e) {
+                    const float2 v =
+                        __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&in[e]));
+                    o[e] = pack_bf16(v.x * f, v.y * f);
                 }
-            }
+                *reinterpret_cast<uint4*>(wsu + (isq ? WS_QT : WS_KT) + blk * 8192 + off) =
+                    make_uint4(o[0], o[1], o[2], o[3]);
+            };
+#pragma unroll
+            for (int it = 0; it < 4; ++it) export_rows(P + 256 * it, true);
             bar_sync(2, 256);  // every Q chunk is read before A overwrites the Q slots
 
             // ---- P (bf16 tile) and A (fp32 blocks) from the Gram matrices: thread (wg, L)
@@ -701,24 +699,27 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
                 const int lim = isP ? rl : rl - 1;
                 float gv[32];
                 tmem_ld8x4(tmem + lane_off + PT_G + 8 * wg, gv);
+                // The lanes of a warp cover two 16-row blocks, so the three cases (block left
+                // of, on, right of the diagonal) are selected per element instead of
+                // branched on. Left of the diagonal: one factor per block times the
+                // column's table entry; on it: the masked exp of a non-positive argument.
+                float fb[4], dg[8];
+#pragma unroll
+                for (int bj = 0; bj < 4; ++bj)
+                    fb[bj] = (bj < br) ? __expf(gr - sc.endgam[bj]) * scl : 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int jj = 8 * wg + e;
+                    dg[e] = __expf(fminf(gr - sc.gam[16 * br + jj], 0.f)) * ((jj <= lim) ? scl : 0.f);
+                }
 #pragma unroll
                 for (int bj = 0; bj < 4; ++bj) {
                     float* v = gv + 8 * bj;
-                    if (bj < br) {
-                        const float f = __expf(gr - sc.endgam[bj]) * scl;
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) v[e] *= f * sc.ctab[16 * bj + 8 * wg + e];
-                    } else if (bj == br) {
-                        // branch-free: exp of a non-positive argument, then the mask
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const int jj = 8 * wg + e;
-                            const float ex = __expf(fminf(gr - sc.gam[16 * bj + jj], 0.f));
-                            v[e] *= ex * ((jj <= lim) ? scl : 0.f);
-                        }
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) v[e] = 0.f;
+                    for (int e = 0; e < 8; ++e) {
+                        const float f = (bj < br) ? fb[bj] * sc.ctab[16 * bj + 8 * wg + e]
+                                                  : ((bj == br) ? dg[e] : 0.f);
+                        v[e] *= f;
                     }
                     if (isP) {
                         st_shared_v4(sw128_chunk(sb + P_P, r, 2 * bj + wg), pack_bf16(v[0], v[1]),
@@ -736,32 +737,38 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
             if (P == 0) TRACE_PREP(24);
 
             // ---- T = (I + A)^-1 in 16x16 blocks
-            // diagonal blocks: forward substitution, four threads per column (thread rq
-            // holds rows 4 rq .. 4 rq + 3), x_m broadcast from its owner at step m. A's
-            // diagonal blocks hold zeros on and above the diagonal, so every row may
-            // accumulate at every step.
-            {
-                const int i = P >> 6, cc = (P >> 2) & 15, rq = P & 3;
-                const float* Ad = Ablk(i, i) + 4 * rq * BS;
-                float acc[4] = {0.f, 0.f, 0.f, 0.f}, xr[4] = {0.f, 0.f, 0.f, 0.f};
+            // diagonal blocks (prep warps 0 and 1): forward substitution, one thread per
+            // column of the block's inverse, its 16 entries in registers. The rows go in
+            // lockstep, so the threads of a block read the same A entry (a broadcast);
+            // the column's zeros above its diagonal keep the full sums exact. Meanwhile
+            // warps 2..7 write K~ to the workspace.
+            if (P < 64) {
+                const int i = P >> 4, cc = P & 15;
+                const float* Ad = Ablk(i, i);
+                float x[16];
 #pragma unroll
-                for (int m = 0; m < 16; ++m) {
-                    const float sh =
-                        __shfl_sync(0xffffffffu, -acc[m & 3], (lane & ~3) | (m >> 2));
-                    const float xm = (m < cc) ? 0.f : ((m == cc) ? 1.f : sh);
-                    if ((m >> 2) == rq) xr[m & 3] = xm;
+                for (int m = 0; m < 16; ++m) x[m] = (m == cc) ? 1.f : 0.f;
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) acc[e] = fmaf(Ad[e * BS + m], xm, acc[e]);
+                for (int m = 1; m < 16; ++m) {
+                    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                    for (int n = 0; n < m; n += 2) {
+                        s0 = fmaf(Ad[m * BS + n], x[n], s0);
+                        if (n + 1 < m) s1 = fmaf(Ad[m * BS + n + 1], x[n + 1], s1);
+                    }
+                    if (m > cc) x[m] = -(s0 + s1);
                 }
-                float* Td = Tb + bidx(i, i) * 16 * BS + 4 * rq * BS;
+                float* Td = Tb + bidx(i, i) * 16 * BS;
                 const int J = 16 * i + cc;
                 const float bj = sc.beta[J], wj = bj * sc.Gam[J];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    Td[e * BS + cc] = xr[e];
-                    st_shared_b16(sw128_elem(tu, 16 * i + 4 * rq + e, J), xr[e] * bj);
-                    st_shared_b16(sw128_elem(tw, 16 * i + 4 * rq + e, J), xr[e] * wj);
+                for (int m = 0; m < 16; ++m) {
+                    Td[m * BS + cc] = x[m];
+                    st_shared_b16(sw128_elem(tu, 16 * i + m, J), x[m] * bj);
+                    st_shared_b16(sw128_elem(tw, 16 * i + m, J), x[m] * wj);
                 }
+            } else {
+                for (int j = P - 64; j < 1024; j += 192) export_rows(j, false);
             }
             bar_sync(2, 256);
             if (P == 0) TRACE_PREP(25);
