@@ -658,8 +658,13 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
         const uint32_t lane_off = (uint32_t)(32 * q) << 16;
         const uint32_t tu = sb + P_TU, tw = sb + P_TW;
 
-        bool ok = wait_or_abort(&bar[PB_FULL], 0, abort_flag, ST_PREP) &&
-                  wait_or_abort(&bar[PB_GRAM], 0, abort_flag, ST_PREP);
+        // One warp polls the mbarriers; the others wait at the named barrier, which costs
+        // no issue slots (the prep is bound by instruction issue, with three CTAs per SM).
+        // The barrier then carries the phase's visibility to every prep thread.
+        bool ok = true;
+        if (pw == 0)
+            ok = wait_or_abort(&bar[PB_FULL], 0, abort_flag, ST_PREP) &&
+                 wait_or_abort(&bar[PB_GRAM], 0, abort_flag, ST_PREP);
         if (!bar_any(2, 256, !ok || *abort_flag)) {
             tc_fence_after();
             if (P == 0) TRACE_PREP(23);
@@ -818,7 +823,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
             }
             // ---- W = T_W K from TMEM (rows 0..63: lanes 0..63) into the W staging tiles;
             // two warps per lane quadrant, one 64-column block each
-            ok = wait_or_abort(&bar[PB_WDONE], 0, abort_flag, ST_PREP);
+            if (pw == 0) ok = wait_or_abort(&bar[PB_WDONE], 0, abort_flag, ST_PREP);
             if (!bar_any(2, 256, !ok || *abort_flag)) {
                 tc_fence_after();
                 if (q < 2) {
