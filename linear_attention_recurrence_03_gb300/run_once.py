@@ -29,11 +29,16 @@ def main(argv=None) -> int:
     p.add_argument("--iters", type=int, default=2)
     p.add_argument("--heads", type=int, default=0,
                    help="prefill: keep only this many value heads (0 = all)")
+    p.add_argument("--batch", type=int, default=0,
+                   help="decode: this many batch rows of 32 value heads (0 = all 256)")
     a = p.parse_args(argv)
     lib_build.build()
     dev = torch.device("cuda:0")
     if a.workload == "decode":
-        x = syn.decode_inputs(syn.DECODE_BH8192)
+        wd = syn.DECODE_BH8192
+        if a.batch:
+            wd = syn.DecodeWorkload(wd.name, a.batch, wd.num_k_heads, wd.num_v_heads, wd.K, wd.V)
+        x = syn.decode_inputs(wd)
         names = ("q", "k", "v", "b", "a", "A_log", "dt_bias", "z", "norm_weight", "state")
         d = [x[n].to(dev) for n in names]
         for _ in range(a.iters):
