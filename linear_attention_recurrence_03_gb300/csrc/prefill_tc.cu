@@ -22,16 +22,24 @@
 // masks, the (I+A)^-1 solve, T_U, P and W) is independent across chunks, so it runs
 // first as a fully parallel grid ("prep", one CTA per (batch, value head, chunk)) that
 // writes three bf16 operand tiles per chunk to a workspace, already in the 128-byte
-// swizzled layout the tensor cores read. The sequential part ("carry", one CTA per
-// (batch, value head, 64-column slice of the state); the slices never communicate)
-// then streams q, k, v and those tiles through a two-stage ring and keeps only the
-// S0-dependent chain per chunk:
+// swizzled layout the tensor cores read. The sequential part ("carry") then streams v
+// and those tiles through a two-stage ring and keeps only the S0-dependent chain per
+// chunk, in one of two forms:
+//   carry_tc_kernel<64>: one CTA per (batch, value head, 64-column slice of the state;
+//   the slices never communicate), state rows in TMEM lanes, used while two CTAs per
+//   head fit the GPU:
+//          [T_U;-] V              -> U~                   (M128 N64  K64)
+//          [W;Q~] S0              -> W S0, Q~ S0          (M128 N64  K128)
+//          [K~_1;P] U             -> P U                  (M128 N64  K64)
+//          K~^T U                 -> state increment      (M128 N64  K64)
+//   carry_t_kernel: one CTA per (batch, value head), the chain transposed (state columns
+//   in TMEM lanes) so that U^T and S0^T enter the MMAs from TMEM:
+//          V^T T_U^T              -> U~^T                 (M128 N64  K64)
+//          S0^T [W;Q~]^T          -> (W S0)^T, (Q~ S0)^T  (M128 N128 K128, A in TMEM)
+//          U^T K~                 -> dS^T                 (M128 N128 K64, A in TMEM)
+//          U^T P^T                -> (P U)^T              (M128 N64  K64, A in TMEM)
 //   prep   [Q;K] K^T              -> QK^T, KK^T           (M128 N64  K128)
 //          [T_W;P] K              -> W                    (M128 N128 K64)
-//   carry  [T_U;P] V              -> U~                   (M128 N64  K64)
-//          [W;Q] S0               -> W S0, Q S0           (M128 N64  K128)
-//          [T_U;P] U              -> P U                  (M128 N64  K64)
-//          K^T U'                 -> state increment      (M128 N64  K64)
 // Stacking two 64-row operands into one 128-row operand fills the M = 128 data path;
 // the half of a result that is not needed is ignored.
 //
@@ -76,7 +84,20 @@ __device__ unsigned long long g_trace[kTraceChunks][kTraceEvents];
         if (blockIdx.y == 0 && blockIdx.z == 0 && blockIdx.x < kTraceChunks) \
             g_trace[blockIdx.x][(ev)] = clock64();                            \
     } while (0)
+// a stamp taken into a register now (TCLK) and stored later (TPUT), away from MMA issue
+#define TCLK(var) const unsigned long long var = clock64()
+#define TPUT(c, ev, var)                                                                \
+    do {                                                                                \
+        if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (c) < kTraceChunks) \
+            g_trace[(c)][(ev)] = (var);                                                 \
+    } while (0)
 #else
+#define TCLK(var) \
+    do {          \
+    } while (0)
+#define TPUT(c, ev, var) \
+    do {                 \
+    } while (0)
 #define TRACE(c, ev) \
     do {             \
     } while (0)
@@ -106,6 +127,12 @@ constexpr int kMinSegmentChunks = 8;
 #define GDN_FIRST_SEGMENT_PERMILLE 450
 #endif
 constexpr int kFirstSegmentPermille = GDN_FIRST_SEGMENT_PERMILLE;
+// Carry form while two CTAs per head fit the GPU: 1 = two 64-column state slices per head
+// (carry_tc_kernel<64>), 0 = one transposed CTA per head (carry_t_kernel).
+#ifndef GDN_CARRY_SPLIT
+#define GDN_CARRY_SPLIT 1
+#endif
+constexpr bool kCarrySplit = GDN_CARRY_SPLIT != 0;
 
 // ---- workspace: per (batch, value head, chunk) unit, eight bf16 tiles of 64 rows x 64
 // columns in the 128-byte swizzled layout, T_U | P | W[:, 0:64] | W[:, 64:128] |
@@ -250,6 +277,11 @@ __device__ __forceinline__ void bar_sync(uint32_t id, uint32_t n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
+// Arrives at a named barrier without waiting for it to complete.
+__device__ __forceinline__ void bar_arrive(uint32_t id, uint32_t n) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 // Named barrier that also ORs a predicate over the participating threads, so that a
 // group decides to stop as one (every thread sees the same result).
 __device__ __forceinline__ bool bar_any(uint32_t id, uint32_t n, bool v) {
@@ -286,6 +318,20 @@ __device__ __forceinline__ void st_shared_b16(uint32_t addr, float x) {
     asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr),
                  "h"(*reinterpret_cast<const unsigned short*>(&h))
                  : "memory");
+}
+
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"((unsigned short)(v & 0xffffu))
+                 : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 r;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "r"(addr)
+                 : "memory");
+    return r;
 }
 
 // Byte address of element (r, col) (bf16) in a 128-byte-swizzled tile of 64-wide rows.
@@ -332,6 +378,23 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait_sleep(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > kWaitNs) {
+            record_failure(abort_flag, bit);
+            return false;
+        }
+    }
+}
+
+// As wait_or_abort, for the short hand-offs of the carry chain: polls with try_wait
+// without a suspend-time hint, which resumes the waiting thread sooner after the phase
+// completes.
+__device__ __forceinline__ bool wait_hot(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                         uint32_t bit) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
         if (globaltimer_ns() - t0 > kWaitNs) {
             record_failure(abort_flag, bit);
@@ -872,6 +935,67 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
 // registers, form U (rows 0-63) while writing the previous chunk's output (rows 64-127),
 // and update the state. MMA order per chunk c: [W; Q~] S0, U~ of chunk c+1 if it has
 // landed, then K^T U', U~ of chunk c+1 if not issued yet, P U.
+// The producer of a carry CTA (one thread): streams chunk c of the head's workspace units
+// (from `wsh`) and its V slice (columns n0 .. n0 + NS - 1, token rows tbase + 64 c, tensor
+// z = zv) through the two-stage ring, in the early (W, Q~, V, T_U) and late (K~, P,
+// scalars) copy groups.
+template <int NS>
+__device__ __forceinline__ void carry_produce(uint8_t* sm, uint64_t* bar, CarryScalars* scal,
+                                              const CUtensorMap* mvp, const uint8_t* wsh,
+                                              int nch, int n0, int tbase, int zv,
+                                              volatile int* abort_flag) {
+    using Cfg = CarryCfg<NS>;
+    const CUtensorMap& mv = *mvp;
+    int issued = 0;
+    for (int c = 0; c < nch; ++c) {
+        const int s = c & 1;
+        uint8_t* st = sm + s * Cfg::STAGE;
+        const uint8_t* wsc = wsh + (size_t)c * WS_UNIT;
+        // early group of chunk c: W, Q~, V, T_U
+        if (c >= 2 && !wait_or_abort(&bar[B_EMPTYE0 + s], ((c >> 1) + 1) & 1, abort_flag,
+                                     ST_PRODUCER))
+            break;
+        if (*abort_flag) break;
+        TRACE(c, 0);
+        uint64_t* fe = &bar[B_FULLE0 + s];
+        mbar_arrive_expect_tx(fe, 4 * 8192 + Cfg::NB * 8192 + 8192);
+        for (int blk = 0; blk < 2; ++blk) {
+            uint8_t* sb = st + blk * BLK_STRIDE;
+            bulk_g2s(sb + OFF_W, wsc + WS_W + blk * 8192, 8192, fe);
+            bulk_g2s(sb + OFF_Q, wsc + WS_QT + blk * 8192, 8192, fe);
+        }
+        for (int blk = 0; blk < Cfg::NB; ++blk)
+            tma_load_3d(st + OFF_V + blk * 8192, &mv, fe, n0 + blk * 64, tbase + c * C,
+                        zv);
+        bulk_g2s(st + Cfg::OFF_TU, wsc + WS_TU, 8192, fe);
+        // late group of chunk c: K~, P, scalars
+        if (c >= 2 && !wait_or_abort(&bar[B_EMPTYL0 + s], ((c >> 1) + 1) & 1, abort_flag,
+                                     ST_PRODUCER))
+            break;
+        uint64_t* fl = &bar[B_FULLL0 + s];
+        mbar_arrive_expect_tx(fl, 3 * 8192 + (uint32_t)sizeof(CarryScalars));
+        for (int blk = 0; blk < 2; ++blk)
+            bulk_g2s(st + blk * BLK_STRIDE + OFF_K, wsc + WS_KT + blk * 8192, 8192, fl);
+        bulk_g2s(st + OFF_P, wsc + WS_P, 8192, fl);
+        bulk_g2s(&scal[s], wsc + WS_CS, sizeof(CarryScalars), fl);
+        issued = c + 1;
+        // chunk c + 2 goes to L2 now
+        if (c + 2 < nch) {
+            for (int blk = 0; blk < Cfg::NB; ++blk)
+                tma_prefetch_l2_3d(&mv, n0 + blk * 64, tbase + (c + 2) * C, zv);
+            bulk_prefetch_l2(wsc + 2 * WS_UNIT, WS_UNIT);
+        }
+    }
+    if (*abort_flag) {
+        // let the copies already issued land before the CTA exits (a group whose
+        // copies were not issued completes no phase: its wait just runs out)
+        for (int c = (issued > 2 ? issued - 2 : 0); c < issued; ++c) {
+            mbar_wait_bounded(&bar[B_FULLE0 + (c & 1)], (c >> 1) & 1, kWaitNs);
+            mbar_wait_bounded(&bar[B_FULLL0 + (c & 1)], (c >> 1) & 1, kWaitNs);
+        }
+    }
+}
+
 template <int NS>
 __global__ void __launch_bounds__(CARRY_THREADS, 1)
     carry_tc_kernel(const __grid_constant__ CUtensorMap mv, TcArgs a) {
@@ -927,58 +1051,9 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
 
     if (warp == 0) {
         // ------------------------------------------------- loads (one thread)
-        if (lane == 0) {
-            const int zv = wb * a.Hv + h;
-            const uint8_t* wsh = a.ws + ws_offset(wb, h, u0, a.Hv, a.nseg);
-            int issued = 0;
-            for (int c = 0; c < nch; ++c) {
-                const int s = c & 1;
-                uint8_t* st = sm + s * Cfg::STAGE;
-                const uint8_t* wsc = wsh + (size_t)c * WS_UNIT;
-                // early group of chunk c: W, Q~, V, T_U
-                if (c >= 2 && !wait_or_abort(&bar[B_EMPTYE0 + s], ((c >> 1) + 1) & 1, abort_flag,
-                                             ST_PRODUCER))
-                    break;
-                if (*abort_flag) break;
-                TRACE(c, 0);
-                uint64_t* fe = &bar[B_FULLE0 + s];
-                mbar_arrive_expect_tx(fe, 4 * 8192 + Cfg::NB * 8192 + 8192);
-                for (int blk = 0; blk < 2; ++blk) {
-                    uint8_t* sb = st + blk * BLK_STRIDE;
-                    bulk_g2s(sb + OFF_W, wsc + WS_W + blk * 8192, 8192, fe);
-                    bulk_g2s(sb + OFF_Q, wsc + WS_QT + blk * 8192, 8192, fe);
-                }
-                for (int blk = 0; blk < Cfg::NB; ++blk)
-                    tma_load_3d(st + OFF_V + blk * 8192, &mv, fe, n0 + blk * 64, tbase + c * C,
-                                zv);
-                bulk_g2s(st + Cfg::OFF_TU, wsc + WS_TU, 8192, fe);
-                // late group of chunk c: K~, P, scalars
-                if (c >= 2 && !wait_or_abort(&bar[B_EMPTYL0 + s], ((c >> 1) + 1) & 1, abort_flag,
-                                             ST_PRODUCER))
-                    break;
-                uint64_t* fl = &bar[B_FULLL0 + s];
-                mbar_arrive_expect_tx(fl, 3 * 8192 + (uint32_t)sizeof(CarryScalars));
-                for (int blk = 0; blk < 2; ++blk)
-                    bulk_g2s(st + blk * BLK_STRIDE + OFF_K, wsc + WS_KT + blk * 8192, 8192, fl);
-                bulk_g2s(st + OFF_P, wsc + WS_P, 8192, fl);
-                bulk_g2s(&scal[s], wsc + WS_CS, sizeof(CarryScalars), fl);
-                issued = c + 1;
-                // chunk c + 2 goes to L2 now
-                if (c + 2 < nch) {
-                    for (int blk = 0; blk < Cfg::NB; ++blk)
-                        tma_prefetch_l2_3d(&mv, n0 + blk * 64, tbase + (c + 2) * C, zv);
-                    bulk_prefetch_l2(wsc + 2 * WS_UNIT, WS_UNIT);
-                }
-            }
-            if (*abort_flag) {
-                // let the copies already issued land before the CTA exits (a group whose
-                // copies were not issued completes no phase: its wait just runs out)
-                for (int c = (issued > 2 ? issued - 2 : 0); c < issued; ++c) {
-                    mbar_wait_bounded(&bar[B_FULLE0 + (c & 1)], (c >> 1) & 1, kWaitNs);
-                    mbar_wait_bounded(&bar[B_FULLL0 + (c & 1)], (c >> 1) & 1, kWaitNs);
-                }
-            }
-        }
+        if (lane == 0)
+            carry_produce<NS>(sm, bar, scal, &mv, a.ws + ws_offset(wb, h, u0, a.Hv, a.nseg), nch,
+                              n0, tbase, wb * a.Hv + h, abort_flag);
     } else if (warp == 2 || warp >= 4) {
         // ----------------------------------------- carry (warps 2, 4..11: 288 threads)
         const bool issuer = warp == 2;
@@ -1199,6 +1274,381 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
     }
 }
 
+// ---------------------------------------------------------------- transposed carry
+
+// carry_t_kernel: one CTA per (value head, sequence) over all 128 state columns, with the
+// chunk recurrence written transposed, so that every operand the SIMT warps produce in a
+// chunk stays in tensor memory and enters the next MMA as its A operand:
+//   U~^T = V^T T_U^T,   (W S0)^T = S0^T W^T,   U^T = U~^T - (W S0)^T,
+//   dS^T = U^T K~,      S1^T = Gamma_last S0^T + dS^T,   O^T = S0^T Q~^T + U^T P^T.
+// TMEM lanes are the value columns v of the state, so the U step and the state update
+// run on all four SM sub-partitions, and no hand-off goes through shared memory.
+// Warp 0: producer (carry_produce<128>, both 64-column V blocks); warp 1 (one thread):
+// every MMA, in the order that keeps the tensor pipe free for the chain: dS^T(c),
+// U~(c+1) (runs during the state update), [W; Q~] S0 of chunk c+1, U^T P^T of chunk c
+// (runs during the next U step); warps 2..9: SIMT, warp (q = warp % 4,
+// g = (warp - 2) / 4) owning lane v = 32 q + lane, fp32 state rows 64 g .. 64 g + 63
+// (registers) and tokens 32 g .. 32 g + 31 of U and of the output.
+struct CarryT {
+    static constexpr uint32_t STAGE = CarryCfg<128>::STAGE;
+    static constexpr uint32_t OUT = 2 * STAGE;  // two output tiles [64 t][64 v] x 2, bf16
+    static constexpr uint32_t SCAL = OUT + 2 * 16384;
+    static constexpr uint32_t BAR = SCAL + 2 * sizeof(CarryScalars);
+    static constexpr uint32_t MISC = BAR + 128;
+    static constexpr uint32_t SMEM = MISC + 64 + 1024;
+    // TMEM (32-bit columns): per chunk parity p, from 192 p: U~^T (64) | (W S0)^T (64) |
+    // O^T (64); once U is formed the state increment dS^T takes the first 128 columns.
+    // Then the bf16 operands S0^T (128 x 128: 64 columns) and, per parity, U^T (128 x 64:
+    // 32 columns; U^T P^T of a chunk still reads it during the next chunk's U step).
+    static constexpr uint32_t UB = 0, WSC = 64, OQ = 128, PSTRIDE = 192;
+    static constexpr uint32_t S0T = 384, UT = 448, TMCOLS = 512;  // U^T of parity p at UT + 32 p
+    static_assert(OUT % 1024 == 0 && SCAL % 16 == 0 && BAR % 8 == 0, "alignment");
+    static_assert(SMEM <= 232448, "shared memory budget");
+};
+constexpr int CARRY_T_THREADS = 320;
+// barriers 0..7 are the ring's (B_FULLE0 .. B_EMPTYL1)
+enum { T_ADONE = B_EMPTYL1 + 1, T_SDONE, T_ODONE0, T_ODONE1, T_DRAIN, T_COUNT };
+static_assert(T_COUNT * 8 <= 128, "barrier block");
+static_assert(CarryT::OQ == CarryT::WSC + 64 && OFF_Q == OFF_W + 8192,
+              "(W S0)^T and (Q~ S0)^T come from one 128-row operand into adjacent columns");
+
+// U~^T = V^T T_U^T over the 64 tokens (V read M-major, T_U as K-major B), into `d`
+__device__ __forceinline__ void issue_t_u(uint32_t tmem, uint32_t st, uint32_t d) {
+    constexpr uint32_t id = idesc_bf16(128, 64, true, false);
+    const uint64_t av = smem_desc_sw128(st + OFF_V, 8192, 1024);
+    const uint64_t bt = smem_desc_sw128(st + CarryCfg<128>::OFF_TU, 16, 1024);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) mma_bf16(tmem + d, dadd(av, k * 2048), dadd(bt, k * 32), id, k > 0);
+}
+
+// [(W S0)^T | (Q~ S0)^T] = S0^T [W; Q~]^T over Dk = 128 ([W_b; Q~_b] is one 128-row
+// K-major operand per 64-column block), S0^T the A operand in TMEM; 128 columns at `d`
+__device__ __forceinline__ void issue_t_s0(uint32_t tmem, uint32_t d, uint32_t st) {
+    constexpr uint32_t id = idesc_bf16(128, 128, false, false);
+    const uint64_t b0 = smem_desc_sw128(st + OFF_W, 16, 1024);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint32_t off = (uint32_t)(k >> 2) * BLK_STRIDE + (uint32_t)(k & 3) * 32u;
+        mma_bf16_ts(tmem + d, tmem + CarryT::S0T + 8u * (uint32_t)k, dadd(b0, off), id, k > 0);
+    }
+}
+
+// dS^T = U^T K~ over the tokens (U^T in TMEM at `ut`, K~ read N-major), 128 columns at `d`
+__device__ __forceinline__ void issue_t_ds(uint32_t tmem, uint32_t d, uint32_t ut, uint32_t st) {
+    constexpr uint32_t id = idesc_bf16(128, 128, false, true);
+    const uint64_t bk = smem_desc_sw128(st + OFF_K, BLK_STRIDE, 1024);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        mma_bf16_ts(tmem + d, tmem + ut + 8u * (uint32_t)k, dadd(bk, k * 2048), id, k > 0);
+}
+
+// O^T += U^T P^T (U^T at `ut`, P as K-major B), onto (Q~ S0)^T at `d`
+__device__ __forceinline__ void issue_t_o(uint32_t tmem, uint32_t d, uint32_t ut, uint32_t st) {
+    constexpr uint32_t id = idesc_bf16(128, 64, false, false);
+    const uint64_t bp = smem_desc_sw128(st + OFF_P, 16, 1024);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        mma_bf16_ts(tmem + d, tmem + ut + 8u * (uint32_t)k, dadd(bp, k * 32), id, 1);
+}
+
+__global__ void __launch_bounds__(CARRY_T_THREADS, 1)
+    carry_t_kernel(const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mo,
+                   TcArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sbase = smem_u32(sm);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + CarryT::BAR);
+    uint32_t* misc = reinterpret_cast<uint32_t*>(sm + CarryT::MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+    CarryScalars* scal = reinterpret_cast<CarryScalars*>(sm + CarryT::SCAL);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int h = blockIdx.y;
+    const int S = a.S;
+    // the sequence of this CTA, as in carry_tc_kernel
+    int wb, u0, nch, tbase, tend, sb;
+    if (a.cu == nullptr) {
+        wb = blockIdx.z, u0 = 0, nch = a.nseg, tbase = a.c0 * C, tend = S;
+        sb = blockIdx.z * a.Hv + h;
+    } else {
+        const int n = blockIdx.z;
+        wb = 0, u0 = a.cb[n], nch = a.cb[n + 1] - a.cb[n], tbase = a.cu[n], tend = a.cu[n + 1];
+        sb = n * a.Hv + h;
+    }
+    if (nch == 0) {
+        if (!a.state_is_input)
+            for (int i = tid; i < 128 * 128; i += CARRY_T_THREADS)
+                a.state[(size_t)sb * 128 * 128 + i] = 0.f;
+        return;
+    }
+    const int zo = wb * a.Hv + h;  // head row of v and out
+
+    if (tid == 0) {
+        for (int i = 0; i < T_COUNT; ++i) mbar_init(&bar[i], 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(misc, CarryT::TMCOLS);
+        tmem_relinquish();
+    }
+    if (tid == 32) {
+        prefetch_tensormap(&mv);
+        prefetch_tensormap(&mo);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+
+    if (warp == 0) {
+        if (lane == 0)
+            carry_produce<128>(sm, bar, scal, &mv, a.ws + ws_offset(wb, h, u0, a.Hv, a.nseg), nch,
+                               0, tbase, zo, abort_flag);
+    } else {
+        const bool issuer = warp == 1;
+        const bool leader = issuer && lane == 0;
+        const int q = warp & 3, g = (warp - 2) >> 2;
+        const int v = 32 * q + lane;
+        const uint32_t lo = (uint32_t)(32 * q) << 16;
+        float* gst = a.state + ((size_t)sb * 128 + (size_t)(64 * g)) * 128 + v;
+        __nv_bfloat16* gout = a.out + (size_t)zo * S * 128;
+
+        float Sr[64];
+        // the bf16 copy of this thread's state rows, as the A operand S0^T
+        auto put_state = [&]() {
+            uint32_t w[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) w[j] = pack_bf16(Sr[2 * j], Sr[2 * j + 1]);
+            tmem_st32u(tmem + lo + CarryT::S0T + 32u * (uint32_t)g, w);
+            tmem_wait_st();
+        };
+        // out = scale O of chunk cc, tokens 32 g .. 32 g + 31 of column v, into the bf16
+        // output tile of the chunk's parity
+        auto stage_out = [&](int cc) {
+            const uint32_t ob = sbase + CarryT::OUT + 16384u * (uint32_t)(cc & 1) +
+                                8192u * (uint32_t)(v >> 6);
+            float o[32];
+            tmem_ld32(tmem + lo + CarryT::PSTRIDE * (uint32_t)(cc & 1) + CarryT::OQ +
+                          32u * (uint32_t)g,
+                      o);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const uint32_t w = pack_bf16(a.scale * o[2 * j], a.scale * o[2 * j + 1]);
+                st_shared_u16(sw128_elem(ob, 32 * g + 2 * j, v & 63), w);
+                st_shared_u16(sw128_elem(ob, 32 * g + 2 * j + 1, v & 63), w >> 16);
+            }
+            fence_proxy_async_smem();
+        };
+        // after a SIMT barrier: the tile goes out by TMA (one thread), or, for a chunk
+        // that ends past the sequence, row by row below tend (all SIMT threads)
+        auto flush_out = [&](int cc) {
+            const int t0 = tbase + cc * C;
+            const uint32_t ob = sbase + CarryT::OUT + 16384u * (uint32_t)(cc & 1);
+            if (t0 + C <= tend) {
+                if (tid == 64) {
+                    tma_store_3d(&mo, ob, 0, t0, zo);
+                    tma_store_3d(&mo, ob + 8192u, 64, t0, zo);
+                    bulk_commit();
+                }
+            } else {
+                for (int i = tid - 64; i < 1024; i += 256) {
+                    const int r = i >> 4, j = i & 15;
+                    if (t0 + r < tend) {
+                        const uint4 x = ld_shared_v4(sw128_chunk(ob + 8192u * (uint32_t)(j >> 3), r, j & 7));
+                        *reinterpret_cast<uint4*>(gout + (size_t)(t0 + r) * 128 + 8 * j) = x;
+                    }
+                }
+            }
+        };
+        // U~ of chunk cc into its parity's columns; ADONE of chunk cc covers it
+        auto issue_next_u = [&](int cc) -> bool {
+            const int sc = cc & 1;
+            if (!wait_or_abort(&bar[B_FULLE0 + sc], (cc >> 1) & 1, abort_flag, ST_MMA)) return false;
+            tc_fence_after();
+            issue_t_u(tmem, sbase + (uint32_t)sc * CarryT::STAGE,
+                      CarryT::PSTRIDE * (uint32_t)sc + CarryT::UB);
+            return true;
+        };
+        // [(W S0)^T | (Q~ S0)^T] of chunk cc from the state just published; its columns held
+        // dS^T and O^T of chunk cc-2, both read by now. The early group of chunk cc (also
+        // read by U~(cc), issued before) is then free.
+        auto issue_next_s0 = [&](int cc) {
+            const int sc = cc & 1;
+            TCLK(t12);
+            tc_fence_after();
+            issue_t_s0(tmem, CarryT::PSTRIDE * (uint32_t)sc + CarryT::WSC,
+                       sbase + (uint32_t)sc * CarryT::STAGE);
+            tc_commit(&bar[T_ADONE]);
+            tc_commit(&bar[B_EMPTYE0 + sc]);
+            TCLK(t3);
+            TPUT(cc, 12, t12);
+            TPUT(cc, 3, t3);
+        };
+
+        // The chain hand-offs are named barriers of the SIMT warps and the issuer warp
+        // (288 threads): barrier 3 when U^T is in TMEM (SIMT warps arrive, the issuer
+        // waits), barrier 4 when the state is (a full barrier that also votes on stopping,
+        // so the group leaves the loop as one). Every participant reaches both barriers in
+        // every chunk: a failed wait only skips work.
+        if (!issuer) {
+            if (a.state_is_input) {
+#pragma unroll
+                for (int i = 0; i < 64; ++i) Sr[i] = gst[(size_t)i * 128];
+            } else {
+#pragma unroll
+                for (int i = 0; i < 64; ++i) Sr[i] = 0.f;
+            }
+            put_state();
+            tc_fence_before();
+        }
+        bool ok = true;
+        int done = 0;
+        if (leader) ok = issue_next_u(0);
+        __syncwarp();
+        bool stop = bar_any(4, 288, !ok || *abort_flag);
+        if (leader && !stop) issue_next_s0(0);
+        for (int c = 0; !stop && c < nch; ++c) {
+            const int s = c & 1;
+            const uint32_t pb = CarryT::PSTRIDE * (uint32_t)s;
+            const uint32_t ut = CarryT::UT + 32u * (uint32_t)s;
+            const uint32_t st = sbase + (uint32_t)s * CarryT::STAGE;
+            if (!issuer) {
+                // Gamma_last is read before barrier 3: the late group is reloaded only after
+                // U^T P^T of the chunk, issued after barrier 4
+                ok = ok && wait_or_abort(&bar[B_FULLL0 + s], (c >> 1) & 1, abort_flag, ST_CARRY);
+                const float Gl = ok ? scal[s].Gl : 0.f;
+                // U^T = U~^T - (W S0)^T for tokens 32 g .. 32 g + 31; ADONE(c) also covers
+                // U~(c) and U^T P^T of chunk c-2, the last reader of this U^T buffer
+                ok = ok && wait_hot(&bar[T_ADONE], c & 1, abort_flag, ST_CARRY);
+                if (tid == 64) TRACE(c, 13);
+                if (ok) {
+                    tc_fence_after();
+                    float ws[32], uv[32];
+                    tmem_ld32x2(tmem + lo + pb + CarryT::WSC + 32u * (uint32_t)g,
+                                tmem + lo + pb + CarryT::UB + 32u * (uint32_t)g, ws, uv);
+                    uint32_t u[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        u[j] = pack_bf16(uv[2 * j] - ws[2 * j], uv[2 * j + 1] - ws[2 * j + 1]);
+                    tmem_st16u(tmem + lo + ut + 16u * (uint32_t)g, u);
+                    tmem_wait_st();
+                }
+                if (lane == 0) TRACE(c, 20 + (warp - 2));
+                tc_fence_before();
+                __syncwarp();
+                bar_arrive(3, 288);
+                // the output of chunk c-1 (its U^T P^T ran during this U step)
+                if (c > 0) {
+                    ok = ok && wait_hot(&bar[T_ODONE0 + (s ^ 1)], ((c - 1) >> 1) & 1, abort_flag,
+                                        ST_CARRY);
+                    if (ok) {
+                        tc_fence_after();
+                        stage_out(c - 1);
+                    }
+                }
+                if (tid == 64) TRACE(c, 17);
+                // S1^T = Gamma_last S0^T + dS^T for rows 64 g .. 64 g + 63 of column v
+                ok = ok && wait_hot(&bar[T_SDONE], c & 1, abort_flag, ST_CARRY);
+                if (tid == 64) TRACE(c, 15);
+                if (ok) {
+                    tc_fence_after();
+                    float d0[32], d1[32];
+                    tmem_ld32x2(tmem + lo + pb + 64u * (uint32_t)g,
+                                tmem + lo + pb + 64u * (uint32_t)g + 32u, d0, d1);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        Sr[j] = fmaf(Gl, Sr[j], d0[j]);
+                        Sr[32 + j] = fmaf(Gl, Sr[32 + j], d1[j]);
+                    }
+                    put_state();
+                }
+                if (lane == 0) TRACE(c, 28 + (warp - 2));
+                tc_fence_before();
+                // the tile of chunk c-3 is read out before the tile of chunk c-1 goes out
+                if (tid == 64) bulk_wait_read_all();
+                if (tid == 64) TRACE(c, 18);
+                __syncwarp();
+            } else {
+                bar_sync(3, 288);
+                if (leader) {
+                    // dS^T(c) into [U~^T | (W S0)^T] of this parity (read by now), then
+                    // U~(c+1) into the other parity, whose columns last held dS^T(c-1)
+                    TCLK(t7);
+                    TPUT(c, 7, t7);
+                    ok = ok && wait_or_abort(&bar[B_FULLL0 + s], (c >> 1) & 1, abort_flag, ST_MMA);
+                    if (ok) {
+                        TCLK(t14);
+                        tc_fence_after();
+                        issue_t_ds(tmem, pb, ut, st);
+                        tc_commit(&bar[T_SDONE]);
+                        TCLK(t9);
+                        TPUT(c, 14, t14);
+                        TPUT(c, 9, t9);
+                        if (c + 1 < nch) ok = issue_next_u(c + 1);
+                        TCLK(t8);
+                        TPUT(c, 8, t8);
+                    }
+                }
+                __syncwarp();
+            }
+            stop = bar_any(4, 288, !ok || *abort_flag);
+            if (stop) break;
+            if (!issuer && c > 0) flush_out(c - 1);
+            if (leader) {
+                if (c + 1 < nch) issue_next_s0(c + 1);
+                // O^T(c) += U^T P^T, behind [W; Q~] S0 of chunk c+1 in the pipe
+                TCLK(t4);
+                issue_t_o(tmem, pb + CarryT::OQ, ut, st);
+                tc_commit(&bar[T_ODONE0 + s]);
+                tc_commit(&bar[B_EMPTYL0 + s]);  // K~, P, scalars of chunk c are read
+                TPUT(c, 4, t4);
+            }
+            __syncwarp();
+            done = c + 1;
+        }
+        // every role decides the epilogue together (lanes 1-31 of the issuer warp only
+        // take part in this barrier)
+        if ((leader || !issuer) && (!ok || done < nch) && !*abort_flag)
+            record_failure(abort_flag, ST_CARRY);
+        __syncwarp();
+        bar_sync(1, 288);
+        ok = !*abort_flag;
+        if (!issuer) {
+            // the output of the last chunk, then the state
+            const int cl = nch - 1;
+            if (ok) {
+                ok = wait_hot(&bar[T_ODONE0 + (cl & 1)], (cl >> 1) & 1, abort_flag, ST_CARRY);
+                if (ok) {
+                    tc_fence_after();
+                    stage_out(cl);
+                }
+            }
+            if (tid == 64) bulk_wait_read_all();
+            __syncwarp();
+            if (!bar_any(2, 256, !ok || *abort_flag)) {
+                flush_out(cl);
+#pragma unroll
+                for (int i = 0; i < 64; ++i) gst[(size_t)i * 128] = Sr[i];
+            }
+            if (tid == 64) bulk_wait_read_all();
+        }
+        // no MMA may be in flight when TMEM is freed
+        if (leader) {
+            tc_commit(&bar[T_DRAIN]);
+            mbar_wait_bounded(&bar[T_DRAIN], 0, kWaitNs);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, CarryT::TMCOLS);
+    }
+}
+
 // ---------------------------------------------------------------- variable-length batch
 
 // One CTA: table[0..N] = chunk bases of the sequences cu[n] .. cu[n+1] - 1 in 64-token
@@ -1318,7 +1768,7 @@ namespace {
 // The two kernels of one segment of the sequence (chunks c0 .. c0 + nseg - 1), whose
 // B Hv nseg workspace units start at `ws`.
 struct SegmentLaunch {
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     const PrefillArgs* a;
     int sms;
 
@@ -1331,8 +1781,8 @@ struct SegmentLaunch {
     // sequences of the carry grid: the batch, or the variable-length batch's sequences
     int rows() const { return a->cu_seqlens ? a->N : a->B; }
     // two carry CTAs per head (64-column state slices) while that still fits the GPU in
-    // one wave, else one CTA per head (128 columns: half the MMA instructions per head)
-    bool split() const { return 2 * rows() * a->Hv <= sms; }
+    // one wave, else one transposed CTA per head
+    bool split() const { return kCarrySplit && 2 * rows() * a->Hv <= sms; }
 
     cudaError_t prep(int c0, int nseg, uint8_t* ws, cudaStream_t st) const {
         prep_tc_kernel<<<dim3(nseg, a->Hv, a->B), PREP_THREADS, PREP_SMEM, st>>>(
@@ -1345,9 +1795,8 @@ struct SegmentLaunch {
                 <<<dim3(2, a->Hv, rows()), CARRY_THREADS, CarryCfg<64>::SMEM, st>>>(
                     mv, args(c0, nseg, ws));
         else
-            carry_tc_kernel<128>
-                <<<dim3(1, a->Hv, rows()), CARRY_THREADS, CarryCfg<128>::SMEM, st>>>(
-                    mv, args(c0, nseg, ws));
+            carry_t_kernel<<<dim3(1, a->Hv, rows()), CARRY_T_THREADS, CarryT::SMEM, st>>>(
+                mv, mo, args(c0, nseg, ws));
         return cudaGetLastError();
     }
 };
@@ -1361,9 +1810,8 @@ cudaError_t set_attributes() {
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)CarryCfg<64>::SMEM);
         if (r == cudaSuccess)
-            r = cudaFuncSetAttribute(carry_tc_kernel<128>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)CarryCfg<128>::SMEM);
+            r = cudaFuncSetAttribute(carry_t_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)CarryT::SMEM);
         return r;
     }();
     return e;
@@ -1402,7 +1850,7 @@ cudaError_t overlap_init(Overlap& o) {
 cudaError_t prepare(SegmentLaunch& L, const PrefillArgs& a) {
     L.a = &a;
     if (!encode_3d(&L.mq, a.q, a.S, a.B * a.Hk) || !encode_3d(&L.mk, a.k, a.S, a.B * a.Hk) ||
-        !encode_3d(&L.mv, a.v, a.S, a.B * a.Hv))
+        !encode_3d(&L.mv, a.v, a.S, a.B * a.Hv) || !encode_3d(&L.mo, a.out, a.S, a.B * a.Hv))
         return cudaErrorInvalidValue;
     cudaError_t e = set_attributes();
     if (e != cudaSuccess) return e;
@@ -1418,7 +1866,7 @@ int prefill_tc_segments(int B, int Hv, int nch, int sms) {
     // The carry of a segment occupies 2 B Hv SMs (one CTA each) for the whole segment;
     // the prep of the next segment runs meanwhile on the SMs left over. Without enough
     // of those, or with too few chunks, one segment.
-    const int carry_sms = 2 * B * Hv;
+    const int carry_sms = (kCarrySplit && 2 * B * Hv <= sms ? 2 : 1) * B * Hv;
     if (carry_sms > sms || sms - carry_sms < sms / 4 || nch < 2 * kMinSegmentChunks) return 1;
     return std::max(1, std::min(kOverlapSegments, nch / kMinSegmentChunks));
 }

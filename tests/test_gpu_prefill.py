@@ -112,6 +112,22 @@ def test_prefill_bf16_batched_workload_sampled_heads():
     _sampled_parity(syn.PREFILL_BF16_BATCHED, [(0, 1), (3, 20), (7, 31)], TOL_BF16)
 
 
+@pytest.mark.parametrize("S,state", [(187, 0.05), (128, None), (64 * 5, 0.05)])
+def test_prefill_transposed_carry_full_parity(S, state):
+    """B*Hv = 80 value heads: more than two carry CTAs per head fit, so the transposed
+    one-CTA-per-head carry runs (state columns in TMEM lanes). Every head against the
+    oracle, with a ragged tail, a zero start and a whole number of chunks; and the same
+    bits on a second call."""
+    w = syn.shrink(syn.PREFILL_BF16_GQA2, B=1, Hk=40, Hv=80, S=S, state_std=state)
+    x = syn.prefill_inputs(w)
+    out, st = gpu_prefill(x)
+    o_ref, s_ref = oracle_prefill_all(x)
+    assert rel(to_np(out), o_ref) <= TOL_BF16["out"]
+    assert rel(to_np(st), s_ref) <= TOL_BF16["state"]
+    o2, s2 = gpu_prefill(x)
+    assert torch.equal(out, o2) and torch.equal(st, s2)
+
+
 @pytest.mark.parametrize("w", [syn.PREFILL_F32_SMALL,
                                syn.shrink(syn.PREFILL_BF16_GQA2, S=256)], ids=["f32", "bf16"])
 def test_prefill_is_bitwise_reproducible(w):
