@@ -320,20 +320,6 @@ __device__ __forceinline__ void st_shared_b16(uint32_t addr, float x) {
                  : "memory");
 }
 
-__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint32_t v) {
-    asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"((unsigned short)(v & 0xffffu))
-                 : "memory");
-}
-
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
-    uint4 r;
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "r"(addr)
-                 : "memory");
-    return r;
-}
-
 // Byte address of element (r, col) (bf16) in a 128-byte-swizzled tile of 64-wide rows.
 __device__ __forceinline__ uint32_t sw128_elem(uint32_t tile, int r, int col) {
     return tile + (uint32_t)(r >> 3) * 1024u + (uint32_t)(r & 7) * 128u +
@@ -1284,15 +1270,14 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
 // TMEM lanes are the value columns v of the state, so the U step and the state update
 // run on all four SM sub-partitions, and no hand-off goes through shared memory.
 // Warp 0: producer (carry_produce<128>, both 64-column V blocks); warp 1 (one thread):
-// every MMA, in the order that keeps the tensor pipe free for the chain: dS^T(c),
-// U~(c+1) (runs during the state update), [W; Q~] S0 of chunk c+1, U^T P^T of chunk c
-// (runs during the next U step); warps 2..9: SIMT, warp (q = warp % 4,
-// g = (warp - 2) / 4) owning lane v = 32 q + lane, fp32 state rows 64 g .. 64 g + 63
-// (registers) and tokens 32 g .. 32 g + 31 of U and of the output.
+// every MMA, in the order that keeps the tensor pipe free for the chain: dS^T(c), then
+// U~(c+1) (runs during the state update), then [W; Q~] S0 of chunk c+1, then U^T P^T(c)
+// (runs during the next U step); warps 2..9: SIMT,
+// warp (q = warp % 4, g = (warp - 2) / 4) owning lane v = 32 q + lane, fp32 state rows
+// 64 g .. 64 g + 63 (registers) and tokens 32 g .. 32 g + 31 of U and of the output.
 struct CarryT {
     static constexpr uint32_t STAGE = CarryCfg<128>::STAGE;
-    static constexpr uint32_t OUT = 2 * STAGE;  // two output tiles [64 t][64 v] x 2, bf16
-    static constexpr uint32_t SCAL = OUT + 2 * 16384;
+    static constexpr uint32_t SCAL = 2 * STAGE;
     static constexpr uint32_t BAR = SCAL + 2 * sizeof(CarryScalars);
     static constexpr uint32_t MISC = BAR + 128;
     static constexpr uint32_t SMEM = MISC + 64 + 1024;
@@ -1302,7 +1287,7 @@ struct CarryT {
     // 32 columns; U^T P^T of a chunk still reads it during the next chunk's U step).
     static constexpr uint32_t UB = 0, WSC = 64, OQ = 128, PSTRIDE = 192;
     static constexpr uint32_t S0T = 384, UT = 448, TMCOLS = 512;  // U^T of parity p at UT + 32 p
-    static_assert(OUT % 1024 == 0 && SCAL % 16 == 0 && BAR % 8 == 0, "alignment");
+    static_assert(SCAL % 16 == 0 && BAR % 8 == 0, "alignment");
     static_assert(SMEM <= 232448, "shared memory budget");
 };
 constexpr int CARRY_T_THREADS = 320;
@@ -1352,8 +1337,7 @@ __device__ __forceinline__ void issue_t_o(uint32_t tmem, uint32_t d, uint32_t ut
 }
 
 __global__ void __launch_bounds__(CARRY_T_THREADS, 1)
-    carry_t_kernel(const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mo,
-                   TcArgs a) {
+    carry_t_kernel(const __grid_constant__ CUtensorMap mv, TcArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(sm);
@@ -1392,10 +1376,7 @@ __global__ void __launch_bounds__(CARRY_T_THREADS, 1)
         tmem_alloc(misc, CarryT::TMCOLS);
         tmem_relinquish();
     }
-    if (tid == 32) {
-        prefetch_tensormap(&mv);
-        prefetch_tensormap(&mo);
-    }
+    if (tid == 32) prefetch_tensormap(&mv);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1423,42 +1404,20 @@ __global__ void __launch_bounds__(CARRY_T_THREADS, 1)
             tmem_st32u(tmem + lo + CarryT::S0T + 32u * (uint32_t)g, w);
             tmem_wait_st();
         };
-        // out = scale O of chunk cc, tokens 32 g .. 32 g + 31 of column v, into the bf16
-        // output tile of the chunk's parity
-        auto stage_out = [&](int cc) {
-            const uint32_t ob = sbase + CarryT::OUT + 16384u * (uint32_t)(cc & 1) +
-                                8192u * (uint32_t)(v >> 6);
+        // out = scale O of chunk cc for tokens 32 g .. 32 g + 31 (below tend) of column v,
+        // straight from the registers: for each token a warp writes 64 contiguous bytes
+        auto store_out = [&](int cc) {
+            const int t0 = tbase + cc * C + 32 * g;
             float o[32];
             tmem_ld32(tmem + lo + CarryT::PSTRIDE * (uint32_t)(cc & 1) + CarryT::OQ +
                           32u * (uint32_t)g,
                       o);
+            unsigned short* dst = reinterpret_cast<unsigned short*>(gout) + (size_t)t0 * 128 + v;
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const uint32_t w = pack_bf16(a.scale * o[2 * j], a.scale * o[2 * j + 1]);
-                st_shared_u16(sw128_elem(ob, 32 * g + 2 * j, v & 63), w);
-                st_shared_u16(sw128_elem(ob, 32 * g + 2 * j + 1, v & 63), w >> 16);
-            }
-            fence_proxy_async_smem();
-        };
-        // after a SIMT barrier: the tile goes out by TMA (one thread), or, for a chunk
-        // that ends past the sequence, row by row below tend (all SIMT threads)
-        auto flush_out = [&](int cc) {
-            const int t0 = tbase + cc * C;
-            const uint32_t ob = sbase + CarryT::OUT + 16384u * (uint32_t)(cc & 1);
-            if (t0 + C <= tend) {
-                if (tid == 64) {
-                    tma_store_3d(&mo, ob, 0, t0, zo);
-                    tma_store_3d(&mo, ob + 8192u, 64, t0, zo);
-                    bulk_commit();
-                }
-            } else {
-                for (int i = tid - 64; i < 1024; i += 256) {
-                    const int r = i >> 4, j = i & 15;
-                    if (t0 + r < tend) {
-                        const uint4 x = ld_shared_v4(sw128_chunk(ob + 8192u * (uint32_t)(j >> 3), r, j & 7));
-                        *reinterpret_cast<uint4*>(gout + (size_t)(t0 + r) * 128 + 8 * j) = x;
-                    }
-                }
+                if (t0 + 2 * j < tend) dst[(size_t)(2 * j) * 128] = (unsigned short)(w & 0xffffu);
+                if (t0 + 2 * j + 1 < tend) dst[(size_t)(2 * j + 1) * 128] = (unsigned short)(w >> 16);
             }
         };
         // U~ of chunk cc into its parity's columns; ADONE of chunk cc covers it
@@ -1538,13 +1497,14 @@ __global__ void __launch_bounds__(CARRY_T_THREADS, 1)
                 tc_fence_before();
                 __syncwarp();
                 bar_arrive(3, 288);
-                // the output of chunk c-1 (its U^T P^T ran during this U step)
+                // the output of chunk c-1 (its U^T P^T ran during this U step) while dS^T(c)
+                // runs
                 if (c > 0) {
                     ok = ok && wait_hot(&bar[T_ODONE0 + (s ^ 1)], ((c - 1) >> 1) & 1, abort_flag,
                                         ST_CARRY);
                     if (ok) {
                         tc_fence_after();
-                        stage_out(c - 1);
+                        store_out(c - 1);
                     }
                 }
                 if (tid == 64) TRACE(c, 17);
@@ -1565,8 +1525,6 @@ __global__ void __launch_bounds__(CARRY_T_THREADS, 1)
                 }
                 if (lane == 0) TRACE(c, 28 + (warp - 2));
                 tc_fence_before();
-                // the tile of chunk c-3 is read out before the tile of chunk c-1 goes out
-                if (tid == 64) bulk_wait_read_all();
                 if (tid == 64) TRACE(c, 18);
                 __syncwarp();
             } else {
@@ -1594,7 +1552,6 @@ __global__ void __launch_bounds__(CARRY_T_THREADS, 1)
             }
             stop = bar_any(4, 288, !ok || *abort_flag);
             if (stop) break;
-            if (!issuer && c > 0) flush_out(c - 1);
             if (leader) {
                 if (c + 1 < nch) issue_next_s0(c + 1);
                 // O^T(c) += U^T P^T, behind [W; Q~] S0 of chunk c+1 in the pipe
@@ -1617,21 +1574,13 @@ __global__ void __launch_bounds__(CARRY_T_THREADS, 1)
         if (!issuer) {
             // the output of the last chunk, then the state
             const int cl = nch - 1;
+            if (ok) ok = wait_hot(&bar[T_ODONE0 + (cl & 1)], (cl >> 1) & 1, abort_flag, ST_CARRY);
             if (ok) {
-                ok = wait_hot(&bar[T_ODONE0 + (cl & 1)], (cl >> 1) & 1, abort_flag, ST_CARRY);
-                if (ok) {
-                    tc_fence_after();
-                    stage_out(cl);
-                }
-            }
-            if (tid == 64) bulk_wait_read_all();
-            __syncwarp();
-            if (!bar_any(2, 256, !ok || *abort_flag)) {
-                flush_out(cl);
+                tc_fence_after();
+                store_out(cl);
 #pragma unroll
                 for (int i = 0; i < 64; ++i) gst[(size_t)i * 128] = Sr[i];
             }
-            if (tid == 64) bulk_wait_read_all();
         }
         // no MMA may be in flight when TMEM is freed
         if (leader) {
@@ -1768,7 +1717,7 @@ namespace {
 // The two kernels of one segment of the sequence (chunks c0 .. c0 + nseg - 1), whose
 // B Hv nseg workspace units start at `ws`.
 struct SegmentLaunch {
-    CUtensorMap mq, mk, mv, mo;
+    CUtensorMap mq, mk, mv;
     const PrefillArgs* a;
     int sms;
 
@@ -1796,7 +1745,7 @@ struct SegmentLaunch {
                     mv, args(c0, nseg, ws));
         else
             carry_t_kernel<<<dim3(1, a->Hv, rows()), CARRY_T_THREADS, CarryT::SMEM, st>>>(
-                mv, mo, args(c0, nseg, ws));
+                mv, args(c0, nseg, ws));
         return cudaGetLastError();
     }
 };
@@ -1850,7 +1799,7 @@ cudaError_t overlap_init(Overlap& o) {
 cudaError_t prepare(SegmentLaunch& L, const PrefillArgs& a) {
     L.a = &a;
     if (!encode_3d(&L.mq, a.q, a.S, a.B * a.Hk) || !encode_3d(&L.mk, a.k, a.S, a.B * a.Hk) ||
-        !encode_3d(&L.mv, a.v, a.S, a.B * a.Hv) || !encode_3d(&L.mo, a.out, a.S, a.B * a.Hv))
+        !encode_3d(&L.mv, a.v, a.S, a.B * a.Hv))
         return cudaErrorInvalidValue;
     cudaError_t e = set_attributes();
     if (e != cudaSuccess) return e;

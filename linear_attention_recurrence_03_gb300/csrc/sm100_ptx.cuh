@@ -157,17 +157,6 @@ __device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src_saddr, uint32_t
                  : "memory");
 }
 
-// Tile store shared -> global through a 3-D tensor map (bulk-group completion; rows past
-// the tensor's bounds are not written). Coordinates must not be negative.
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src_saddr, int x,
-                                             int y, int z) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-            reinterpret_cast<uint64_t>(map)),
-        "r"(src_saddr), "r"(x), "r"(y), "r"(z)
-        : "memory");
-}
-
 __device__ __forceinline__ void bulk_commit() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
