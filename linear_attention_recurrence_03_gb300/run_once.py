@@ -3,6 +3,7 @@ command for profilers (a fixed number of launches, no timing loop, no oracle).
 
     python -m linear_attention_recurrence_03_gb300.run_once decode --iters 2
     python -m linear_attention_recurrence_03_gb300.run_once prefill_layer --iters 2
+    python -m linear_attention_recurrence_03_gb300.run_once prefill_batched --batch 3 --iters 2
 """
 from __future__ import annotations
 
@@ -30,7 +31,8 @@ def main(argv=None) -> int:
     p.add_argument("--heads", type=int, default=0,
                    help="prefill: keep only this many value heads (0 = all)")
     p.add_argument("--batch", type=int, default=0,
-                   help="decode: this many batch rows of 32 value heads (0 = all 256)")
+                   help="decode: this many batch rows of 32 value heads (0 = all 256); "
+                        "prefill: this many batch rows (0 = the workload's)")
     a = p.parse_args(argv)
     lib_build.build()
     dev = torch.device("cuda:0")
@@ -47,6 +49,8 @@ def main(argv=None) -> int:
         w = PREFILL[a.workload]
         if a.heads:
             w = syn.shrink(w, Hv=a.heads, Hk=max(1, a.heads * w.Hk // w.Hv))
+        if a.batch:
+            w = syn.shrink(w, B=a.batch)
         x = syn.prefill_inputs(w)
         t = [x[n].to(dev) for n in ("q", "k", "v", "g_log", "beta")]
         st = None if x["state"] is None else x["state"].to(dev)
