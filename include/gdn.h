@@ -61,8 +61,8 @@ typedef enum gdn_tril_algorithm {
 /*
  * gdn_prefill_workspace_bytes -- scratch (device memory) gdn_prefill needs for this
  * shape. Returns 0 when no workspace is needed, or (size_t)-1 if the shape is invalid.
- * The bf16 path with Dk = Dv = 128 (the tensor-core kernels) needs 66560 bytes per
- * (batch, value head, 64-token chunk): B * Hv * ceil(S / 64) * 66560; every other
+ * The bf16 path with Dk = Dv = 128 (the tensor-core kernels) needs 66064 bytes per
+ * (batch, value head, 64-token chunk): B * Hv * ceil(S / 64) * 66064; every other
  * shape needs none.
  */
 size_t gdn_prefill_workspace_bytes(int B, int Hk, int Hv, int S, int Dk, int Dv,
@@ -105,7 +105,7 @@ gdn_status gdn_prefill(const void* q, const void* k, const void* v,
 /*
  * gdn_prefill_varlen_workspace_bytes -- device scratch gdn_prefill_varlen needs for N
  * sequences packed into T tokens: on the bf16 Dk = Dv = 128 path (tensor cores)
- * Hv * (ceil(T / 64) + N) * 66560 bytes rounded up to 256, plus 4 * (N + 2); on every
+ * Hv * (ceil(T / 64) + N) * 66064 bytes rounded up to 256, plus 4 * (N + 2); on every
  * other path 4 * (N + 2) rounded up to 16. (size_t)-1 for an invalid shape.
  */
 size_t gdn_prefill_varlen_workspace_bytes(int N, int Hk, int Hv, int T, int Dk, int Dv,

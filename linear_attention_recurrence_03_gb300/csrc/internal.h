@@ -70,8 +70,9 @@ cudaError_t launch_prefill_simt(const PrefillArgs& a, bool bf16, cudaStream_t st
                                 int* launched);
 
 // tcgen05 chunked prefill (bf16, Dk = Dv = 128, S > 0): a parallel prep kernel writes
-// 65 KB of operand tiles per (batch, value head, 64-token chunk) to the workspace, then a
-// carry kernel runs the sequential part. *launched receives the kernels enqueued.
+// up to 64.5 KB of operand tiles and scalars per (batch, value head, 64-token chunk) to
+// the workspace, then a carry kernel runs the sequential part. *launched receives the
+// kernels enqueued.
 bool prefill_tc_supported(const PrefillArgs& a, bool bf16);
 size_t prefill_tc_workspace_bytes(int B, int Hv, int S);
 size_t prefill_tc_unit_bytes();

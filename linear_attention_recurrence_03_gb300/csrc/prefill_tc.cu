@@ -21,10 +21,11 @@
 // Two kernels. Everything that does not depend on S0 (the Gram matrices, the decay
 // masks, the (I+A)^-1 solve, T_U, P and W) is independent across chunks, so it runs
 // first as a fully parallel grid ("prep", one CTA per (batch, value head, chunk)) that
-// writes three bf16 operand tiles per chunk to a workspace, already in the 128-byte
-// swizzled layout the tensor cores read. The sequential part ("carry") then streams v
-// and those tiles through a two-stage ring and keeps only the S0-dependent chain per
-// chunk, in one of two forms:
+// writes bf16 operand tiles (T_U, P, W, and for the two-slice carry Q~ and K~) and the
+// decay scalars per chunk to a workspace, the tiles already in the 128-byte swizzled
+// layout the tensor cores read. The sequential part ("carry") then streams v and those
+// tiles through a two-stage ring and keeps only the S0-dependent chain per chunk, in one
+// of two forms:
 //   carry_tc_kernel<64>: one CTA per (batch, value head, 64-column slice of the state;
 //   the slices never communicate), state rows in TMEM lanes, used while two CTAs per
 //   head fit the GPU:
@@ -33,10 +34,11 @@
 //          [K~_1;P] U             -> P U                  (M128 N64  K64)
 //          K~^T U                 -> state increment      (M128 N64  K64)
 //   carry_t_kernel: one CTA per (batch, value head), the chain transposed (state columns
-//   in TMEM lanes) so that U^T and S0^T enter the MMAs from TMEM:
+//   in TMEM lanes) so that U^T and S0^T enter the MMAs from TMEM; it loads q and k itself
+//   and applies their row decays in its SIMT steps (U' = diag(exp(gamma_last - gamma)) U):
 //          V^T T_U^T              -> U~^T                 (M128 N64  K64)
-//          S0^T [W;Q~]^T          -> (W S0)^T, (Q~ S0)^T  (M128 N128 K128, A in TMEM)
-//          U^T K~                 -> dS^T                 (M128 N128 K64, A in TMEM)
+//          S0^T [W;Q]^T           -> (W S0)^T, (Q S0)^T   (M128 N128 K128, A in TMEM)
+//          U'^T K                 -> dS^T                 (M128 N128 K64, A in TMEM)
 //          U^T P^T                -> (P U)^T              (M128 N64  K64, A in TMEM)
 //   prep   [Q;K] K^T              -> QK^T, KK^T           (M128 N64  K128)
 //          [T_W;P] K              -> W                    (M128 N128 K64)
@@ -134,21 +136,25 @@ constexpr int kFirstSegmentPermille = GDN_FIRST_SEGMENT_PERMILLE;
 #endif
 constexpr bool kCarrySplit = GDN_CARRY_SPLIT != 0;
 
-// ---- workspace: per (batch, value head, chunk) unit, eight bf16 tiles of 64 rows x 64
-// columns in the 128-byte swizzled layout, T_U | P | W[:, 0:64] | W[:, 64:128] |
-// Q~[:, 0:64] | Q~[:, 64:128] | K~[:, 0:64] | K~[:, 64:128] with Q~ = diag(Gamma) Q and
-// K~ = diag(exp(gamma_last - gamma)) K, then the carry's decay scalars
-constexpr uint32_t WS_UNIT = 66560;
+// ---- workspace: per (batch, value head, chunk) unit, bf16 tiles of 64 rows x 64 columns
+// in the 128-byte swizzled layout, T_U | P | W[:, 0:64] | W[:, 64:128] | Q~[:, 0:64] |
+// Q~[:, 64:128] | K~[:, 0:64] | K~[:, 64:128], then the carry's decay scalars, with
+// Q~ = diag(Gamma) Q and K~ = diag(exp(gamma_last - gamma)) K. The Q~ and K~ tiles are
+// written only for the two-slice carry (latency-bound: the row decays are applied before
+// it runs); the transposed carry reads q and k itself and applies the decays in its own
+// steps, so its units carry T_U, P, W and the scalars only (half the traffic).
 constexpr uint32_t WS_TU = 0, WS_P = 8192, WS_W = 16384, WS_QT = 32768, WS_KT = 49152,
                    WS_CS = 65536;
 
 struct CarryScalars {
     float kdec[C];  // exp(gamma_last - gamma_r)
+    float Gam[C];   // exp(gamma_r)
     float Gl;       // exp(gamma_last)
     float pad[3];
 };
-static_assert(sizeof(CarryScalars) % 16 == 0 && WS_CS + sizeof(CarryScalars) <= WS_UNIT,
-              "scalars fit the unit as whole 16-byte rows");
+constexpr uint32_t WS_UNIT = WS_CS + (uint32_t)sizeof(CarryScalars);
+static_assert(sizeof(CarryScalars) % 16 == 0 && WS_UNIT % 16 == 0,
+              "scalars and units are whole 16-byte rows");
 
 // ---- prep kernel: shared memory map (offsets from a 1024-byte aligned base), sized
 // for three CTAs per SM
@@ -197,6 +203,7 @@ enum { PB_FULL = 0, PB_GRAM, PB_PREP, PB_WDONE, PB_DRAIN, PB_COUNT };
 //     V slice (64 tokens x NS columns, in 64-column blocks), T_U ([T_U; -] one operand)
 //     early group (read by U~ and [W; Q~] S0, freed as soon as they complete): W, Q~, V,
 //     T_U; late group (read by K~^T U, P U and the state update): K~, P and the scalars
+//     (the transposed carry loads q and k into the Q~ and K~ slots)
 //   two U tiles (64 tokens x NS, by chunk parity), the bf16 state operand (128 x NS,
 //   64-column blocks), per-stage scalars, barriers
 // warp 0: producer; warp 2: MMA issuer (an SM sub-partition whose SIMT warps only write the
@@ -256,6 +263,8 @@ struct TcArgs {
     const int* cu;
     const int* cb;
     int N;
+    // the prep writes Q~ and K~ to the workspace (for the two-slice carry)
+    int export_qk;
 };
 
 __device__ __forceinline__ size_t ws_offset(int b, int h, int c, int Hv, int nch) {
@@ -514,7 +523,7 @@ __device__ __forceinline__ void issue_u(uint32_t tmem, uint32_t st, uint32_t tb)
     for (int k = 0; k < 4; ++k) mma_bf16(tmem + tb, dadd(au, k * 32), dadd(bv, k * 2048), id, k > 0);
 }
 
-// carry: [W S0; Q~ S0] = [W; Q~] S0 over Dk = 128, into the TMEM buffer `ta`
+// carry: [W S0; Q S0] = [W; Q] S0 over Dk = 128, into the TMEM buffer `ta`
 template <int NS>
 __device__ __forceinline__ void issue_carry1(uint32_t tmem, uint32_t st, uint32_t s_tile,
                                              uint32_t ta) {
@@ -528,7 +537,7 @@ __device__ __forceinline__ void issue_carry1(uint32_t tmem, uint32_t st, uint32_
     }
 }
 
-// carry: the state increment K~^T U over the tokens (K~ read M-major), into `tb`
+// carry: the state increment K^T U' over the tokens (K read M-major), into `tb`
 template <int NS>
 __device__ __forceinline__ void issue_carry3(uint32_t tmem, uint32_t st, uint32_t u_tile,
                                              uint32_t tb) {
@@ -540,8 +549,9 @@ __device__ __forceinline__ void issue_carry3(uint32_t tmem, uint32_t st, uint32_
         mma_bf16(tmem + tb, dadd(ak, k * 2048), dadd(bu2, k * 2048), id, k > 0);
 }
 
-// carry: [K~_1 U; P U] = [K~_1; P] U, accumulated onto [W S0; Q~ S0] in `ta`: the lower
-// half becomes the un-scaled output Q~ S0 + P U (the upper half is no longer needed)
+// carry: [K_1 U; P U] = [K_1; P] U, accumulated onto [W S0; diag(Gamma) Q S0] in `ta`: the
+// lower half becomes the un-scaled output diag(Gamma) Q S0 + P U (the upper half is no
+// longer needed)
 template <int NS>
 __device__ __forceinline__ void issue_carry2(uint32_t tmem, uint32_t st, uint32_t u_tile,
                                              uint32_t ta) {
@@ -652,6 +662,8 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
         CarryScalars& cs = *reinterpret_cast<CarryScalars*>(sm + P_CS);
         cs.kdec[lane] = __expf(gl - x0);
         cs.kdec[lane + 32] = __expf(gl - x1);
+        cs.Gam[lane] = __expf(x0);
+        cs.Gam[lane + 32] = __expf(x1);
         if (lane == 31) cs.Gl = __expf(gl);
         sc.gam[lane] = x0;
         sc.gam[lane + 32] = x1;
@@ -739,9 +751,11 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
                 *reinterpret_cast<uint4*>(wsu + (isq ? WS_QT : WS_KT) + blk * 8192 + off) =
                     make_uint4(o[0], o[1], o[2], o[3]);
             };
+            if (a.export_qk) {
 #pragma unroll
-            for (int it = 0; it < 4; ++it) export_rows(P + 256 * it, true);
-            bar_sync(2, 256);  // every Q chunk is read before A overwrites the Q slots
+                for (int it = 0; it < 4; ++it) export_rows(P + 256 * it, true);
+                bar_sync(2, 256);  // every Q chunk is read before A overwrites the Q slots
+            }
 
             // ---- P (bf16 tile) and A (fp32 blocks) from the Gram matrices: thread (wg, L)
             // takes row L of [QK^T; KK^T], columns 16 bj + 8 wg .. + 7 of every 16-block bj
@@ -795,7 +809,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
             // column of the block's inverse, its 16 entries in registers. The rows go in
             // lockstep, so the threads of a block read the same A entry (a broadcast);
             // the column's zeros above its diagonal keep the full sums exact. Meanwhile
-            // warps 2..7 write K~ to the workspace.
+            // warps 2..7 write K~ to the workspace (when it is exported).
             if (P < 64) {
                 const int i = P >> 4, cc = P & 15;
                 const float* Ad = Ablk(i, i);
@@ -821,7 +835,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
                     st_shared_b16(sw128_elem(tu, 16 * i + m, J), x[m] * bj);
                     st_shared_b16(sw128_elem(tw, 16 * i + m, J), x[m] * wj);
                 }
-            } else {
+            } else if (a.export_qk) {
                 for (int j = P - 64; j < 1024; j += 192) export_rows(j, false);
             }
             bar_sync(2, 256);
@@ -915,29 +929,32 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
 // ---------------------------------------------------------------- the carry kernel
 
 // One CTA per (NS-column slice of the state, value head h, batch b), sequential over
-// chunks. Warp 0 streams the chunk's k and v slice (TMA) and the prep's tiles and scalars
+// chunks. Warp 0 streams the chunk's v slice (TMA) and the prep's tiles and scalars
 // (bulk copies) into a two-stage ring; warp 2 (one thread) issues every MMA; warps 4..11
 // (two per TMEM lane quadrant, thread = state row L, NS/2 columns) keep the fp32 state in
 // registers, form U (rows 0-63) while writing the previous chunk's output (rows 64-127),
 // and update the state. MMA order per chunk c: [W; Q~] S0, U~ of chunk c+1 if it has
-// landed, then K^T U', U~ of chunk c+1 if not issued yet, P U.
-// The producer of a carry CTA (one thread): streams chunk c of the head's workspace units
-// (from `wsh`) and its V slice (columns n0 .. n0 + NS - 1, token rows tbase + 64 c, tensor
-// z = zv) through the two-stage ring, in the early (W, Q~, V, T_U) and late (K~, P,
-// scalars) copy groups.
+// landed, then K~^T U, U~ of chunk c+1 if not issued yet, P U.
+
+// The producer of a carry CTA (one thread): streams chunk c (token rows tbase + 64 c) into
+// the two-stage ring, in the early (W, Q~ or q, V, T_U) and late (K~ or k, P, scalars) copy
+// groups: the prep's tiles and scalars from the head's workspace units (from `wsh`), the V
+// slice (columns n0 .. n0 + NS - 1, tensor z = zv), and either the prep's Q~ and K~
+// (qk_ws) or q and k of the key head (tensor z = zq, both 64-column blocks).
 template <int NS>
 __device__ __forceinline__ void carry_produce(uint8_t* sm, uint64_t* bar, CarryScalars* scal,
-                                              const CUtensorMap* mvp, const uint8_t* wsh,
-                                              int nch, int n0, int tbase, int zv,
-                                              volatile int* abort_flag) {
+                                              const CUtensorMap* mqp, const CUtensorMap* mkp,
+                                              const CUtensorMap* mvp, bool qk_ws,
+                                              const uint8_t* wsh, int nch, int n0, int tbase,
+                                              int zq, int zv, volatile int* abort_flag) {
     using Cfg = CarryCfg<NS>;
-    const CUtensorMap& mv = *mvp;
     int issued = 0;
     for (int c = 0; c < nch; ++c) {
         const int s = c & 1;
         uint8_t* st = sm + s * Cfg::STAGE;
         const uint8_t* wsc = wsh + (size_t)c * WS_UNIT;
-        // early group of chunk c: W, Q~, V, T_U
+        const int t = tbase + c * C;
+        // early group of chunk c: W, Q~ or q, V, T_U
         if (c >= 2 && !wait_or_abort(&bar[B_EMPTYE0 + s], ((c >> 1) + 1) & 1, abort_flag,
                                      ST_PRODUCER))
             break;
@@ -948,28 +965,40 @@ __device__ __forceinline__ void carry_produce(uint8_t* sm, uint64_t* bar, CarryS
         for (int blk = 0; blk < 2; ++blk) {
             uint8_t* sb = st + blk * BLK_STRIDE;
             bulk_g2s(sb + OFF_W, wsc + WS_W + blk * 8192, 8192, fe);
-            bulk_g2s(sb + OFF_Q, wsc + WS_QT + blk * 8192, 8192, fe);
+            if (qk_ws) bulk_g2s(sb + OFF_Q, wsc + WS_QT + blk * 8192, 8192, fe);
+            else tma_load_3d(sb + OFF_Q, mqp, fe, blk * 64, t, zq);
         }
         for (int blk = 0; blk < Cfg::NB; ++blk)
-            tma_load_3d(st + OFF_V + blk * 8192, &mv, fe, n0 + blk * 64, tbase + c * C,
-                        zv);
+            tma_load_3d(st + OFF_V + blk * 8192, mvp, fe, n0 + blk * 64, t, zv);
         bulk_g2s(st + Cfg::OFF_TU, wsc + WS_TU, 8192, fe);
-        // late group of chunk c: K~, P, scalars
+        // late group of chunk c: K~ or k, P, scalars
         if (c >= 2 && !wait_or_abort(&bar[B_EMPTYL0 + s], ((c >> 1) + 1) & 1, abort_flag,
                                      ST_PRODUCER))
             break;
         uint64_t* fl = &bar[B_FULLL0 + s];
         mbar_arrive_expect_tx(fl, 3 * 8192 + (uint32_t)sizeof(CarryScalars));
-        for (int blk = 0; blk < 2; ++blk)
-            bulk_g2s(st + blk * BLK_STRIDE + OFF_K, wsc + WS_KT + blk * 8192, 8192, fl);
+        for (int blk = 0; blk < 2; ++blk) {
+            uint8_t* dk = st + blk * BLK_STRIDE + OFF_K;
+            if (qk_ws) bulk_g2s(dk, wsc + WS_KT + blk * 8192, 8192, fl);
+            else tma_load_3d(dk, mkp, fl, blk * 64, t, zq);
+        }
         bulk_g2s(st + OFF_P, wsc + WS_P, 8192, fl);
         bulk_g2s(&scal[s], wsc + WS_CS, sizeof(CarryScalars), fl);
         issued = c + 1;
-        // chunk c + 2 goes to L2 now
+        // chunk c + 2 goes to L2 now (only the parts of the unit that were written)
         if (c + 2 < nch) {
-            for (int blk = 0; blk < Cfg::NB; ++blk)
-                tma_prefetch_l2_3d(&mv, n0 + blk * 64, tbase + (c + 2) * C, zv);
-            bulk_prefetch_l2(wsc + 2 * WS_UNIT, WS_UNIT);
+            const int t2 = t + 2 * C;
+            for (int blk = 0; blk < Cfg::NB; ++blk) tma_prefetch_l2_3d(mvp, n0 + blk * 64, t2, zv);
+            if (qk_ws) {
+                bulk_prefetch_l2(wsc + 2 * WS_UNIT, WS_UNIT);
+            } else {
+                for (int blk = 0; blk < 2; ++blk) {
+                    tma_prefetch_l2_3d(mqp, blk * 64, t2, zq);
+                    tma_prefetch_l2_3d(mkp, blk * 64, t2, zq);
+                }
+                bulk_prefetch_l2(wsc + 2 * WS_UNIT, WS_QT);
+                bulk_prefetch_l2(wsc + 2 * WS_UNIT + WS_CS, sizeof(CarryScalars));
+            }
         }
     }
     if (*abort_flag) {
@@ -984,7 +1013,8 @@ __device__ __forceinline__ void carry_produce(uint8_t* sm, uint64_t* bar, CarryS
 
 template <int NS>
 __global__ void __launch_bounds__(CARRY_THREADS, 1)
-    carry_tc_kernel(const __grid_constant__ CUtensorMap mv, TcArgs a) {
+    carry_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                    const __grid_constant__ CUtensorMap mv, TcArgs a) {
     using Cfg = CarryCfg<NS>;
     constexpr int CPT = Cfg::CPT, NP = CPT / 32;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -1038,8 +1068,9 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------- loads (one thread)
         if (lane == 0)
-            carry_produce<NS>(sm, bar, scal, &mv, a.ws + ws_offset(wb, h, u0, a.Hv, a.nseg), nch,
-                              n0, tbase, wb * a.Hv + h, abort_flag);
+            carry_produce<NS>(sm, bar, scal, &mq, &mk, &mv, true,
+                              a.ws + ws_offset(wb, h, u0, a.Hv, a.nseg), nch, n0, tbase,
+                              wb * a.Hk + h / (a.Hv / a.Hk), wb * a.Hv + h, abort_flag);
     } else if (warp == 2 || warp >= 4) {
         // ----------------------------------------- carry (warps 2, 4..11: 288 threads)
         const bool issuer = warp == 2;
@@ -1265,14 +1296,15 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
 // carry_t_kernel: one CTA per (value head, sequence) over all 128 state columns, with the
 // chunk recurrence written transposed, so that every operand the SIMT warps produce in a
 // chunk stays in tensor memory and enters the next MMA as its A operand:
-//   U~^T = V^T T_U^T,   (W S0)^T = S0^T W^T,   U^T = U~^T - (W S0)^T,
-//   dS^T = U^T K~,      S1^T = Gamma_last S0^T + dS^T,   O^T = S0^T Q~^T + U^T P^T.
+//   U~^T = V^T T_U^T,   [(W S0)^T | (Q S0)^T] = S0^T [W; Q]^T,   U^T = U~^T - (W S0)^T,
+//   U'^T = U^T diag(exp(gamma_last - gamma)),   dS^T = U'^T K,
+//   S1^T = Gamma_last S0^T + dS^T,   O^T = (Q S0)^T diag(Gamma) + U^T P^T.
 // TMEM lanes are the value columns v of the state, so the U step and the state update
 // run on all four SM sub-partitions, and no hand-off goes through shared memory.
 // Warp 0: producer (carry_produce<128>, both 64-column V blocks); warp 1 (one thread):
 // every MMA, in the order that keeps the tensor pipe free for the chain: dS^T(c), then
-// U~(c+1) (runs during the state update), then [W; Q~] S0 of chunk c+1, then U^T P^T(c)
-// (runs during the next U step); warps 2..9: SIMT,
+// U~(c+1) (runs during the state update), then [W; Q] S0 of chunk c+1 and U^T P^T(c)
+// (both complete before the next U step rewrites U^T); warps 2..9: SIMT,
 // warp (q = warp % 4, g = (warp - 2) / 4) owning lane v = 32 q + lane, fp32 state rows
 // 64 g .. 64 g + 63 (registers) and tokens 32 g .. 32 g + 31 of U and of the output.
 struct CarryT {
@@ -1283,10 +1315,10 @@ struct CarryT {
     static constexpr uint32_t SMEM = MISC + 64 + 1024;
     // TMEM (32-bit columns): per chunk parity p, from 192 p: U~^T (64) | (W S0)^T (64) |
     // O^T (64); once U is formed the state increment dS^T takes the first 128 columns.
-    // Then the bf16 operands S0^T (128 x 128: 64 columns) and, per parity, U^T (128 x 64:
-    // 32 columns; U^T P^T of a chunk still reads it during the next chunk's U step).
+    // Then the bf16 operands S0^T (128 x 128: 64 columns), U^T and U'^T (128 x 64: 32
+    // columns each).
     static constexpr uint32_t UB = 0, WSC = 64, OQ = 128, PSTRIDE = 192;
-    static constexpr uint32_t S0T = 384, UT = 448, TMCOLS = 512;  // U^T of parity p at UT + 32 p
+    static constexpr uint32_t S0T = 384, UT = 448, UPT = 480, TMCOLS = 512;
     static_assert(SCAL % 16 == 0 && BAR % 8 == 0, "alignment");
     static_assert(SMEM <= 232448, "shared memory budget");
 };
@@ -1295,7 +1327,7 @@ constexpr int CARRY_T_THREADS = 320;
 enum { T_ADONE = B_EMPTYL1 + 1, T_SDONE, T_ODONE0, T_ODONE1, T_DRAIN, T_COUNT };
 static_assert(T_COUNT * 8 <= 128, "barrier block");
 static_assert(CarryT::OQ == CarryT::WSC + 64 && OFF_Q == OFF_W + 8192,
-              "(W S0)^T and (Q~ S0)^T come from one 128-row operand into adjacent columns");
+              "(W S0)^T and (Q S0)^T come from one 128-row operand into adjacent columns");
 
 // U~^T = V^T T_U^T over the 64 tokens (V read M-major, T_U as K-major B), into `d`
 __device__ __forceinline__ void issue_t_u(uint32_t tmem, uint32_t st, uint32_t d) {
@@ -1306,7 +1338,7 @@ __device__ __forceinline__ void issue_t_u(uint32_t tmem, uint32_t st, uint32_t d
     for (int k = 0; k < 4; ++k) mma_bf16(tmem + d, dadd(av, k * 2048), dadd(bt, k * 32), id, k > 0);
 }
 
-// [(W S0)^T | (Q~ S0)^T] = S0^T [W; Q~]^T over Dk = 128 ([W_b; Q~_b] is one 128-row
+// [(W S0)^T | (Q S0)^T] = S0^T [W; Q]^T over Dk = 128 ([W_b; Q_b] is one 128-row
 // K-major operand per 64-column block), S0^T the A operand in TMEM; 128 columns at `d`
 __device__ __forceinline__ void issue_t_s0(uint32_t tmem, uint32_t d, uint32_t st) {
     constexpr uint32_t id = idesc_bf16(128, 128, false, false);
@@ -1318,7 +1350,7 @@ __device__ __forceinline__ void issue_t_s0(uint32_t tmem, uint32_t d, uint32_t s
     }
 }
 
-// dS^T = U^T K~ over the tokens (U^T in TMEM at `ut`, K~ read N-major), 128 columns at `d`
+// dS^T = U'^T K over the tokens (U'^T in TMEM at `ut`, K read N-major), 128 columns at `d`
 __device__ __forceinline__ void issue_t_ds(uint32_t tmem, uint32_t d, uint32_t ut, uint32_t st) {
     constexpr uint32_t id = idesc_bf16(128, 128, false, true);
     const uint64_t bk = smem_desc_sw128(st + OFF_K, BLK_STRIDE, 1024);
@@ -1327,7 +1359,7 @@ __device__ __forceinline__ void issue_t_ds(uint32_t tmem, uint32_t d, uint32_t u
         mma_bf16_ts(tmem + d, tmem + ut + 8u * (uint32_t)k, dadd(bk, k * 2048), id, k > 0);
 }
 
-// O^T += U^T P^T (U^T at `ut`, P as K-major B), onto (Q~ S0)^T at `d`
+// O^T += U^T P^T (U^T at `ut`, P as K-major B), onto (Q S0)^T diag(Gamma) at `d`
 __device__ __forceinline__ void issue_t_o(uint32_t tmem, uint32_t d, uint32_t ut, uint32_t st) {
     constexpr uint32_t id = idesc_bf16(128, 64, false, false);
     const uint64_t bp = smem_desc_sw128(st + OFF_P, 16, 1024);
@@ -1337,7 +1369,8 @@ __device__ __forceinline__ void issue_t_o(uint32_t tmem, uint32_t d, uint32_t ut
 }
 
 __global__ void __launch_bounds__(CARRY_T_THREADS, 1)
-    carry_t_kernel(const __grid_constant__ CUtensorMap mv, TcArgs a) {
+    carry_t_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                   const __grid_constant__ CUtensorMap mv, TcArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(sm);
@@ -1376,7 +1409,11 @@ __global__ void __launch_bounds__(CARRY_T_THREADS, 1)
         tmem_alloc(misc, CarryT::TMCOLS);
         tmem_relinquish();
     }
-    if (tid == 32) prefetch_tensormap(&mv);
+    if (tid == 32) {
+        prefetch_tensormap(&mq);
+        prefetch_tensormap(&mk);
+        prefetch_tensormap(&mv);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1384,8 +1421,9 @@ __global__ void __launch_bounds__(CARRY_T_THREADS, 1)
 
     if (warp == 0) {
         if (lane == 0)
-            carry_produce<128>(sm, bar, scal, &mv, a.ws + ws_offset(wb, h, u0, a.Hv, a.nseg), nch,
-                               0, tbase, zo, abort_flag);
+            carry_produce<128>(sm, bar, scal, &mq, &mk, &mv, false,
+                               a.ws + ws_offset(wb, h, u0, a.Hv, a.nseg), nch, 0, tbase,
+                               wb * a.Hk + h / (a.Hv / a.Hk), zo, abort_flag);
     } else {
         const bool issuer = warp == 1;
         const bool leader = issuer && lane == 0;
@@ -1429,17 +1467,14 @@ __global__ void __launch_bounds__(CARRY_T_THREADS, 1)
                       CarryT::PSTRIDE * (uint32_t)sc + CarryT::UB);
             return true;
         };
-        // [(W S0)^T | (Q~ S0)^T] of chunk cc from the state just published; its columns held
-        // dS^T and O^T of chunk cc-2, both read by now. The early group of chunk cc (also
-        // read by U~(cc), issued before) is then free.
+        // [(W S0)^T | (Q S0)^T] of chunk cc from the state just published; its columns held
+        // dS^T and O^T of chunk cc-2, both read by now
         auto issue_next_s0 = [&](int cc) {
             const int sc = cc & 1;
             TCLK(t12);
             tc_fence_after();
             issue_t_s0(tmem, CarryT::PSTRIDE * (uint32_t)sc + CarryT::WSC,
                        sbase + (uint32_t)sc * CarryT::STAGE);
-            tc_commit(&bar[T_ADONE]);
-            tc_commit(&bar[B_EMPTYE0 + sc]);
             TCLK(t3);
             TPUT(cc, 12, t12);
             TPUT(cc, 3, t3);
@@ -1466,19 +1501,23 @@ __global__ void __launch_bounds__(CARRY_T_THREADS, 1)
         if (leader) ok = issue_next_u(0);
         __syncwarp();
         bool stop = bar_any(4, 288, !ok || *abort_flag);
-        if (leader && !stop) issue_next_s0(0);
+        if (leader && !stop) {
+            issue_next_s0(0);
+            tc_commit(&bar[T_ADONE]);
+            tc_commit(&bar[B_EMPTYE0]);
+        }
         for (int c = 0; !stop && c < nch; ++c) {
             const int s = c & 1;
             const uint32_t pb = CarryT::PSTRIDE * (uint32_t)s;
-            const uint32_t ut = CarryT::UT + 32u * (uint32_t)s;
             const uint32_t st = sbase + (uint32_t)s * CarryT::STAGE;
             if (!issuer) {
-                // Gamma_last is read before barrier 3: the late group is reloaded only after
-                // U^T P^T of the chunk, issued after barrier 4
+                // the late group's scalars are read before barrier 4: it is reloaded only
+                // after U^T P^T of the chunk, issued after that barrier
                 ok = ok && wait_or_abort(&bar[B_FULLL0 + s], (c >> 1) & 1, abort_flag, ST_CARRY);
                 const float Gl = ok ? scal[s].Gl : 0.f;
-                // U^T = U~^T - (W S0)^T for tokens 32 g .. 32 g + 31; ADONE(c) also covers
-                // U~(c) and U^T P^T of chunk c-2, the last reader of this U^T buffer
+                // U^T = U~^T - (W S0)^T and U'^T = U^T diag(exp(gamma_last - gamma)) for
+                // tokens 32 g .. 32 g + 31; ADONE(c) also covers U~(c) and U^T P^T of chunk
+                // c-1, the last reader of U^T
                 ok = ok && wait_hot(&bar[T_ADONE], c & 1, abort_flag, ST_CARRY);
                 if (tid == 64) TRACE(c, 13);
                 if (ok) {
@@ -1486,19 +1525,45 @@ __global__ void __launch_bounds__(CARRY_T_THREADS, 1)
                     float ws[32], uv[32];
                     tmem_ld32x2(tmem + lo + pb + CarryT::WSC + 32u * (uint32_t)g,
                                 tmem + lo + pb + CarryT::UB + 32u * (uint32_t)g, ws, uv);
-                    uint32_t u[16];
+                    const float4* kd4 = reinterpret_cast<const float4*>(scal[s].kdec + 32 * g);
+                    uint32_t u[16], u2[16];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        u[j] = pack_bf16(uv[2 * j] - ws[2 * j], uv[2 * j + 1] - ws[2 * j + 1]);
-                    tmem_st16u(tmem + lo + ut + 16u * (uint32_t)g, u);
+                    for (int j = 0; j < 8; ++j) {
+                        const float4 kd = kd4[j];
+                        const float d0 = uv[4 * j] - ws[4 * j], d1 = uv[4 * j + 1] - ws[4 * j + 1];
+                        const float d2 = uv[4 * j + 2] - ws[4 * j + 2];
+                        const float d3 = uv[4 * j + 3] - ws[4 * j + 3];
+                        u[2 * j] = pack_bf16(d0, d1);
+                        u[2 * j + 1] = pack_bf16(d2, d3);
+                        u2[2 * j] = pack_bf16(kd.x * d0, kd.y * d1);
+                        u2[2 * j + 1] = pack_bf16(kd.z * d2, kd.w * d3);
+                    }
+                    tmem_st16u(tmem + lo + CarryT::UT + 16u * (uint32_t)g, u);
+                    tmem_st16u(tmem + lo + CarryT::UPT + 16u * (uint32_t)g, u2);
                     tmem_wait_st();
                 }
                 if (lane == 0) TRACE(c, 20 + (warp - 2));
                 tc_fence_before();
                 __syncwarp();
                 bar_arrive(3, 288);
-                // the output of chunk c-1 (its U^T P^T ran during this U step) while dS^T(c)
-                // runs
+                // while dS^T(c) runs: (Q S0)^T(c) diag(Gamma) in place, before U^T P^T(c)
+                // accumulates onto it after barrier 4, and the output of chunk c-1
+                if (ok) {
+                    const uint32_t oq = tmem + lo + pb + CarryT::OQ + 32u * (uint32_t)g;
+                    const float4* gm4 = reinterpret_cast<const float4*>(scal[s].Gam + 32 * g);
+                    float o[32];
+                    tmem_ld32(oq, o);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float4 gm = gm4[j];
+                        o[4 * j] *= gm.x;
+                        o[4 * j + 1] *= gm.y;
+                        o[4 * j + 2] *= gm.z;
+                        o[4 * j + 3] *= gm.w;
+                    }
+                    tmem_st32(oq, o);
+                    tmem_wait_st();
+                }
                 if (c > 0) {
                     ok = ok && wait_hot(&bar[T_ODONE0 + (s ^ 1)], ((c - 1) >> 1) & 1, abort_flag,
                                         ST_CARRY);
@@ -1538,7 +1603,7 @@ __global__ void __launch_bounds__(CARRY_T_THREADS, 1)
                     if (ok) {
                         TCLK(t14);
                         tc_fence_after();
-                        issue_t_ds(tmem, pb, ut, st);
+                        issue_t_ds(tmem, pb, CarryT::UPT, st);
                         tc_commit(&bar[T_SDONE]);
                         TCLK(t9);
                         TPUT(c, 14, t14);
@@ -1553,12 +1618,17 @@ __global__ void __launch_bounds__(CARRY_T_THREADS, 1)
             stop = bar_any(4, 288, !ok || *abort_flag);
             if (stop) break;
             if (leader) {
+                // [W; Q] S0 of chunk c+1, then O^T(c) += U^T P^T behind it in the pipe; the
+                // next ADONE covers both, so the next U step finds U^T free
                 if (c + 1 < nch) issue_next_s0(c + 1);
-                // O^T(c) += U^T P^T, behind [W; Q~] S0 of chunk c+1 in the pipe
                 TCLK(t4);
-                issue_t_o(tmem, pb + CarryT::OQ, ut, st);
+                issue_t_o(tmem, pb + CarryT::OQ, CarryT::UT, st);
+                if (c + 1 < nch) {
+                    tc_commit(&bar[T_ADONE]);
+                    tc_commit(&bar[B_EMPTYE0 + (s ^ 1)]);  // W, Q, V, T_U of chunk c+1 are read
+                }
                 tc_commit(&bar[T_ODONE0 + s]);
-                tc_commit(&bar[B_EMPTYL0 + s]);  // K~, P, scalars of chunk c are read
+                tc_commit(&bar[B_EMPTYL0 + s]);  // K, P, scalars of chunk c are read
                 TPUT(c, 4, t4);
             }
             __syncwarp();
@@ -1725,7 +1795,8 @@ struct SegmentLaunch {
         const int sin = (c0 > 0 || a->state_is_input) ? 1 : 0;
         return TcArgs{a->g,     a->beta, a->scale, a->B, a->Hk,  a->Hv,
                       a->S,     c0,      nseg,     a->state, sin,
-                      static_cast<__nv_bfloat16*>(a->out), ws, a->cu_seqlens, a->table, a->N};
+                      static_cast<__nv_bfloat16*>(a->out), ws, a->cu_seqlens, a->table, a->N,
+                      split() ? 1 : 0};
     }
     // sequences of the carry grid: the batch, or the variable-length batch's sequences
     int rows() const { return a->cu_seqlens ? a->N : a->B; }
@@ -1742,10 +1813,10 @@ struct SegmentLaunch {
         if (split())
             carry_tc_kernel<64>
                 <<<dim3(2, a->Hv, rows()), CARRY_THREADS, CarryCfg<64>::SMEM, st>>>(
-                    mv, args(c0, nseg, ws));
+                    mq, mk, mv, args(c0, nseg, ws));
         else
             carry_t_kernel<<<dim3(1, a->Hv, rows()), CARRY_T_THREADS, CarryT::SMEM, st>>>(
-                mv, args(c0, nseg, ws));
+                mq, mk, mv, args(c0, nseg, ws));
         return cudaGetLastError();
     }
 };

@@ -68,10 +68,10 @@ def test_prefill_rejects_bad_arguments(lib, kw, msg):
 
 def test_workspace_query(lib):
     assert lib.gdn_prefill_workspace_bytes(1, 3, 4, 64, 128, 128, 1) == ctypes.c_size_t(-1).value
-    # tensor-core path: 66560 bytes per (batch, value head, 64-token chunk), ragged tail
+    # tensor-core path: 66064 bytes per (batch, value head, 64-token chunk), ragged tail
     # rounded up; the fp32 and other-head-dim paths need none
-    assert lib.gdn_prefill_workspace_bytes(1, 16, 32, 8192, 128, 128, 1) == 32 * 128 * 66560
-    assert lib.gdn_prefill_workspace_bytes(2, 1, 3, 65, 128, 128, 1) == 2 * 3 * 2 * 66560
+    assert lib.gdn_prefill_workspace_bytes(1, 16, 32, 8192, 128, 128, 1) == 32 * 128 * 66064
+    assert lib.gdn_prefill_workspace_bytes(2, 1, 3, 65, 128, 128, 1) == 2 * 3 * 2 * 66064
     assert lib.gdn_prefill_workspace_bytes(1, 16, 32, 8192, 128, 128, 0) == 0
     assert lib.gdn_prefill_workspace_bytes(1, 16, 32, 8192, 64, 128, 1) == 0
 
@@ -147,9 +147,9 @@ def test_conv1d_rejects_bad_arguments(lib, kw, msg):
 
 
 def test_varlen_workspace_query(lib):
-    # tensor-core path: Hv * (ceil(T/64) + N) units of 66560 bytes (to 256), then the
+    # tensor-core path: Hv * (ceil(T/64) + N) units of 66064 bytes (to 256), then the
     # N + 2 ints of the chunk table; fp32 / other head dims: the table alone (to 16)
-    units = 32 * (4096 // 64 + 5) * 66560
+    units = 32 * (4096 // 64 + 5) * 66064
     assert lib.gdn_prefill_varlen_workspace_bytes(5, 16, 32, 4096, 128, 128, 1) == \
         (units + 255) // 256 * 256 + 4 * 7
     assert lib.gdn_prefill_varlen_workspace_bytes(5, 2, 2, 100, 64, 64, 0) == 32
