@@ -86,15 +86,15 @@ constexpr uint32_t kStatusBadSeqlens = 16u;
 // B * Hv * nseg units; the state carries over between consecutive calls.
 cudaError_t launch_prefill_tc(const PrefillArgs& a, int c0, int nseg, cudaStream_t stream,
                               int* launched);
-// The whole sequence with a workspace of B * Hv * ceil(S / 64) units, in
-// prefill_tc_segments(...) segments when the carry leaves SMs free (the first one of
-// prefill_tc_segment_chunks(...) chunks, the others sharing the rest): the prep of
-// segment j + 1 (helper stream, low priority) then runs beside the carry of segment j
-// (helper stream, high priority), forked from and joined back to `stream` by events.
+// The whole sequence with a workspace of B * Hv * ceil(S / 64) units, in the segments
+// prefill_tc_schedule(...) gives when the carry leaves SMs free: the prep of segment j + 1
+// (helper stream, low priority) then runs beside the carry of segment j (helper stream,
+// high priority), forked from and joined back to `stream` by events.
 cudaError_t launch_prefill_tc_overlapped(const PrefillArgs& a, cudaStream_t stream,
                                          int* launched);
-int prefill_tc_segments(int B, int Hv, int nch, int sms);
-int prefill_tc_segment_chunks(int B, int Hv, int nch, int sms);
+// Segment sizes (chunks) of the overlapped schedule into sizes[0 .. n-1]; returns n (at
+// most max_segments, 1 when the carry leaves too few SMs free or there are few chunks).
+int prefill_tc_schedule(int B, int Hv, int nch, int sms, int* sizes, int max_segments);
 
 // Depthwise causal conv1d decode token + silu + window shift, split into q | k | v with
 // q and k repeated over the value heads.

@@ -116,19 +116,26 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 
 // Overlapped schedule (the prep of the next segment of the sequence runs beside the carry
 // of the current one): at most this many segments, of at least kMinSegmentChunks chunks.
+// The prep of a segment on the SMs the carry leaves (88 of 152 for 64 carry CTAs) runs
+// about 1.22x faster per chunk than the carry, so each segment can be that much longer
+// than the one before, and the exposed prep of the first one shrinks as segments are
+// added (45% of the chunks for two segments, 27% for three, 18% for four).
 #ifndef GDN_OVERLAP_SEGMENTS
 #define GDN_OVERLAP_SEGMENTS 2
 #endif
+#ifndef GDN_SEGMENT_GROWTH_PERMILLE
+#define GDN_SEGMENT_GROWTH_PERMILLE 1220
+#endif
 constexpr int kOverlapSegments = GDN_OVERLAP_SEGMENTS;
 constexpr int kMinSegmentChunks = 8;
-// Share (per mille) of the chunks in the first segment: its prep is exposed, the others
-// run beside the carry of the segment before. The prep of the rest on the SMs the carry
-// leaves (88 of 152 for 64 carry CTAs) takes about as long as the carry of the first
-// when the first holds ~45%.
-#ifndef GDN_FIRST_SEGMENT_PERMILLE
-#define GDN_FIRST_SEGMENT_PERMILLE 450
+constexpr int kSegmentGrowthPermille = GDN_SEGMENT_GROWTH_PERMILLE;
+// 1: a carry segment is launched as a programmatic dependent of the one before it, so its
+// setup overlaps that one's last chunks (the state is read after griddepcontrol.wait).
+#ifndef GDN_CARRY_PDL
+#define GDN_CARRY_PDL 1
 #endif
-constexpr int kFirstSegmentPermille = GDN_FIRST_SEGMENT_PERMILLE;
+constexpr bool kCarryPdl = GDN_CARRY_PDL != 0;
+constexpr int kMaxSegments = 8;
 // Carry form while two CTAs per head fit the GPU: 1 = two 64-column state slices per head
 // (carry_tc_kernel<64>), 0 = one transposed CTA per head (carry_t_kernel).
 #ifndef GDN_CARRY_SPLIT
@@ -1043,6 +1050,7 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
     }
     if (nch == 0) {
         // an empty sequence: the state passes through (zero when none was supplied)
+        grid_dep_wait();
         if (!a.state_is_input)
             for (int i = tid; i < 128 * NS; i += CARRY_THREADS)
                 a.state[((size_t)sb * 128 + i / NS) * 128 + n0 + i % NS] = 0.f;
@@ -1067,10 +1075,14 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
 
     if (warp == 0) {
         // ------------------------------------------------- loads (one thread)
-        if (lane == 0)
+        if (lane == 0) {
             carry_produce<NS>(sm, bar, scal, &mq, &mk, &mv, true,
                               a.ws + ws_offset(wb, h, u0, a.Hv, a.nseg), nch, n0, tbase,
                               wb * a.Hk + h / (a.Hv / a.Hk), wb * a.Hv + h, abort_flag);
+            // every load is issued (the last chunks are in flight): a dependent carry
+            // segment may start its setup
+            grid_dep_launch_dependents();
+        }
     } else if (warp == 2 || warp >= 4) {
         // ----------------------------------------- carry (warps 2, 4..11: 288 threads)
         const bool issuer = warp == 2;
@@ -1089,6 +1101,7 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
         // the fp32 state: row L, columns col0 .. col0 + CPT - 1 of the slice, in registers
         float Sr[CPT];
         if (!issuer) {
+            grid_dep_wait();  // the carry of the segment before wrote this state
             if (a.state_is_input) {
 #pragma unroll
                 for (int j = 0; j < CPT; j += 4) {
@@ -1393,6 +1406,7 @@ __global__ void __launch_bounds__(CARRY_T_THREADS, 1)
         sb = n * a.Hv + h;
     }
     if (nch == 0) {
+        grid_dep_wait();
         if (!a.state_is_input)
             for (int i = tid; i < 128 * 128; i += CARRY_T_THREADS)
                 a.state[(size_t)sb * 128 * 128 + i] = 0.f;
@@ -1420,10 +1434,12 @@ __global__ void __launch_bounds__(CARRY_T_THREADS, 1)
     const uint32_t tmem = misc[0];
 
     if (warp == 0) {
-        if (lane == 0)
+        if (lane == 0) {
             carry_produce<128>(sm, bar, scal, &mq, &mk, &mv, false,
                                a.ws + ws_offset(wb, h, u0, a.Hv, a.nseg), nch, 0, tbase,
                                wb * a.Hk + h / (a.Hv / a.Hk), zo, abort_flag);
+            grid_dep_launch_dependents();  // as in carry_tc_kernel
+        }
     } else {
         const bool issuer = warp == 1;
         const bool leader = issuer && lane == 0;
@@ -1486,6 +1502,7 @@ __global__ void __launch_bounds__(CARRY_T_THREADS, 1)
         // so the group leaves the loop as one). Every participant reaches both barriers in
         // every chunk: a failed wait only skips work.
         if (!issuer) {
+            grid_dep_wait();  // the carry of the segment before wrote this state
             if (a.state_is_input) {
 #pragma unroll
                 for (int i = 0; i < 64; ++i) Sr[i] = gst[(size_t)i * 128];
@@ -1809,15 +1826,27 @@ struct SegmentLaunch {
             mq, mk, args(c0, nseg, ws));
         return cudaGetLastError();
     }
-    cudaError_t carry(int c0, int nseg, uint8_t* ws, cudaStream_t st) const {
-        if (split())
-            carry_tc_kernel<64>
-                <<<dim3(2, a->Hv, rows()), CARRY_THREADS, CarryCfg<64>::SMEM, st>>>(
-                    mq, mk, mv, args(c0, nseg, ws));
-        else
-            carry_t_kernel<<<dim3(1, a->Hv, rows()), CARRY_T_THREADS, CarryT::SMEM, st>>>(
-                mq, mk, mv, args(c0, nseg, ws));
-        return cudaGetLastError();
+    // pdl: launched as a programmatic dependent of the previous kernel in `st` (the carry
+    // of the segment before), which lets its setup run before that one ends
+    cudaError_t carry(int c0, int nseg, uint8_t* ws, cudaStream_t st, bool pdl = false) const {
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.stream = st;
+        cfg.attrs = attr;
+        cfg.numAttrs = pdl ? 1 : 0;
+        const TcArgs ta = args(c0, nseg, ws);
+        if (split()) {
+            cfg.gridDim = dim3(2, a->Hv, rows());
+            cfg.blockDim = dim3(CARRY_THREADS);
+            cfg.dynamicSmemBytes = CarryCfg<64>::SMEM;
+            return cudaLaunchKernelEx(&cfg, carry_tc_kernel<64>, mq, mk, mv, ta);
+        }
+        cfg.gridDim = dim3(1, a->Hv, rows());
+        cfg.blockDim = dim3(CARRY_T_THREADS);
+        cfg.dynamicSmemBytes = CarryT::SMEM;
+        return cudaLaunchKernelEx(&cfg, carry_t_kernel, mq, mk, mv, ta);
     }
 };
 
@@ -1882,20 +1911,32 @@ cudaError_t prepare(SegmentLaunch& L, const PrefillArgs& a) {
 
 }  // namespace
 
-int prefill_tc_segments(int B, int Hv, int nch, int sms) {
-    // The carry of a segment occupies 2 B Hv SMs (one CTA each) for the whole segment;
-    // the prep of the next segment runs meanwhile on the SMs left over. Without enough
-    // of those, or with too few chunks, one segment.
+int prefill_tc_schedule(int B, int Hv, int nch, int sms, int* sizes, int max_segments) {
+    // The carry of a segment occupies B Hv or 2 B Hv SMs (one CTA each) for the whole
+    // segment; the prep of the next segment runs meanwhile on the SMs left over. Without
+    // enough of those, or with too few chunks, one segment.
     const int carry_sms = (kCarrySplit && 2 * B * Hv <= sms ? 2 : 1) * B * Hv;
-    if (carry_sms > sms || sms - carry_sms < sms / 4 || nch < 2 * kMinSegmentChunks) return 1;
-    return std::max(1, std::min(kOverlapSegments, nch / kMinSegmentChunks));
-}
-
-int prefill_tc_segment_chunks(int B, int Hv, int nch, int sms) {
-    const int g = prefill_tc_segments(B, Hv, nch, sms);
-    if (g == 1) return nch;
-    const int first = (int)(((long)nch * kFirstSegmentPermille + 500) / 1000);
-    return std::max(kMinSegmentChunks, std::min(first, nch - kMinSegmentChunks * (g - 1)));
+    int g = std::min(std::min(kOverlapSegments, max_segments), nch / kMinSegmentChunks);
+    if (carry_sms > sms || sms - carry_sms < sms / 4 || g < 2) g = 1;
+    if (g == 1) {
+        sizes[0] = nch;
+        return 1;
+    }
+    // sizes s_k = s_1 r^k, sum nch: s_1 = nch (r - 1) / (r^g - 1)
+    const double r = kSegmentGrowthPermille / 1000.0;
+    double rg = 1.0;
+    for (int k = 0; k < g; ++k) rg *= r;
+    const double s1 = (double)nch * (r - 1.0) / (rg - 1.0);
+    int used = 0;
+    double x = s1;
+    for (int k = 0; k < g; ++k, x *= r) {
+        const int left = g - 1 - k;  // segments after this one
+        int n = k == g - 1 ? nch - used : (int)(x + 0.5);
+        n = std::max(kMinSegmentChunks, std::min(n, nch - used - left * kMinSegmentChunks));
+        sizes[k] = n;
+        used += n;
+    }
+    return g;
 }
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a, int c0, int nseg, cudaStream_t stream,
@@ -1953,13 +1994,11 @@ cudaError_t launch_prefill_tc_overlapped(const PrefillArgs& a, cudaStream_t stre
     if (e != cudaSuccess) return e;
     int dev = 0;
     cudaGetDevice(&dev);
-    const int seg = prefill_tc_segment_chunks(a.B, a.Hv, nch, L.sms);
-    const int g = prefill_tc_segments(a.B, a.Hv, nch, L.sms);
-    // the first segment is `seg` chunks, the others share the rest evenly
-    const int rest = g > 1 ? (nch - seg + g - 2) / (g - 1) : 0;
+    int sizes[kMaxSegments];
+    const int g = prefill_tc_schedule(a.B, a.Hv, nch, L.sms, sizes, kMaxSegments);
     Overlap* o = overlap_for(dev);
     uint8_t* ws = static_cast<uint8_t*>(a.workspace);
-    if (seg >= nch || o == nullptr) {
+    if (g == 1 || o == nullptr) {
         e = L.prep(0, nch, ws, stream);
         if (e != cudaSuccess) return e;
         *launched = 1;
@@ -1978,15 +2017,16 @@ cudaError_t launch_prefill_tc_overlapped(const PrefillArgs& a, cudaStream_t stre
     // prep of segment j+1 overlaps the carry of segment j; each carry waits for its prep
     // (a wait takes the event's latest record at the time it is enqueued)
     cudaError_t le = cudaSuccess;
-    for (int c0 = 0, n = 0; c0 < nch && le == cudaSuccess; c0 += n) {
-        n = c0 == 0 ? seg : std::min(rest, nch - c0);
+    for (int j = 0, c0 = 0; j < g && le == cudaSuccess; c0 += sizes[j], ++j) {
+        const int n = sizes[j];
         uint8_t* wsj = ws + (size_t)a.B * (size_t)a.Hv * (size_t)c0 * WS_UNIT;
         le = L.prep(c0, n, wsj, o->prep);
         if (le != cudaSuccess) break;
         ++*launched;
         le = cudaEventRecord(o->prepped, o->prep);
         if (le == cudaSuccess) le = cudaStreamWaitEvent(o->carry, o->prepped, 0);
-        if (le == cudaSuccess) le = L.carry(c0, n, wsj, o->carry);
+        // segments after the first are programmatic dependents of the carry before them
+        if (le == cudaSuccess) le = L.carry(c0, n, wsj, o->carry, kCarryPdl && j > 0);
         if (le == cudaSuccess) ++*launched;
     }
     // join, also after a failed launch, so that no work is left outside the caller's stream

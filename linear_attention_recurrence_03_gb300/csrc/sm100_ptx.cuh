@@ -179,6 +179,21 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes
                  : "memory");
 }
 
+// ------------------------------------------------------------------------ grid dependencies
+
+// Programmatic dependent launch: waits until the grids this one depends on have completed
+// and their memory operations are visible (a no-op for a grid launched without the
+// dependency attribute).
+__device__ __forceinline__ void grid_dep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the grids that depend on this one launch once every CTA of it has signalled (or
+// exited); they still wait for its completion in grid_dep_wait().
+__device__ __forceinline__ void grid_dep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------------ TMEM
 
 // Whole warp: allocates `ncols` (power of two >= 32) TMEM columns; the base address is
