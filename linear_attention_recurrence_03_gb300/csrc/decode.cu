@@ -30,14 +30,17 @@ constexpr int NT = 256;
 constexpr int NWARP = NT / 32;
 constexpr int ROWS = kMaxHeadDim / NWARP;  // 16 state rows per warp at most
 
+// TG: tokens whose inputs are staged together (1 for a single step, NWARP otherwise)
+template <int TG>
 struct Smem {
-    float qn[kMaxHeadDim];
-    float kn[kMaxHeadDim];
-    float v[kMaxHeadDim];
-    float z[kMaxHeadDim];
+    // inputs of up to TG tokens: q^, k^ (normalised in place), v, z
+    float qn[TG][kMaxHeadDim];
+    float kn[TG][kMaxHeadDim];
+    float v[TG][kMaxHeadDim];
+    float z[TG][kMaxHeadDim];
     float u[kMaxHeadDim];
     float red[2][NWARP][kMaxHeadDim];
-    float scal[8];  // 0: 1/|q|, 1: 1/|k|, 2: k^.q^, 3: beta, 4: alpha, 5: 1/rms
+    float scal[TG][5];  // 0: k^.q^, 1: beta, 2: alpha, 3: 1/|q|, 4: 1/|k|
     float part[NWARP];
 };
 
@@ -57,9 +60,9 @@ __device__ __forceinline__ int col_of(int lane, int c) {
     return VEC4 ? 4 * lane + c : lane + 32 * c;
 }
 
-template <bool VEC4>
+template <bool VEC4, int TG>
 __global__ void __launch_bounds__(NT, 2) decode_kernel(DecodeArgs a) {
-    __shared__ Smem s;
+    __shared__ Smem<TG> s;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int bh = blockIdx.x, h = bh % a.H;
     const int K = a.K, V = a.V;
@@ -85,117 +88,119 @@ __global__ void __launch_bounds__(NT, 2) decode_kernel(DecodeArgs a) {
         }
     }
 
-    // 2. small per-row inputs, token by token; thread i < 128 holds element i of the
-    // next token's q, k, v, z (and thread 0 its b, a) in registers, loaded one token
-    // ahead so that their latency hides behind the current token
-    float nq = 0.f, nk = 0.f, nv = 0.f, nz = 0.f, nb = 0.f, na = 0.f;
-    auto fetch = [&](int tok) {
-        const size_t row = (size_t)tok * BH + (size_t)bh;
-        if (tid < kMaxHeadDim) {
-            nq = tid < K ? __bfloat162float(a.q[row * K + tid]) : 0.f;
-            nk = tid < K ? __bfloat162float(a.k[row * K + tid]) : 0.f;
-            nv = tid < V ? __bfloat162float(a.v[row * V + tid]) : 0.f;
-            nz = tid < V ? __bfloat162float(a.z[row * V + tid]) : 0.f;
+    // 2. the inputs of TG tokens at a time, staged in shared memory and turned into q^, k^,
+    // k^.q^, beta and alpha (none of it depends on the state); each token then needs two
+    // barriers
+    for (int t0 = 0; t0 < a.T; t0 += TG) {
+        const int nt = min(TG, a.T - t0);
+        if (t0 > 0) __syncthreads();  // the previous group's inputs are read
+        for (int e = tid; e < nt * kMaxHeadDim; e += NT) {
+            const int t = e / kMaxHeadDim, i = e % kMaxHeadDim;
+            const size_t row = (size_t)(t0 + t) * BH + (size_t)bh;
+            s.qn[t][i] = i < K ? __bfloat162float(a.q[row * K + i]) : 0.f;
+            s.kn[t][i] = i < K ? __bfloat162float(a.k[row * K + i]) : 0.f;
+            s.v[t][i] = i < V ? __bfloat162float(a.v[row * V + i]) : 0.f;
+            s.z[t][i] = i < V ? __bfloat162float(a.z[row * V + i]) : 0.f;
         }
-        if (tid == 0) {
-            nb = __bfloat162float(a.b[row]);
-            na = __bfloat162float(a.a[row]);
+        __syncthreads();
+        // l2 norms: job j = 2 t + (0: q, 1: k) on warp j mod NWARP (each sum in
+        // lane-strided order); beta and alpha of token t on lane 0 of warp (2 nt + t) mod
+        // NWARP, so that one token's work spreads over three warps
+        for (int j = w; j < 2 * nt; j += NWARP) {
+            const int t = j >> 1;
+            const float* x = (j & 1) ? s.kn[t] : s.qn[t];
+            float acc = 0.f;
+            for (int i = lane; i < kMaxHeadDim; i += 32) acc = fmaf(x[i], x[i], acc);
+            acc = warp_sum(acc);
+            if (lane == 0) s.scal[t][3 + (j & 1)] = 1.f / sqrtf(acc + kEpsL2);
         }
-    };
-    fetch(0);
-    for (int tok = 0; tok < a.T; ++tok) {
-    if (tok > 0) __syncthreads();  // the previous token's shared inputs are read
-    const size_t row = (size_t)tok * BH + (size_t)bh;  // this token's input row
-    if (tid < kMaxHeadDim) {
-        s.qn[tid] = nq;
-        s.kn[tid] = nk;
-        s.v[tid] = nv;
-        s.z[tid] = nz;
-    }
-    if (tid == 0) {
-        s.scal[3] = sigmoid_f(nb);
-        const float gg = -expf(a.A_log[h]) * softplus_f(na + a.dt_bias[h]);
-        s.scal[4] = expf(gg);
-    }
-    if (tok + 1 < a.T) fetch(tok + 1);
-    __syncthreads();
-    // 3. l2 norms of q and k (warps 0 and 1), then normalise
-    if (w < 2) {
-        const float* x = (w == 0) ? s.qn : s.kn;
-        float acc = 0.f;
-        for (int i = lane; i < kMaxHeadDim; i += 32) acc = fmaf(x[i], x[i], acc);
-        acc = warp_sum(acc);
-        if (lane == 0) s.scal[w] = 1.f / sqrtf(acc + kEpsL2);
-    }
-    __syncthreads();
-    for (int i = tid; i < kMaxHeadDim; i += NT) {
-        s.qn[i] *= s.scal[0];
-        s.kn[i] *= s.scal[1];
-    }
-    __syncthreads();
-    if (w == 0) {
-        float acc = 0.f;
-        for (int i = lane; i < kMaxHeadDim; i += 32) acc = fmaf(s.kn[i], s.qn[i], acc);
-        acc = warp_sum(acc);
-        if (lane == 0) s.scal[2] = acc;
-    }
-    // 4. per-warp partial x = S^T k^ and y = S^T q^ over this warp's rows
-    {
-        float px[4] = {0.f, 0.f, 0.f, 0.f}, py[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int m = 0; m < ROWS; ++m) {
-            const int i = w + NWARP * m;
-            const float ki = s.kn[i], qi = s.qn[i];  // zero beyond K
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                px[c] = fmaf(ki, st[m][c], px[c]);
-                py[c] = fmaf(qi, st[m][c], py[c]);
+        if (lane == 0) {
+            for (int t = 0; t < nt; ++t) {
+                if ((2 * nt + t) % NWARP != w) continue;
+                const size_t row = (size_t)(t0 + t) * BH + (size_t)bh;
+                s.scal[t][1] = sigmoid_f(__bfloat162float(a.b[row]));
+                const float gg = -expf(a.A_log[h]) *
+                                 softplus_f(__bfloat162float(a.a[row]) + a.dt_bias[h]);
+                s.scal[t][2] = expf(gg);
             }
         }
+        __syncthreads();
+        for (int e = tid; e < nt * kMaxHeadDim; e += NT) {
+            const int t = e / kMaxHeadDim, i = e % kMaxHeadDim;
+            s.qn[t][i] *= s.scal[t][3];
+            s.kn[t][i] *= s.scal[t][4];
+        }
+        __syncthreads();
+        // k^.q^ of token t on warp t (read after the first barrier of the token loop)
+        if (w < nt) {
+            float acc = 0.f;
+            for (int i = lane; i < kMaxHeadDim; i += 32) acc = fmaf(s.kn[w][i], s.qn[w][i], acc);
+            acc = warp_sum(acc);
+            if (lane == 0) s.scal[w][0] = acc;
+        }
+        for (int t = 0; t < nt; ++t) {
+            const size_t row = (size_t)(t0 + t) * BH + (size_t)bh;  // this token's row
+            // 3. per-warp partial x = S^T k^ and y = S^T q^ over this warp's rows
+            {
+                float px[4] = {0.f, 0.f, 0.f, 0.f}, py[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const int j = col_of<VEC4>(lane, c);
-            s.red[0][w][j] = px[c];
-            s.red[1][w][j] = py[c];
+                for (int m = 0; m < ROWS; ++m) {
+                    const int i = w + NWARP * m;
+                    const float ki = s.kn[t][i], qi = s.qn[t][i];  // zero beyond K
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        px[c] = fmaf(ki, st[m][c], px[c]);
+                        py[c] = fmaf(qi, st[m][c], py[c]);
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int j = col_of<VEC4>(lane, c);
+                    s.red[0][w][j] = px[c];
+                    s.red[1][w][j] = py[c];
+                }
+            }
+            __syncthreads();
+            // 4. u = beta (v - alpha x); o = (alpha y + u (k^.q^)) / sqrt(K)
+            const float kq = s.scal[t][0], beta = s.scal[t][1], alpha = s.scal[t][2];
+            float o = 0.f;
+            if (tid < kMaxHeadDim) {
+                const int j = tid;
+                float x = 0.f, y = 0.f;
+#pragma unroll
+                for (int ww = 0; ww < NWARP; ++ww) { x += s.red[0][ww][j]; y += s.red[1][ww][j]; }
+                const float u = (j < V) ? beta * (s.v[t][j] - alpha * x) : 0.f;
+                s.u[j] = u;
+                o = (j < V) ? (alpha * y + u * kq) / sqrtf((float)K) : 0.f;
+                const float sq = warp_sum(o * o);
+                if (lane == 0) s.part[w] = sq;
+            }
+            __syncthreads();
+            // 5. RMSNormGated epilogue (threads 0..V-1), bf16 out
+            if (tid < V) {
+                float ms = 0.f;
+#pragma unroll
+                for (int ww = 0; ww < kMaxHeadDim / 32; ++ww) ms += s.part[ww];
+                ms /= (float)V;
+                const float zj = s.z[t][tid];
+                const float y =
+                    o * (1.f / sqrtf(ms + kEpsRms)) * a.norm_weight[tid] * (zj * sigmoid_f(zj));
+                a.out[row * V + tid] = __float2bfloat16_rn(y);
+            }
+            // 6. S' = alpha S + k^ u^T in registers (rows beyond K stay zero). The next
+            // token's partials overwrite s.red only after this thread's reads of s.u and
+            // s.part, and its u after the next barrier.
+#pragma unroll
+            for (int m = 0; m < ROWS; ++m) {
+                const int i = w + NWARP * m;
+                const float ki = s.kn[t][i];  // zero beyond K
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    st[m][c] = fmaf(alpha, st[m][c], ki * s.u[col_of<VEC4>(lane, c)]);
+            }
         }
     }
-    __syncthreads();
-    // 5. u = beta (v - alpha x); o = (alpha y + u (k^.q^)) / sqrt(K)
-    const float beta = s.scal[3], alpha = s.scal[4];
-    float o = 0.f;
-    if (tid < kMaxHeadDim) {
-        const int j = tid;
-        float x = 0.f, y = 0.f;
-#pragma unroll
-        for (int ww = 0; ww < NWARP; ++ww) { x += s.red[0][ww][j]; y += s.red[1][ww][j]; }
-        const float u = (j < V) ? beta * (s.v[j] - alpha * x) : 0.f;
-        s.u[j] = u;
-        o = (j < V) ? (alpha * y + u * s.scal[2]) / sqrtf((float)K) : 0.f;
-        const float sq = warp_sum(o * o);
-        if (lane == 0) s.part[w] = sq;
-    }
-    __syncthreads();
-    // 6. RMSNormGated epilogue (threads 0..V-1), bf16 out
-    if (tid < V) {
-        float ms = 0.f;
-#pragma unroll
-        for (int ww = 0; ww < kMaxHeadDim / 32; ++ww) ms += s.part[ww];
-        ms /= (float)V;
-        const float zj = s.z[tid];
-        const float y = o * (1.f / sqrtf(ms + kEpsRms)) * a.norm_weight[tid] * (zj * sigmoid_f(zj));
-        a.out[row * V + tid] = __float2bfloat16_rn(y);
-    }
-    // 7. S' = alpha S + k^ u^T in registers (rows beyond K stay zero)
-#pragma unroll
-    for (int m = 0; m < ROWS; ++m) {
-        const int i = w + NWARP * m;
-        const float ki = s.kn[i];  // zero beyond K
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-            st[m][c] = fmaf(alpha, st[m][c], ki * s.u[col_of<VEC4>(lane, c)]);
-    }
-    }  // tokens
-    // 8. the state, written once
+    // 7. the state, written once
 #pragma unroll
     for (int m = 0; m < ROWS; ++m) {
         const int i = w + NWARP * m;
@@ -217,10 +222,15 @@ __global__ void __launch_bounds__(NT, 2) decode_kernel(DecodeArgs a) {
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     if (a.BH == 0 || a.T == 0) return cudaSuccess;
-    if (a.V == kMaxHeadDim)
-        decode_kernel<true><<<a.BH, NT, 0, stream>>>(a);
-    else
-        decode_kernel<false><<<a.BH, NT, 0, stream>>>(a);
+    // a single step stages one token's inputs (the smaller footprint keeps the streaming
+    // step at its bandwidth); several tokens are staged NWARP at a time
+    if (a.V == kMaxHeadDim) {
+        if (a.T == 1) decode_kernel<true, 1><<<a.BH, NT, 0, stream>>>(a);
+        else decode_kernel<true, NWARP><<<a.BH, NT, 0, stream>>>(a);
+    } else {
+        if (a.T == 1) decode_kernel<false, 1><<<a.BH, NT, 0, stream>>>(a);
+        else decode_kernel<false, NWARP><<<a.BH, NT, 0, stream>>>(a);
+    }
     return cudaGetLastError();
 }
 
