@@ -428,18 +428,19 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-// d += Ablk (16x16) * Bblk[:, 8 nt .. 8 nt + 7]
+// d += Ablk (16x16) * Bblk[:, 8 nt .. 8 nt + 7]; both blocks hold values already rounded to
+// tf32 (the off-diagonal blocks of A and the blocks of T are stored that way)
 __device__ __forceinline__ void block_mma(float (&d)[4], const float* Ablk, const float* Bblk,
                                           int nt, int g, int t) {
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {
         uint32_t a[4], b[2];
-        a[0] = to_tf32(Ablk[g * BS + ks * 8 + t]);
-        a[1] = to_tf32(Ablk[(g + 8) * BS + ks * 8 + t]);
-        a[2] = to_tf32(Ablk[g * BS + ks * 8 + t + 4]);
-        a[3] = to_tf32(Ablk[(g + 8) * BS + ks * 8 + t + 4]);
-        b[0] = to_tf32(Bblk[(ks * 8 + t) * BS + nt * 8 + g]);
-        b[1] = to_tf32(Bblk[(ks * 8 + t + 4) * BS + nt * 8 + g]);
+        a[0] = __float_as_uint(Ablk[g * BS + ks * 8 + t]);
+        a[1] = __float_as_uint(Ablk[(g + 8) * BS + ks * 8 + t]);
+        a[2] = __float_as_uint(Ablk[g * BS + ks * 8 + t + 4]);
+        a[3] = __float_as_uint(Ablk[(g + 8) * BS + ks * 8 + t + 4]);
+        b[0] = __float_as_uint(Bblk[(ks * 8 + t) * BS + nt * 8 + g]);
+        b[1] = __float_as_uint(Bblk[(ks * 8 + t + 4) * BS + nt * 8 + g]);
         mma_tf32(d, a, b);
     }
 }
@@ -459,30 +460,31 @@ __device__ __forceinline__ void c_to_b(const float (&x)[4], int g, int t, uint32
     b[1][1] = to_tf32(odd ? d3 : d2);
 }
 
-// e += Tblk (16x16 fp32 block) * X, with X given as B fragments
+// e += Tblk (16x16 block, tf32-rounded) * X, with X given as B fragments
 __device__ __forceinline__ void block_mma_b(float (&e)[4], const float* Tblk,
                                             const uint32_t (&b)[2][2], int g, int t) {
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {
         uint32_t a[4];
-        a[0] = to_tf32(Tblk[g * BS + ks * 8 + t]);
-        a[1] = to_tf32(Tblk[(g + 8) * BS + ks * 8 + t]);
-        a[2] = to_tf32(Tblk[g * BS + ks * 8 + t + 4]);
-        a[3] = to_tf32(Tblk[(g + 8) * BS + ks * 8 + t + 4]);
+        a[0] = __float_as_uint(Tblk[g * BS + ks * 8 + t]);
+        a[1] = __float_as_uint(Tblk[(g + 8) * BS + ks * 8 + t]);
+        a[2] = __float_as_uint(Tblk[g * BS + ks * 8 + t + 4]);
+        a[3] = __float_as_uint(Tblk[(g + 8) * BS + ks * 8 + t + 4]);
         mma_tf32(e, a, b[ks]);
     }
 }
 
-// Stores T(i,j)[:, 8 nt .. 8 nt + 7] = -e (C fragment): the fp32 block and the bf16
-// T_U / T_W entries (columns scaled by beta_j and beta_j Gamma_j).
+// Stores T(i,j)[:, 8 nt .. 8 nt + 7] = -e (C fragment): the block (rounded to tf32: only
+// the tf32 products read it) and the bf16 T_U / T_W entries (columns scaled by beta_j and
+// beta_j Gamma_j, from the unrounded values).
 __device__ __forceinline__ void block_store(const float (&e)[4], float* Tout, int i, int j, int nt,
                                             int g, int t, const float* beta, const float* Gam,
                                             uint32_t tu, uint32_t tw) {
     const int c0 = nt * 8 + 2 * t;  // column inside the block
-    Tout[g * BS + c0] = -e[0];
-    Tout[g * BS + c0 + 1] = -e[1];
-    Tout[(g + 8) * BS + c0] = -e[2];
-    Tout[(g + 8) * BS + c0 + 1] = -e[3];
+    Tout[g * BS + c0] = __uint_as_float(to_tf32(-e[0]));
+    Tout[g * BS + c0 + 1] = __uint_as_float(to_tf32(-e[1]));
+    Tout[(g + 8) * BS + c0] = __uint_as_float(to_tf32(-e[2]));
+    Tout[(g + 8) * BS + c0 + 1] = __uint_as_float(to_tf32(-e[3]));
     const int J = 16 * j + c0, R0 = 16 * i + g, R1 = R0 + 8;
     const float b0 = beta[J], b1 = beta[J + 1];
     const float w0 = b0 * Gam[J], w1 = b1 * Gam[J + 1];
@@ -765,42 +767,61 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
             }
 
             // ---- P (bf16 tile) and A (fp32 blocks) from the Gram matrices: thread (wg, L)
-            // takes row L of [QK^T; KK^T], columns 16 bj + 8 wg .. + 7 of every 16-block bj
+            // takes row L of [QK^T; KK^T], columns 16 bj + 8 wg .. + 7 of every 16-block bj.
+            // A warp's rows fill the two row blocks bq, bq + 1, so blocks left of bq and
+            // right of bq + 1 are uniform over the warp (one factor per block times the
+            // column's table entry; zero); in the two blocks between, each lane selects left
+            // of, on (the masked exp of a non-positive argument) or right of its diagonal.
+            // The off-diagonal blocks of A feed only the tf32 products of the inverse's
+            // doubling steps, so they are stored rounded to tf32.
             {
                 const int r = L & 63, br = r >> 4, rl = r & 15;
-                const bool isP = L < 64;
+                const int bq = (r >> 5) * 2;  // uniform over the warp
+                const bool isP = L < 64;      // uniform over the warp
                 const float gr = sc.gam[r];
                 const float scl = isP ? 1.f : sc.beta[r];
                 const int lim = isP ? rl : rl - 1;
                 float gv[32];
                 tmem_ld8x4(tmem + lane_off + PT_G + 8 * wg, gv);
-                // The lanes of a warp cover two 16-row blocks, so the three cases (block left
-                // of, on, right of the diagonal) are selected per element instead of
-                // branched on. Left of the diagonal: one factor per block times the
-                // column's table entry; on it: the masked exp of a non-positive argument.
-                float fb[4], dg[8];
+                float dg[8];
+                {
+                    const float4* gp = reinterpret_cast<const float4*>(sc.gam + 16 * br + 8 * wg);
+                    const float4 g0 = gp[0], g1 = gp[1];
+                    const float gj[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 #pragma unroll
-                for (int bj = 0; bj < 4; ++bj)
-                    fb[bj] = (bj < br) ? __expf(gr - sc.endgam[bj]) * scl : 0.f;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int jj = 8 * wg + e;
-                    dg[e] = __expf(fminf(gr - sc.gam[16 * br + jj], 0.f)) * ((jj <= lim) ? scl : 0.f);
+                    for (int e = 0; e < 8; ++e)
+                        dg[e] = __expf(fminf(gr - gj[e], 0.f)) * ((8 * wg + e <= lim) ? scl : 0.f);
                 }
 #pragma unroll
                 for (int bj = 0; bj < 4; ++bj) {
                     float* v = gv + 8 * bj;
+                    if (bj > bq + 1) {  // right of the diagonal for the whole warp
+                        if (isP)
+                            st_shared_v4(sw128_chunk(sb + P_P, r, 2 * bj + wg), 0u, 0u, 0u, 0u);
+                        continue;
+                    }
+                    const float4* cp = reinterpret_cast<const float4*>(sc.ctab + 16 * bj + 8 * wg);
+                    const float4 c0 = cp[0], c1 = cp[1];
+                    const float ct[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                    if (bj < bq) {  // left of the diagonal for the whole warp
+                        const float fb = __expf(gr - sc.endgam[bj]) * scl;
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float f = (bj < br) ? fb[bj] * sc.ctab[16 * bj + 8 * wg + e]
-                                                  : ((bj == br) ? dg[e] : 0.f);
-                        v[e] *= f;
+                        for (int e = 0; e < 8; ++e) v[e] *= fb * ct[e];
+                    } else {
+                        const float fb = (bj < br) ? __expf(gr - sc.endgam[bj]) * scl : 0.f;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            v[e] *= (bj < br) ? fb * ct[e] : ((bj == br) ? dg[e] : 0.f);
                     }
                     if (isP) {
                         st_shared_v4(sw128_chunk(sb + P_P, r, 2 * bj + wg), pack_bf16(v[0], v[1]),
                                      pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]),
                                      pack_bf16(v[6], v[7]));
                     } else if (bj <= br) {
+                        if (bj < br) {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(to_tf32(v[e]));
+                        }
                         float* dst = Ablk(br, bj) + rl * BS + 8 * wg;
                         *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
                         *reinterpret_cast<float4*>(dst + 4) = make_float4(v[4], v[5], v[6], v[7]);
@@ -838,7 +859,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
                 const float bj = sc.beta[J], wj = bj * sc.Gam[J];
 #pragma unroll
                 for (int m = 0; m < 16; ++m) {
-                    Td[m * BS + cc] = x[m];
+                    Td[m * BS + cc] = __uint_as_float(to_tf32(x[m]));  // read by tf32 MMAs only
                     st_shared_b16(sw128_elem(tu, 16 * i + m, J), x[m] * bj);
                     st_shared_b16(sw128_elem(tw, 16 * i + m, J), x[m] * wj);
                 }
