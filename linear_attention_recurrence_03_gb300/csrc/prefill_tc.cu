@@ -746,16 +746,18 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
             auto export_rows = [&](int j, bool isq) {
                 const CarryScalars& cs = *reinterpret_cast<const CarryScalars*>(sm + P_CS);
                 const int blk = j >> 9, off = (j & 511) * 16, row = (j & 511) >> 3;
-                const float f = isq ? sc.Gam[row] : cs.kdec[row];
+                // one packed bf16 product per pair (the row factor rounded to bf16)
+                const __nv_bfloat162 f2 =
+                    __float2bfloat162_rn(isq ? sc.Gam[row] : cs.kdec[row]);
                 const uint4 x = *reinterpret_cast<const uint4*>(
                     sm + blk * PQ_STRIDE + (isq ? PQ_Q : PQ_K) + off);
                 const uint32_t in[4] = {x.x, x.y, x.z, x.w};
                 uint32_t o[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float2 v =
-                        __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&in[e]));
-                    o[e] = pack_bf16(v.x * f, v.y * f);
+                    const __nv_bfloat162 r =
+                        __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&in[e]), f2);
+                    o[e] = *reinterpret_cast<const uint32_t*>(&r);
                 }
                 *reinterpret_cast<uint4*>(wsu + (isq ? WS_QT : WS_KT) + blk * 8192 + off) =
                     make_uint4(o[0], o[1], o[2], o[3]);
@@ -855,14 +857,8 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
                     if (m > cc) x[m] = -(s0 + s1);
                 }
                 float* Td = Tb + bidx(i, i) * 16 * BS;
-                const int J = 16 * i + cc;
-                const float bj = sc.beta[J], wj = bj * sc.Gam[J];
 #pragma unroll
-                for (int m = 0; m < 16; ++m) {
-                    Td[m * BS + cc] = __uint_as_float(to_tf32(x[m]));  // read by tf32 MMAs only
-                    st_shared_b16(sw128_elem(tu, 16 * i + m, J), x[m] * bj);
-                    st_shared_b16(sw128_elem(tw, 16 * i + m, J), x[m] * wj);
-                }
+                for (int m = 0; m < 16; ++m) Td[m * BS + cc] = __uint_as_float(to_tf32(x[m]));
             } else if (a.export_qk) {
                 for (int j = P - 64; j < 1024; j += 192) export_rows(j, false);
             }
@@ -879,6 +875,32 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
                 block_mma_b(e, Tb + bidx(i, i) * 16 * BS, bx, g8, t4);
                 block_store(e, Tb + bidx(i, j) * 16 * BS, i, j, nt, g8, t4, sc.beta, sc.Gam, tu,
                             tw);
+            } else {
+                // meanwhile the diagonal blocks go to the bf16 T_U / T_W tiles: thread = 8
+                // columns (one 16-byte chunk) of one row of one block, columns scaled by
+                // beta_J and beta_J Gamma_J (zeros above the diagonal come with the block)
+                const int u = P - 128, i = u >> 5, m = (u >> 1) & 15, hh = u & 1;
+                const float* src = Tb + bidx(i, i) * 16 * BS + m * BS + 8 * hh;
+                const int J = 16 * i + 8 * hh;
+                const float4 t0 = *reinterpret_cast<const float4*>(src);
+                const float4 t1 = *reinterpret_cast<const float4*>(src + 4);
+                const float4 b0 = *reinterpret_cast<const float4*>(sc.beta + J);
+                const float4 b1 = *reinterpret_cast<const float4*>(sc.beta + J + 4);
+                const float4 g0 = *reinterpret_cast<const float4*>(sc.Gam + J);
+                const float4 g1 = *reinterpret_cast<const float4*>(sc.Gam + J + 4);
+                const float tv[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+                const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+                const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+                uint32_t ou[4], ow[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float u0 = tv[2 * e] * bv[2 * e], u1 = tv[2 * e + 1] * bv[2 * e + 1];
+                    ou[e] = pack_bf16(u0, u1);
+                    ow[e] = pack_bf16(u0 * gv[2 * e], u1 * gv[2 * e + 1]);
+                }
+                const int R = 16 * i + m;
+                st_shared_v4(sw128_chunk(tu, R, J >> 3), ou[0], ou[1], ou[2], ou[3]);
+                st_shared_v4(sw128_chunk(tw, R, J >> 3), ow[0], ow[1], ow[2], ow[3]);
             }
             bar_sync(2, 256);
             if (P == 0) TRACE_PREP(26);
