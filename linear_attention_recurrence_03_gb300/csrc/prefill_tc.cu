@@ -1035,20 +1035,20 @@ __device__ __forceinline__ void carry_produce(uint8_t* sm, uint64_t* bar, CarryS
         bulk_g2s(st + OFF_P, wsc + WS_P, 8192, fl);
         bulk_g2s(&scal[s], wsc + WS_CS, sizeof(CarryScalars), fl);
         issued = c + 1;
-        // chunk c + 2 goes to L2 now (only the parts of the unit that were written)
-        if (c + 2 < nch) {
+        // chunk c + 2 goes to L2 now (only the parts of the unit that were written), for
+        // the transposed carry, whose full waves are bound by HBM bandwidth. The two-slice
+        // carry does without: the prefetches share the SM's copy engine with the chunk
+        // loads its chain waits for (a traced chunk takes about 2.6K cycles without them,
+        // 2.9K with).
+        if (!qk_ws && c + 2 < nch) {
             const int t2 = t + 2 * C;
             for (int blk = 0; blk < Cfg::NB; ++blk) tma_prefetch_l2_3d(mvp, n0 + blk * 64, t2, zv);
-            if (qk_ws) {
-                bulk_prefetch_l2(wsc + 2 * WS_UNIT, WS_UNIT);
-            } else {
-                for (int blk = 0; blk < 2; ++blk) {
-                    tma_prefetch_l2_3d(mqp, blk * 64, t2, zq);
-                    tma_prefetch_l2_3d(mkp, blk * 64, t2, zq);
-                }
-                bulk_prefetch_l2(wsc + 2 * WS_UNIT, WS_QT);
-                bulk_prefetch_l2(wsc + 2 * WS_UNIT + WS_CS, sizeof(CarryScalars));
+            for (int blk = 0; blk < 2; ++blk) {
+                tma_prefetch_l2_3d(mqp, blk * 64, t2, zq);
+                tma_prefetch_l2_3d(mkp, blk * 64, t2, zq);
             }
+            bulk_prefetch_l2(wsc + 2 * WS_UNIT, WS_QT);
+            bulk_prefetch_l2(wsc + 2 * WS_UNIT + WS_CS, sizeof(CarryScalars));
         }
     }
     if (*abort_flag) {
