@@ -70,6 +70,14 @@ __global__ void __launch_bounds__(NT, 2) decode_kernel(DecodeArgs a) {
     float* S1 = a.state_out + (size_t)bh * K * V;
     const size_t BH = (size_t)a.BH;
 
+    // 0. the state of the row a later CTA on this SM will take (pf_rows = the CTAs resident
+    // at once) goes to L2 now, so the reads keep streaming while this CTA computes
+    if (tid == 0 && a.pf_rows > 0 && bh + a.pf_rows < a.BH && (K * V) % 4 == 0)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                         S0 + (size_t)a.pf_rows * K * V),
+                     "r"((uint32_t)(K * V) * 4u)
+                     : "memory");
+
     // 1. issue the state loads first: 16 rows x 4 columns per thread
     float st[ROWS][4];
 #pragma unroll
@@ -220,8 +228,18 @@ __global__ void __launch_bounds__(NT, 2) decode_kernel(DecodeArgs a) {
 
 }  // namespace
 
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
-    if (a.BH == 0 || a.T == 0) return cudaSuccess;
+cudaError_t launch_decode(const DecodeArgs& args, cudaStream_t stream) {
+    if (args.BH == 0 || args.T == 0) return cudaSuccess;
+    // two CTAs per SM are resident (launch bounds): rows that far ahead are prefetched
+    constexpr int kMaxDevices = 64;
+    static int sms_of[kMaxDevices] = {};
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices) {
+        if (sms_of[dev] == 0) cudaDeviceGetAttribute(&sms_of[dev], cudaDevAttrMultiProcessorCount, dev);
+        sms = sms_of[dev];
+    }
+    DecodeArgs a = args;
+    a.pf_rows = 2 * sms;
     // a single step stages one token's inputs (the smaller footprint keeps the streaming
     // step at its bandwidth); several tokens are staged NWARP at a time
     if (a.V == kMaxHeadDim) {

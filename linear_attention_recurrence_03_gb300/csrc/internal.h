@@ -62,6 +62,7 @@ struct DecodeArgs {
     __nv_bfloat16* out;       // [T, BH, V]
     int BH, H, K, V;
     int T;                    // consecutive tokens per call (1: the single decode step)
+    int pf_rows = 0;          // set by the launcher: rows ahead whose state goes to L2
 };
 
 // SIMT fp32 chunked prefill (any Dk, Dv <= 128; q/k/v fp32 or bf16). *launched
