@@ -231,8 +231,8 @@ __global__ void __launch_bounds__(NT, 2) decode_kernel(DecodeArgs a) {
 cudaError_t launch_decode(const DecodeArgs& args, cudaStream_t stream) {
     if (args.BH == 0 || args.T == 0) return cudaSuccess;
     // two CTAs per SM are resident (launch bounds): rows that far ahead are prefetched, in
-    // the single step (the multi-token form holds each CTA T times as long and ran slower
-    // with the prefetch: 0.61 against 0.51 ms at T = 8)
+    // the single step, where it was measured to help (the multi-token form, whose CTAs stay
+    // T times as long, measured the same with and without it)
     constexpr int kMaxDevices = 64;
     static int sms_of[kMaxDevices] = {};
     int dev = 0, sms = 0;
