@@ -144,14 +144,26 @@ gdn_status gdn_prefill_varlen(const void* q, const void* k, const void* v, const
                               void* workspace, size_t workspace_bytes, void* stream);
 
 /*
- * gdn_prefill_noalloc -- gdn_prefill without a caller workspace: the scratch is a
- * fixed 128 MiB device array inside the library (allocated when the library's module is
- * loaded), so the call allocates nothing. Arguments, results and errors as gdn_prefill.
- * On the tensor-core path (bf16, Dk = Dv = 128) the sequence is processed in segments of
- * whole 64-token chunks that fit the scratch (2016 (batch, head, chunk) units), the state
- * carrying over from one segment to the next; the result equals gdn_prefill's.
- * GDN_EUNSUPPORTED if B * Hv exceeds 2016. The scratch is shared by every caller in the
- * process: calls must not run concurrently (issue them on one stream, or synchronise).
+ * gdn_prefill_noalloc -- gdn_prefill for callers that cannot hand the library device memory:
+ * a plug-in inside a host runtime that owns the device memory and gives the plug-in no
+ * allocator, or a latency-critical loop in which an allocation (cudaMalloc can synchronise
+ * the device) is not allowed. The call takes no workspace and allocates nothing: its scratch
+ * is a fixed 128 MiB array in the library's own device memory, which every GPU that loads
+ * the library holds until the process exits. (The pages have no counterpart of this call.)
+ *
+ * Arguments, results and errors as gdn_prefill (the caller still passes inputs, state and
+ * out). On the tensor-core path (bf16, Dk = Dv = 128) the sequence is processed in segments
+ * of whole 64-token chunks that fit the scratch -- 128 MiB / 66064 bytes per (batch, value
+ * head, chunk) unit = 2031 units -- the state carrying over in fp32 from one segment to the
+ * next, so the result equals gdn_prefill's. GDN_EUNSUPPORTED, with a message, when B * Hv
+ * exceeds 2031 (not even one chunk per head fits). Every other path needs no scratch and
+ * runs as gdn_prefill.
+ *
+ * The first call on each device looks up the array's device address (with that device
+ * current); make that first call before any stream capture begins. Every call shares the one
+ * array, whose contents the next call overwrites before reading: calls that overlap on the
+ * GPU (other streams, other threads) race on it, so issue them on one stream or synchronise
+ * between them.
  */
 gdn_status gdn_prefill_noalloc(const void* q, const void* k, const void* v,
                                const float* g_log, const float* beta, float scale,

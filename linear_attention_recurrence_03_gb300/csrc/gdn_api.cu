@@ -6,6 +6,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstdint>
+#include <mutex>
 #include <string>
 
 #include "gdn.h"
@@ -16,10 +17,33 @@ namespace {
 thread_local std::string g_last_error;
 std::atomic<unsigned long long> g_launches{0};
 
-// Scratch of gdn_prefill_noalloc: device memory of the library's own module, so that the
-// call itself allocates nothing.
+// Scratch of gdn_prefill_noalloc, for callers that may not allocate device memory while
+// they run: a file-scope device array of the library's own module (every device that loads
+// the library holds it until the process exits), so the call itself allocates nothing.
 constexpr size_t kStaticScratchBytes = size_t(128) << 20;
 __device__ __align__(256) unsigned char g_prefill_scratch[kStaticScratchBytes];
+
+// In host code `g_prefill_scratch` names a host-side stand-in, not device memory: the
+// array's device address is looked up once per device (with that device current) and
+// kept here; the kernels are given that address.
+constexpr int kMaxScratchDevices = 64;
+void* g_scratch_addr[kMaxScratchDevices];
+cudaError_t g_scratch_err[kMaxScratchDevices];
+std::once_flag g_scratch_once[kMaxScratchDevices];
+
+// Device address of the scratch array on the current device (the set-up runs on the
+// first call for each device).
+cudaError_t scratch_address(void** addr) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxScratchDevices) return cudaErrorInvalidDevice;
+    std::call_once(g_scratch_once[dev], [dev] {
+        g_scratch_err[dev] = cudaGetSymbolAddress(&g_scratch_addr[dev], g_prefill_scratch);
+    });
+    *addr = g_scratch_addr[dev];
+    return g_scratch_err[dev];
+}
 
 gdn_status fail(gdn_status st, const char* fmt, ...) {
     char buf[512];
@@ -170,9 +194,10 @@ gdn_status gdn_prefill_noalloc(const void* q, const void* k, const void* v, cons
         return fail(GDN_EUNSUPPORTED, "gdn_prefill_noalloc: B*Hv = %zu exceeds the %zu "
                     "(batch, head) pairs its static scratch holds", heads, units);
     void* scratch = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&scratch, g_prefill_scratch);
-    if (e != cudaSuccess)
-        return fail(GDN_ECUDA, "gdn_prefill_noalloc: scratch address: %s", cudaGetErrorString(e));
+    cudaError_t e = scratch_address(&scratch);
+    if (e != cudaSuccess || scratch == nullptr)
+        return fail(GDN_ECUDA, "gdn_prefill_noalloc: device address of the static scratch: %s",
+                    cudaGetErrorString(e));
     const int nch = (S + 63) / 64;
     const int seg = (int)std::min<size_t>(units / heads, (size_t)nch);
     const cudaStream_t s = static_cast<cudaStream_t>(stream);

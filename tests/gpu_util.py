@@ -68,15 +68,3 @@ def gpu_decode(x, in_place=False):
     out, st = gdn.gdn_decode_step(*args, x["num_v_heads"], state_out=st_out)
     torch.cuda.synchronize()
     return out.cpu(), st.cpu()
-
-
-def oracle_decode_rows(x, rows):
-    sel = torch.as_tensor(rows)
-    sub = {n: (x[n][sel] if n in ("q", "k", "v", "b", "a", "z", "state") else x[n])
-           for n in DECODE_NAMES}
-    # row r keeps its head index: rows are taken with whole head groups, so pass the
-    # per-row A_log/dt_bias by expanding the head vectors to one entry per sampled row
-    H = x["num_v_heads"]
-    sub["A_log"] = x["A_log"][sel % H]
-    sub["dt_bias"] = x["dt_bias"][sel % H]
-    return oracle.decode_step(*(sub[n] for n in DECODE_NAMES), len(rows))

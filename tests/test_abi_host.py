@@ -81,9 +81,13 @@ def test_prefill_requires_its_workspace(lib):
     assert "workspace" in lib.gdn_last_error().decode()
 
 
-def test_noalloc_rejects_more_heads_than_its_scratch(lib):
+@pytest.mark.parametrize("B,Hv", [(1, 4096), (1, 2032), (8, 254), (2, 1024)])
+def test_noalloc_rejects_more_heads_than_its_scratch(lib, B, Hv):
+    """The 128 MiB scratch holds 2031 units of 66064 bytes: B * Hv = 2032 and above are
+    refused on the host, before any launch (the accepted 2031 runs in the GPU tests)."""
+    assert (128 << 20) // 66064 == 2031
     vp = ctypes.c_void_p
-    rc = lib.gdn_prefill_noalloc(vp(16), vp(16), vp(16), vp(16), vp(16), 1.0, 1, 1, 1, 4096,
+    rc = lib.gdn_prefill_noalloc(vp(16), vp(16), vp(16), vp(16), vp(16), 1.0, 1, B, 1, Hv,
                                  64, 128, 128, vp(16), 0, vp(16), None)
     assert rc == gdn.GDN_EUNSUPPORTED
     assert "static scratch" in lib.gdn_last_error().decode()
