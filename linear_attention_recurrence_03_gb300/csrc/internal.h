@@ -113,7 +113,7 @@ struct Conv1dArgs {
 cudaError_t launch_conv1d_decode(const Conv1dArgs& a, cudaStream_t stream);
 
 // (I + A)^-1 of n strictly lower-triangular 64 x 64 fp32 matrices: algorithm 0 forward
-// substitution, 1 the Neumann product on the tensor cores.
+// substitution, 1 the Neumann product on the tcgen05 tensor cores (kind::tf32).
 cudaError_t launch_tril_inverse(const float* A, float* T, int n, int algorithm,
                                 cudaStream_t stream);
 
@@ -123,5 +123,6 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 // Device status word of each translation unit that has bounded waits: returns the
 // bits set since the last call and clears them (the stream must be synchronised).
 uint32_t prefill_tc_take_status();
+uint32_t tril_take_status();
 
 }  // namespace gdn

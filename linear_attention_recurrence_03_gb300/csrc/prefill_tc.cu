@@ -112,7 +112,15 @@ namespace {
 using namespace ptx;
 
 constexpr int C = 64;    // chunk length
+// Limit of every bounded wait. GDN_TEST_STALL (a test-only build, never the library's
+// default) shortens it to 5 ms and has the carry kernels' producer skip the loads of the
+// second chunk, so that a test can see the waits run out, the kernel unwind and the status
+// word report it.
+#ifdef GDN_TEST_STALL
+constexpr uint64_t kWaitNs = 5000000ull;
+#else
 constexpr uint64_t kWaitNs = 2000000000ull;
+#endif
 
 // Overlapped schedule (the prep of the next segment of the sequence runs beside the carry
 // of the current one): at most this many segments, of at least kMinSegmentChunks chunks.
@@ -998,9 +1006,12 @@ __device__ __forceinline__ void carry_produce(uint8_t* sm, uint64_t* bar, CarryS
                                               const uint8_t* wsh, int nch, int n0, int tbase,
                                               int zq, int zv, volatile int* abort_flag) {
     using Cfg = CarryCfg<NS>;
-    int issued = 0;
+    int lastE[2] = {-1, -1}, lastL[2] = {-1, -1};  // last chunk of each group in each stage
     for (int c = 0; c < nch; ++c) {
         const int s = c & 1;
+#ifdef GDN_TEST_STALL
+        if (c == 1) continue;  // test build: the second chunk is never loaded
+#endif
         uint8_t* st = sm + s * Cfg::STAGE;
         const uint8_t* wsc = wsh + (size_t)c * WS_UNIT;
         const int t = tbase + c * C;
@@ -1021,6 +1032,7 @@ __device__ __forceinline__ void carry_produce(uint8_t* sm, uint64_t* bar, CarryS
         for (int blk = 0; blk < Cfg::NB; ++blk)
             tma_load_3d(st + OFF_V + blk * 8192, mvp, fe, n0 + blk * 64, t, zv);
         bulk_g2s(st + Cfg::OFF_TU, wsc + WS_TU, 8192, fe);
+        lastE[s] = c;
         // late group of chunk c: K~ or k, P, scalars
         if (c >= 2 && !wait_or_abort(&bar[B_EMPTYL0 + s], ((c >> 1) + 1) & 1, abort_flag,
                                      ST_PRODUCER))
@@ -1034,7 +1046,7 @@ __device__ __forceinline__ void carry_produce(uint8_t* sm, uint64_t* bar, CarryS
         }
         bulk_g2s(st + OFF_P, wsc + WS_P, 8192, fl);
         bulk_g2s(&scal[s], wsc + WS_CS, sizeof(CarryScalars), fl);
-        issued = c + 1;
+        lastL[s] = c;
         // chunk c + 2 goes to L2 now (only the parts of the unit that were written), for
         // the transposed carry, whose full waves are bound by HBM bandwidth. The two-slice
         // carry does without: the prefetches share the SM's copy engine with the chunk
@@ -1051,13 +1063,14 @@ __device__ __forceinline__ void carry_produce(uint8_t* sm, uint64_t* bar, CarryS
             bulk_prefetch_l2(wsc + 2 * WS_UNIT + WS_CS, sizeof(CarryScalars));
         }
     }
-    if (*abort_flag) {
-        // let the copies already issued land before the CTA exits (a group whose
-        // copies were not issued completes no phase: its wait just runs out)
-        for (int c = (issued > 2 ? issued - 2 : 0); c < issued; ++c) {
-            mbar_wait_bounded(&bar[B_FULLE0 + (c & 1)], (c >> 1) & 1, kWaitNs);
-            mbar_wait_bounded(&bar[B_FULLL0 + (c & 1)], (c >> 1) & 1, kWaitNs);
-        }
+    // every load is issued (the last chunks are in flight): a dependent carry segment may
+    // start its setup
+    grid_dep_launch_dependents();
+    // every copy issued lands before the CTA exits (also when a consumer gave up before
+    // waiting for it); a group never issued is not waited for
+    for (int s = 0; s < 2; ++s) {
+        if (lastE[s] >= 0) mbar_wait_bounded(&bar[B_FULLE0 + s], (lastE[s] >> 1) & 1, kWaitNs);
+        if (lastL[s] >= 0) mbar_wait_bounded(&bar[B_FULLL0 + s], (lastL[s] >> 1) & 1, kWaitNs);
     }
 }
 
@@ -1122,9 +1135,7 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
             carry_produce<NS>(sm, bar, scal, &mq, &mk, &mv, true,
                               a.ws + ws_offset(wb, h, u0, a.Hv, a.nseg), nch, n0, tbase,
                               wb * a.Hk + h / (a.Hv / a.Hk), wb * a.Hv + h, abort_flag);
-            // every load is issued (the last chunks are in flight): a dependent carry
-            // segment may start its setup
-            grid_dep_launch_dependents();
+
         }
     } else if (warp == 2 || warp >= 4) {
         // ----------------------------------------- carry (warps 2, 4..11: 288 threads)
@@ -1481,7 +1492,6 @@ __global__ void __launch_bounds__(CARRY_T_THREADS, 1)
             carry_produce<128>(sm, bar, scal, &mq, &mk, &mv, false,
                                a.ws + ws_offset(wb, h, u0, a.Hv, a.nseg), nch, 0, tbase,
                                wb * a.Hk + h / (a.Hv / a.Hk), zo, abort_flag);
-            grid_dep_launch_dependents();  // as in carry_tc_kernel
         }
     } else {
         const bool issuer = warp == 1;
@@ -1904,6 +1914,7 @@ cudaError_t set_attributes() {
         if (r == cudaSuccess)
             r = cudaFuncSetAttribute(carry_t_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)CarryT::SMEM);
+
         return r;
     }();
     return e;

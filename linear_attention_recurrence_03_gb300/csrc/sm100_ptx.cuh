@@ -254,6 +254,31 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem desc], kind::tf32: A and B are 32-bit elements read as
+// tf32 (the low 13 mantissa bits are not used), fp32 accumulate. A (M = 128) is read from
+// tensor memory, row m in lane m, one element per 32-bit column: one K = 8 step spans 8
+// columns. A may be an fp32 accumulator an earlier MMA wrote, once that MMA has completed.
+__device__ __forceinline__ void mma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// D[tmem] (+)= A[smem desc] * B[smem desc], kind::tf32 (both operands in shared memory).
+__device__ __forceinline__ void mma_tf32_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // 32 TMEM lanes x 32 consecutive fp32 columns: thread l of the warp receives lane
 // (lane base of taddr) + l, columns col..col+31. Includes the wait for completion.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
@@ -426,6 +451,22 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
     return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
            ((b_mn ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
            (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Instruction descriptor for kind::tf32: tf32 A and B (format 2), fp32 D, dense, both
+// operands K-major. `neg_b` negates B (D = A (-B) + D).
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N, bool neg_b = false) {
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((neg_b ? 1u : 0u) << 14) |
+           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Byte offset of element (row, col) of a 32-bit tile stored K-major in the 128-byte swizzle
+// layout: 32 elements (128 bytes) per row of a k-block, 8-row atoms of 1024 bytes, the
+// 16-byte chunk index XOR-ed with (row % 8); k-block kb = col / 32 starts at kb * rows * 128.
+__host__ __device__ constexpr uint32_t sw128_offset32(uint32_t row, uint32_t col,
+                                                      uint32_t rows) {
+    return (col >> 5) * rows * 128u + (row >> 3) * 1024u + (row & 7u) * 128u +
+           (((((col & 31u) >> 2) ^ (row & 7u)) & 7u) << 4) + ((col & 3u) << 2);
 }
 
 // Byte offset of element (row, col) of a bf16 tile stored in the 128-byte swizzle

@@ -1,0 +1,58 @@
+"""A bounded wait of the tensor-core prefill runs out, and the library says so.
+
+Every mbarrier wait in the tensor-core kernels has a time limit; when one runs out the
+kernel records a status bit, the other roles leave their loops, the MMAs and copies already
+issued complete, tensor memory is freed, and gdn_get_device_status() reports GDN_ETIMEOUT.
+This test makes that happen without a fault: a copy of the library built with the test-only
+define GDN_TEST_STALL (wait limit 5 ms; the carry kernel's producer never loads the second
+64-token chunk) runs one tiny prefill (1 head, S = 128), whose consumers then wait for data
+that never comes. The normal library is then called on the same GPU and must give a clean
+status and parity with the oracle: the stalled kernel left no tensor memory allocated and
+nothing waiting.
+"""
+import os
+
+import pytest
+import torch
+
+from gpu_util import DEV, TOL_BF16, ensure_built, gpu_prefill, oracle_prefill_all, rel, to_np
+import linear_attention_recurrence_03_gb300 as gdn
+from linear_attention_recurrence_03_gb300 import build as lib_build
+from linear_attention_recurrence_03_gb300 import synthetic as syn
+
+pytestmark = pytest.mark.gpu
+
+
+def _stall_library():
+    path = os.path.join(lib_build.BUILD + "_gdn_test_stall", "libgdn_test_stall.so")
+    lib_build.build(defines=("GDN_TEST_STALL",), lib_path=path)
+    return gdn.load_library(path)
+
+
+def test_bounded_wait_runs_out_then_library_recovers():
+    ensure_built()
+    stall = _stall_library()
+    w = syn.shrink(syn.PREFILL_BF16_GQA2, B=1, Hk=1, Hv=1, S=128, state_std=None)
+    x = syn.prefill_inputs(w)
+    X = [x[n].to(DEV) for n in ("q", "k", "v", "g_log", "beta")]
+    import ctypes
+    vp = ctypes.c_void_p
+    state = torch.empty((1, 1, 128, 128), dtype=torch.float32, device=DEV)
+    out = torch.empty((1, 1, 128, 128), dtype=torch.bfloat16, device=DEV)
+    wsb = stall.gdn_prefill_workspace_bytes(1, 1, 1, 128, 128, 128, gdn.GDN_DTYPE_BF16)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    stream = vp(torch.cuda.current_stream().cuda_stream)
+    rc = stall.gdn_prefill(*(vp(t.data_ptr()) for t in X), float(x["scale"]),
+                           gdn.GDN_DTYPE_BF16, 1, 1, 1, 128, 128, 128, vp(state.data_ptr()), 0,
+                           vp(out.data_ptr()), vp(ws.data_ptr()), wsb, stream)
+    assert rc == gdn.GDN_OK  # enqueued: the failure is found on the device
+    assert stall.gdn_get_device_status(stream) == gdn.GDN_ETIMEOUT
+    assert "bounded wait" in stall.gdn_last_error().decode()
+    # the status word was read and cleared
+    assert stall.gdn_get_device_status(stream) == gdn.GDN_OK
+    # the normal library on the same GPU: clean status and parity
+    o, s = gpu_prefill(x)
+    assert gdn.gdn_get_device_status() == gdn.GDN_OK
+    o_ref, s_ref = oracle_prefill_all(x)
+    assert rel(to_np(o), o_ref) <= TOL_BF16["out"]
+    assert rel(to_np(s), s_ref) <= TOL_BF16["state"]
