@@ -20,8 +20,9 @@
 //
 // Multi-token form (T consecutive steps of the same rows in one call; an extension, not
 // on the pages): the state stays in registers across the T tokens, so its 2 x 64 KB of
-// HBM traffic is paid once per call; token t's inputs sit at offset t * BH rows. The
-// tokens are taken in blocks of up to eight in chunk form (derived from the same step):
+// HBM traffic is paid once per call; token t's inputs sit at offset t * BH rows. Up to
+// four tokens run one after another on the register state; more are taken in blocks of
+// eight in chunk form (derived from the same step):
 // with gamma_t = g_1 + ... + g_t (from the block start), Gamma_t = exp(gamma_t) and
 // D[t][i] = exp(gamma_t - gamma_i) (i <= t, never above 1),
 //   X[t] = S0^T k^_t, Y[t] = S0^T q^_t            (one pass over the old state, all t)
@@ -257,8 +258,8 @@ struct MultiSmem {
     float ssq[TB][kMaxHeadDim / 32];
 };
 
-// NB tokens per block (2, 4 or 8; the last block of a call may hold fewer real tokens,
-// the rest padded with zero rows, which contribute exactly nothing). Warp w holds the
+// NB tokens per block (the last block of a call may hold fewer real tokens, the rest
+// padded with zero rows, which contribute exactly nothing). Warp w holds the
 // contiguous state rows 16 w .. 16 w + 15, lane l four columns (as in the single step), so
 // that a warp's slice of k^ or q^ is four 16-byte broadcast loads.
 template <bool VEC4, int NB>
@@ -509,8 +510,7 @@ __global__ void __launch_bounds__(NT, 2) decode_multi_kernel(DecodeArgs a) {
     }
 }
 
-// Launches the chunk form with NB tokens per block (the smallest of 2, 4, 8 that holds T,
-// or 8 for longer calls).
+// Launches the chunk form with NB tokens per block.
 template <bool VEC4, int NB>
 cudaError_t launch_multi(const DecodeArgs& a, cudaStream_t stream) {
     static cudaError_t attr = [] {
@@ -530,13 +530,6 @@ cudaError_t launch_multi(const DecodeArgs& a, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-template <bool VEC4>
-cudaError_t launch_multi_any(const DecodeArgs& a, cudaStream_t stream) {
-    if (a.T <= 2) return launch_multi<VEC4, 2>(a, stream);
-    if (a.T <= 4) return launch_multi<VEC4, 4>(a, stream);
-    return launch_multi<VEC4, 8>(a, stream);
-}
-
 }  // namespace
 
 cudaError_t launch_decode(const DecodeArgs& args, cudaStream_t stream) {
@@ -553,12 +546,22 @@ cudaError_t launch_decode(const DecodeArgs& args, cudaStream_t stream) {
     }
     DecodeArgs a = args;
     a.pf_rows = a.T == 1 ? 2 * sms : 0;
-    // a single step stages one token's inputs (the smaller footprint keeps the streaming
-    // step at its bandwidth); several tokens run in the chunk form
-    if (a.T > 1) return a.V == kMaxHeadDim ? launch_multi_any<true>(a, stream)
-                                           : launch_multi_any<false>(a, stream);
-    if (a.V == kMaxHeadDim) decode_kernel<true, 1><<<a.BH, NT, 0, stream>>>(a);
-    else decode_kernel<false, 1><<<a.BH, NT, 0, stream>>>(a);
+    // More than kPerTokenMaxT tokens: the chunk form (blocks of eight). Up to that, the
+    // token loop, which measured faster there (T = 2: 0.212 against 0.242 ms, T = 4: 0.309
+    // against 0.332 ms at BH = 8192; T = 8: 0.608 against 0.512 ms); a single step stages
+    // one token's inputs (the smaller footprint keeps the streaming step at its bandwidth),
+    // several tokens NWARP at a time.
+    constexpr int kPerTokenMaxT = 4;
+    if (a.T > kPerTokenMaxT)
+        return a.V == kMaxHeadDim ? launch_multi<true, TB>(a, stream)
+                                  : launch_multi<false, TB>(a, stream);
+    if (a.V == kMaxHeadDim) {
+        if (a.T == 1) decode_kernel<true, 1><<<a.BH, NT, 0, stream>>>(a);
+        else decode_kernel<true, NWARP><<<a.BH, NT, 0, stream>>>(a);
+    } else {
+        if (a.T == 1) decode_kernel<false, 1><<<a.BH, NT, 0, stream>>>(a);
+        else decode_kernel<false, NWARP><<<a.BH, NT, 0, stream>>>(a);
+    }
     return cudaGetLastError();
 }
 
