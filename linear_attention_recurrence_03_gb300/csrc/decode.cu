@@ -239,32 +239,68 @@ __global__ void __launch_bounds__(NT, 2) decode_kernel(DecodeArgs a) {
 
 // ---------------------------------------------------------------- several tokens
 
-constexpr int TB = 8;   // tokens per block of the chunk form
-constexpr int RG = 4;   // tokens per reduction group (partials held in registers)
-constexpr int MROWS = kMaxHeadDim / NWARP;  // 16 contiguous state rows per warp
+// The chunk form (more than four tokens per call), blocks of TB tokens. One CTA of
+// MT = 512 threads per row; the 64 KB state sits in shared memory (one bulk copy, started
+// first, so its latency overlaps the staging of the inputs, the norms and the small Gram
+// products), which leaves the registers free for two CTAs per SM. k^ and q^ are stored
+// token-minor ([row][token]), so that a thread's four tokens of a row are one 16-byte
+// broadcast load in both passes over the state.
+constexpr int TB = 8;
+constexpr int MT = 512;
+constexpr int MW = MT / 32;
+constexpr uint64_t kDecodeWaitNs = 2000000000ull;
+
+// Status bit of a bounded wait of this file that ran out (decode_take_status).
+__device__ uint32_t g_decode_status = 0;
 
 struct MultiSmem {
-    float qn[TB][kMaxHeadDim];   // q^ (normalised in place); zero for padding tokens
-    float kn[TB][kMaxHeadDim];   // k^
+    float S[kMaxHeadDim * kMaxHeadDim];  // the state, row-major [K][V] (row stride 128)
+    float kT[kMaxHeadDim][TB];           // k^ token-minor (zero rows for padding tokens)
+    float qT[kMaxHeadDim][TB];           // q^ token-minor
     float v[TB][kMaxHeadDim];
     float z[TB][kMaxHeadDim];
-    float X[TB][kMaxHeadDim];    // S0^T k^_t, then u_t
-    float Y[TB][kMaxHeadDim];    // S0^T q^_t, then the un-normalised o_t
-    float red[2 * RG][NWARP][kMaxHeadDim];
-    float A[TB][TB];             // beta_t D[t][i] (k^_t . k^_i), i < t
-    float P[TB][TB];             // D[t][i] (k^_i . q^_t), i <= t
+    float X[TB][kMaxHeadDim];            // S0^T k^_t (partials summed), then u_t
+    float Y[TB][kMaxHeadDim];            // S0^T q^_t, then the un-normalised o_t
+    float red[2][2 * TB][kMaxHeadDim];   // the second row half's partial sums
+    float A[TB][TB];                     // beta_t D[t][i] (k^_t . k^_i), i < t
+    float P[TB][TB];                     // D[t][i] (k^_i . q^_t), i <= t
     float kk[TB][TB], kq[TB][TB];
     float gam[TB], Gam[TB], dlast[TB], beta[TB], g[TB], inv[2][TB];
     float ssq[TB][kMaxHeadDim / 32];
+    unsigned long long bar;
+    int failed;
 };
 
-// NB tokens per block (the last block of a call may hold fewer real tokens, the rest
-// padded with zero rows, which contribute exactly nothing). Warp w holds the
-// contiguous state rows 16 w .. 16 w + 15, lane l four columns (as in the single step), so
-// that a warp's slice of k^ or q^ is four 16-byte broadcast loads.
-template <bool VEC4, int NB>
-__global__ void __launch_bounds__(NT, 2) decode_multi_kernel(DecodeArgs a) {
-    extern __shared__ __align__(16) uint8_t smraw[];
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Waits (at most kDecodeWaitNs) for phase 0 of the mbarrier at `bar`; false if it ran out.
+__device__ __forceinline__ bool wait_phase0(uint32_t bar) {
+    const uint64_t t_start = globaltimer();
+    while (true) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar)
+            : "memory");
+        if (ok) return true;
+        if (globaltimer() - t_start > kDecodeWaitNs) return false;
+    }
+}
+
+template <bool FULL>  // FULL: K = V = 128 (one bulk copy of the state)
+__global__ void __launch_bounds__(MT, 2) decode_multi_kernel(DecodeArgs a) {
+    extern __shared__ __align__(128) uint8_t smraw[];
     MultiSmem& s = *reinterpret_cast<MultiSmem*>(smraw);
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int bh = blockIdx.x, h = bh % a.H;
@@ -273,40 +309,46 @@ __global__ void __launch_bounds__(NT, 2) decode_multi_kernel(DecodeArgs a) {
     float* S1 = a.state_out + (size_t)bh * K * V;
     const size_t BH = (size_t)a.BH;
     const float rsK = 1.f / sqrtf((float)K);
-    const int r0w = MROWS * w;  // this warp's first state row
+    const uint32_t bar = smem_addr(&s.bar);
 
-    // the state, loaded once: 16 rows x 4 columns per thread
-    float st[MROWS][4];
-#pragma unroll
-    for (int m = 0; m < MROWS; ++m) {
-        const int i = r0w + m;
-        if (VEC4) {
-            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (i < K) x = __ldcs(reinterpret_cast<const float4*>(S0 + (size_t)i * V) + lane);
-            st[m][0] = x.x; st[m][1] = x.y; st[m][2] = x.z; st[m][3] = x.w;
-        } else {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int j = col_of<false>(lane, c);
-                st[m][c] = (i < K && j < V) ? __ldcs(S0 + (size_t)i * V + j) : 0.f;
-            }
+    // 0. the state: one bulk copy (K = V = 128), else plain loads with zero padding
+    if (FULL) {
+        if (tid == 0) {
+            s.failed = 0;
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                         "r"(65536u)
+                         : "memory");
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], "
+                "%2, [%3];" ::"r"(smem_addr(s.S)),
+                "l"(reinterpret_cast<uint64_t>(S0)), "r"(65536u), "r"(bar)
+                : "memory");
         }
+    } else {
+        for (int e = tid; e < kMaxHeadDim * kMaxHeadDim; e += MT) {
+            const int i = e / kMaxHeadDim, j = e % kMaxHeadDim;
+            s.S[e] = (i < K && j < V) ? __ldcs(S0 + (size_t)i * V + j) : 0.f;
+        }
+        if (tid == 0) s.failed = 0;
     }
 
-    for (int t0 = 0; t0 < a.T; t0 += NB) {
-        const int nt = min(NB, a.T - t0);  // real tokens of this block
-        if (t0 > 0) __syncthreads();      // the previous block's inputs and u are read
+    for (int t0 = 0; t0 < a.T; t0 += TB) {
+        const int nt = min(TB, a.T - t0);  // real tokens of this block
+        const bool last = t0 + TB >= a.T;
+        __syncthreads();  // (the mbarrier is initialised; the previous block is done)
         // 1. inputs of the block (padding tokens: zero rows, beta = 0, g = 0)
-        for (int e = tid; e < NB * kMaxHeadDim; e += NT) {
+        for (int e = tid; e < TB * kMaxHeadDim; e += MT) {
             const int t = e / kMaxHeadDim, i = e % kMaxHeadDim;
             const size_t row = (size_t)(t0 + t) * BH + (size_t)bh;
             const bool real = t < nt;
-            s.qn[t][i] = (real && i < K) ? __bfloat162float(a.q[row * K + i]) : 0.f;
-            s.kn[t][i] = (real && i < K) ? __bfloat162float(a.k[row * K + i]) : 0.f;
+            s.qT[i][t] = (real && i < K) ? __bfloat162float(a.q[row * K + i]) : 0.f;
+            s.kT[i][t] = (real && i < K) ? __bfloat162float(a.k[row * K + i]) : 0.f;
             s.v[t][i] = (real && i < V) ? __bfloat162float(a.v[row * V + i]) : 0.f;
             s.z[t][i] = (real && i < V) ? __bfloat162float(a.z[row * V + i]) : 0.f;
         }
-        if (tid < NB) {
+        if (tid < TB) {
             const size_t row = (size_t)(t0 + tid) * BH + (size_t)bh;
             const bool real = tid < nt;
             s.beta[tid] = real ? sigmoid_f(__bfloat162float(a.b[row])) : 0.f;
@@ -315,108 +357,100 @@ __global__ void __launch_bounds__(NT, 2) decode_multi_kernel(DecodeArgs a) {
                             : 0.f;
         }
         __syncthreads();
-        // 2. the l2 norms (job j: token j / 2, q or k), the decay prefix (one thread)
-        for (int j = w; j < 2 * NB; j += NWARP) {
-            const float* x = (j & 1) ? s.kn[j >> 1] : s.qn[j >> 1];
+        // 2. the l2 norms (warp j: token j / 2, q or k), the decay prefix (one thread)
+        if (w < 2 * TB) {
+            const int t = w >> 1;
             float acc = 0.f;
 #pragma unroll
-            for (int i = lane; i < kMaxHeadDim; i += 32) acc = fmaf(x[i], x[i], acc);
+            for (int i = lane; i < kMaxHeadDim; i += 32) {
+                const float x = (w & 1) ? s.kT[i][t] : s.qT[i][t];
+                acc = fmaf(x, x, acc);
+            }
             acc = warp_sum(acc);
-            if (lane == 0) s.inv[j & 1][j >> 1] = 1.f / sqrtf(acc + kEpsL2);
+            if (lane == 0) s.inv[w & 1][t] = 1.f / sqrtf(acc + kEpsL2);
         }
-        if (tid == NT - 1) {
+        if (tid == MT - 1) {
             float gm = 0.f;
 #pragma unroll
-            for (int t = 0; t < NB; ++t) {
+            for (int t = 0; t < TB; ++t) {
                 gm += s.g[t];
                 s.gam[t] = gm;
                 s.Gam[t] = expf(gm);
             }
 #pragma unroll
-            for (int t = 0; t < NB; ++t) s.dlast[t] = expf(gm - s.gam[t]);
+            for (int t = 0; t < TB; ++t) s.dlast[t] = expf(gm - s.gam[t]);
         }
         __syncthreads();
-        for (int e = tid; e < NB * kMaxHeadDim; e += NT) {
-            const int t = e / kMaxHeadDim, i = e % kMaxHeadDim;
-            s.qn[t][i] *= s.inv[0][t];
-            s.kn[t][i] *= s.inv[1][t];
+        for (int e = tid; e < TB * kMaxHeadDim; e += MT) {
+            const int i = e / TB, t = e % TB;
+            s.qT[i][t] *= s.inv[0][t];
+            s.kT[i][t] *= s.inv[1][t];
         }
         __syncthreads();
-        // 3. the small Gram products k^_t . k^_i and k^_i . q^_t (i <= t), one warp per job
-        for (int j = w; j < NB * NB; j += NWARP) {
-            const int t = j / NB, i = j % NB;
-            if (i > t) continue;
-            float akk = 0.f, akq = 0.f;
-#pragma unroll
-            for (int e = lane; e < kMaxHeadDim; e += 32) {
-                akk = fmaf(s.kn[t][e], s.kn[i][e], akk);
-                akq = fmaf(s.kn[i][e], s.qn[t][e], akq);
+        // 3. the small Gram products k^_t . k^_i and k^_i . q^_t (i <= t): four adjacent
+        // threads per product, thread `part` taking rows part, part + 4, ... (so a warp's
+        // loads fall in distinct banks), joined by two shuffles
+        {
+            const int part = tid & 3, pr = tid >> 2;  // pr: 0..127
+            const int kind = pr >> 6, t = (pr >> 3) & 7, i = pr & 7;
+            float acc = 0.f;
+            if (i <= t) {
+#pragma unroll 8
+                for (int e = part; e < kMaxHeadDim; e += 4)
+                    acc = fmaf(s.kT[e][i], kind ? s.qT[e][t] : s.kT[e][t], acc);
             }
-            akk = warp_sum(akk);
-            akq = warp_sum(akq);
-            if (lane == 0) {
-                s.kk[t][i] = akk;
-                s.kq[t][i] = akq;
+            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+            if (part == 0 && i <= t) {
+                if (kind) s.kq[t][i] = acc;
+                else s.kk[t][i] = acc;
             }
         }
-        // 4. X[t] = S0^T k^_t and Y[t] = S0^T q^_t from the registers, RG tokens at a time
-#pragma unroll
-        for (int r0 = 0; r0 < NB; r0 += RG) {
-            constexpr int NR = NB < RG ? NB : RG;
-            if (r0 > 0) __syncthreads();  // s.red of the previous group is read
-            float px[NR][4], py[NR][4];
-#pragma unroll
-            for (int r = 0; r < NR; ++r)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) px[r][c] = py[r][c] = 0.f;
-#pragma unroll
-            for (int m4 = 0; m4 < MROWS; m4 += 4) {
-#pragma unroll
-                for (int r = 0; r < NR; ++r) {
-                    const float4 k4 = *reinterpret_cast<const float4*>(&s.kn[r0 + r][r0w + m4]);
-                    const float4 q4 = *reinterpret_cast<const float4*>(&s.qn[r0 + r][r0w + m4]);
-                    const float kv[4] = {k4.x, k4.y, k4.z, k4.w};
-                    const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
-#pragma unroll
-                    for (int mm = 0; mm < 4; ++mm)
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            px[r][c] = fmaf(kv[mm], st[m4 + mm][c], px[r][c]);
-                            py[r][c] = fmaf(qv[mm], st[m4 + mm][c], py[r][c]);
-                        }
-                }
+        // the state has landed (first block); a copy that never lands is waited for once
+        // more before the CTA leaves
+        if (FULL && t0 == 0 && !wait_phase0(bar)) {
+            atomicOr(&g_decode_status, 1u);
+            s.failed = 1;
+        }
+        __syncthreads();
+        if (s.failed) {
+            if (tid == 0) wait_phase0(bar);
+            return;
+        }
+        // 4. X[t] = S0^T k^_t and Y[t] = S0^T q^_t: thread (column j, tokens 4 th .. 4 th + 3,
+        // rows 64 rh .. 64 rh + 63); the second row half adds its partials through red
+        {
+            const int j = tid & (kMaxHeadDim - 1), th = (tid >> 7) & 1, rh = tid >> 8;
+            float px[4] = {0.f, 0.f, 0.f, 0.f}, py[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+            for (int i = 64 * rh; i < 64 * rh + 64; ++i) {
+                const float sv = s.S[i * kMaxHeadDim + j];
+                const float4 k4 = *reinterpret_cast<const float4*>(&s.kT[i][4 * th]);
+                const float4 q4 = *reinterpret_cast<const float4*>(&s.qT[i][4 * th]);
+                px[0] = fmaf(k4.x, sv, px[0]); px[1] = fmaf(k4.y, sv, px[1]);
+                px[2] = fmaf(k4.z, sv, px[2]); px[3] = fmaf(k4.w, sv, px[3]);
+                py[0] = fmaf(q4.x, sv, py[0]); py[1] = fmaf(q4.y, sv, py[1]);
+                py[2] = fmaf(q4.z, sv, py[2]); py[3] = fmaf(q4.w, sv, py[3]);
             }
+            if (rh == 1) {
 #pragma unroll
-            for (int r = 0; r < NR; ++r) {
-                if (VEC4) {  // this lane's four adjacent columns as one vector
-                    *reinterpret_cast<float4*>(&s.red[2 * r][w][4 * lane]) =
-                        make_float4(px[r][0], px[r][1], px[r][2], px[r][3]);
-                    *reinterpret_cast<float4*>(&s.red[2 * r + 1][w][4 * lane]) =
-                        make_float4(py[r][0], py[r][1], py[r][2], py[r][3]);
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const int j = col_of<false>(lane, c);
-                        s.red[2 * r][w][j] = px[r][c];
-                        s.red[2 * r + 1][w][j] = py[r][c];
-                    }
+                for (int r = 0; r < 4; ++r) {
+                    s.red[0][4 * th + r][j] = px[r];
+                    s.red[1][4 * th + r][j] = py[r];
                 }
             }
             __syncthreads();
-            // the sums over the warps, in a fixed order: thread (job, column)
+            if (rh == 0) {
 #pragma unroll
-            for (int e = tid; e < 2 * NR * kMaxHeadDim; e += NT) {
-                const int jb = e / kMaxHeadDim, j = e % kMaxHeadDim;
-                float acc = 0.f;
-#pragma unroll
-                for (int ww = 0; ww < NWARP; ++ww) acc += s.red[jb][ww][j];
-                if (jb & 1) s.Y[r0 + (jb >> 1)][j] = acc;
-                else s.X[r0 + (jb >> 1)][j] = acc;
+                for (int r = 0; r < 4; ++r) {
+                    s.X[4 * th + r][j] = px[r] + s.red[0][4 * th + r][j];
+                    s.Y[4 * th + r][j] = py[r] + s.red[1][4 * th + r][j];
+                }
             }
         }
         // the coefficients of the solve and of the outputs
-        if (tid < NB * NB) {
-            const int t = tid / NB, i = tid % NB;
+        if (tid >= MT - TB * TB) {
+            const int e = tid - (MT - TB * TB), t = e / TB, i = e % TB;
             const float d = (i <= t) ? expf(s.gam[t] - s.gam[i]) : 0.f;
             s.A[t][i] = (i < t) ? s.beta[t] * d * s.kk[t][i] : 0.f;
             s.P[t][i] = (i <= t) ? d * s.kq[t][i] : 0.f;
@@ -426,9 +460,9 @@ __global__ void __launch_bounds__(NT, 2) decode_multi_kernel(DecodeArgs a) {
         // sums of o_t^2 per warp
         if (tid < kMaxHeadDim) {
             const int j = tid;
-            float u[NB], o[NB];
+            float u[TB], o[TB];
 #pragma unroll
-            for (int t = 0; t < NB; ++t) {
+            for (int t = 0; t < TB; ++t) {
                 float r = (j < V) ? s.beta[t] * (s.v[t][j] - s.Gam[t] * s.X[t][j]) : 0.f;
 #pragma unroll
                 for (int i = 0; i < t; ++i) r = fmaf(-s.A[t][i], u[i], r);
@@ -439,8 +473,8 @@ __global__ void __launch_bounds__(NT, 2) decode_multi_kernel(DecodeArgs a) {
                 o[t] = (j < V) ? y * rsK : 0.f;
             }
 #pragma unroll
-            for (int t = 0; t < NB; ++t) {
-                s.X[t][j] = u[t];
+            for (int t = 0; t < TB; ++t) {
+                s.X[t][j] = u[t] * s.dlast[t];  // the update pass needs D[last][t] u_t
                 s.Y[t][j] = o[t];
                 const float sq = warp_sum(o[t] * o[t]);
                 if (lane == 0) s.ssq[t][w] = sq;
@@ -448,7 +482,7 @@ __global__ void __launch_bounds__(NT, 2) decode_multi_kernel(DecodeArgs a) {
         }
         __syncthreads();
         // 6. RMSNormGated of each real token
-        for (int e = tid; e < nt * kMaxHeadDim; e += NT) {
+        for (int e = tid; e < nt * kMaxHeadDim; e += MT) {
             const int t = e / kMaxHeadDim, j = e % kMaxHeadDim;
             if (j >= V) continue;
             float ms = 0.f;
@@ -461,72 +495,50 @@ __global__ void __launch_bounds__(NT, 2) decode_multi_kernel(DecodeArgs a) {
             const size_t row = (size_t)(t0 + t) * BH + (size_t)bh;
             a.out[row * V + j] = __float2bfloat16_rn(y);
         }
-        // 7. S_last = Gamma_last S0 + sum_t D[last][t] k^_t u_t^T in the registers, token
-        // by token (a padding token adds exact zeros)
-        const float Gl = s.Gam[NB - 1];
+        // 7. S_last = Gamma_last S0 + sum_t D[last][t] k^_t u_t^T: thread (column j, rows
+        // 32 rq .. 32 rq + 31); written to global memory after the last block, else back
+        // to shared memory for the next one (a padding token adds exact zeros)
+        {
+            const int j = tid & (kMaxHeadDim - 1), rq = tid >> 7;
+            const float Gl = s.Gam[TB - 1];
+            float u[TB];
 #pragma unroll
-        for (int m = 0; m < MROWS; ++m)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) st[m][c] *= Gl;
-#pragma unroll
-        for (int t = 0; t < NB; ++t) {
-            float u4[4];
-            if (VEC4) {
-                const float4 x = *reinterpret_cast<const float4*>(&s.X[t][4 * lane]);
-                u4[0] = x.x, u4[1] = x.y, u4[2] = x.z, u4[3] = x.w;
-            } else {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) u4[c] = s.X[t][col_of<false>(lane, c)];
-            }
-            const float dl = s.dlast[t];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) u4[c] *= dl;
-#pragma unroll
-            for (int m4 = 0; m4 < MROWS; m4 += 4) {
-                const float4 k4 = *reinterpret_cast<const float4*>(&s.kn[t][r0w + m4]);
-                const float kv[4] = {k4.x, k4.y, k4.z, k4.w};
-#pragma unroll
-                for (int mm = 0; mm < 4; ++mm)
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) st[m4 + mm][c] = fmaf(kv[mm], u4[c], st[m4 + mm][c]);
-            }
-        }
-    }
-    // the state, written once
-#pragma unroll
-    for (int m = 0; m < MROWS; ++m) {
-        const int i = r0w + m;
-        if (i >= K) continue;
-        if (VEC4) {
-            __stcs(reinterpret_cast<float4*>(S1 + (size_t)i * V) + lane,
-                   make_float4(st[m][0], st[m][1], st[m][2], st[m][3]));
-        } else {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int j = col_of<false>(lane, c);
-                if (j < V) __stcs(S1 + (size_t)i * V + j, st[m][c]);
+            for (int t = 0; t < TB; ++t) u[t] = s.X[t][j];
+#pragma unroll 4
+            for (int i = 32 * rq; i < 32 * rq + 32; ++i) {
+                const float4 k0 = *reinterpret_cast<const float4*>(&s.kT[i][0]);
+                const float4 k1 = *reinterpret_cast<const float4*>(&s.kT[i][4]);
+                float x = Gl * s.S[i * kMaxHeadDim + j];
+                x = fmaf(k0.x, u[0], x); x = fmaf(k0.y, u[1], x);
+                x = fmaf(k0.z, u[2], x); x = fmaf(k0.w, u[3], x);
+                x = fmaf(k1.x, u[4], x); x = fmaf(k1.y, u[5], x);
+                x = fmaf(k1.z, u[6], x); x = fmaf(k1.w, u[7], x);
+                if (last) {
+                    if (i < K && j < V) __stcs(S1 + (size_t)i * V + j, x);
+                } else {
+                    s.S[i * kMaxHeadDim + j] = x;
+                }
             }
         }
     }
 }
 
-// Launches the chunk form with NB tokens per block.
-template <bool VEC4, int NB>
+template <bool FULL>
 cudaError_t launch_multi(const DecodeArgs& a, cudaStream_t stream) {
     static cudaError_t attr = [] {
         // shared memory above the default 48 KB, and the largest carveout so that two CTAs
         // fit an SM
-        cudaError_t e = cudaFuncSetAttribute(decode_multi_kernel<VEC4, NB>,
+        cudaError_t e = cudaFuncSetAttribute(decode_multi_kernel<FULL>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)sizeof(MultiSmem));
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(decode_multi_kernel<VEC4, NB>,
+            e = cudaFuncSetAttribute(decode_multi_kernel<FULL>,
                                      cudaFuncAttributePreferredSharedMemoryCarveout,
                                      (int)cudaSharedmemCarveoutMaxShared);
         return e;
     }();
     if (attr != cudaSuccess) return attr;
-    decode_multi_kernel<VEC4, NB><<<a.BH, NT, sizeof(MultiSmem), stream>>>(a);
+    decode_multi_kernel<FULL><<<a.BH, MT, sizeof(MultiSmem), stream>>>(a);
     return cudaGetLastError();
 }
 
@@ -553,8 +565,8 @@ cudaError_t launch_decode(const DecodeArgs& args, cudaStream_t stream) {
     // several tokens NWARP at a time.
     constexpr int kPerTokenMaxT = 4;
     if (a.T > kPerTokenMaxT)
-        return a.V == kMaxHeadDim ? launch_multi<true, TB>(a, stream)
-                                  : launch_multi<false, TB>(a, stream);
+        return (a.K == kMaxHeadDim && a.V == kMaxHeadDim) ? launch_multi<true>(a, stream)
+                                                          : launch_multi<false>(a, stream);
     if (a.V == kMaxHeadDim) {
         if (a.T == 1) decode_kernel<true, 1><<<a.BH, NT, 0, stream>>>(a);
         else decode_kernel<true, NWARP><<<a.BH, NT, 0, stream>>>(a);
@@ -563,6 +575,16 @@ cudaError_t launch_decode(const DecodeArgs& args, cudaStream_t stream) {
         else decode_kernel<false, NWARP><<<a.BH, NT, 0, stream>>>(a);
     }
     return cudaGetLastError();
+}
+
+uint32_t decode_take_status() {
+    uint32_t bits = 0;
+    if (cudaMemcpyFromSymbol(&bits, g_decode_status, sizeof(bits)) != cudaSuccess) return 0;
+    if (bits != 0) {
+        const uint32_t zero = 0;
+        cudaMemcpyToSymbol(g_decode_status, &zero, sizeof(zero));
+    }
+    return bits;
 }
 
 }  // namespace gdn

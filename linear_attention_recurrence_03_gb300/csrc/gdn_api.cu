@@ -359,7 +359,8 @@ gdn_status gdn_get_device_status(void* stream) {
     const cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return fail(GDN_ECUDA, "gdn_get_device_status: %s", cudaGetErrorString(e));
-    const uint32_t bits = gdn::prefill_tc_take_status() | gdn::tril_take_status();
+    const uint32_t bits =
+        gdn::prefill_tc_take_status() | gdn::tril_take_status() | gdn::decode_take_status();
     if (bits & gdn::kStatusBadSeqlens)
         return fail(GDN_EINVAL, "gdn_prefill_varlen: cu_seqlens was not 0 = cu[0] <= ... <= "
                     "cu[N] <= T; every sequence was treated as empty");

@@ -124,5 +124,6 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 // bits set since the last call and clears them (the stream must be synchronised).
 uint32_t prefill_tc_take_status();
 uint32_t tril_take_status();
+uint32_t decode_take_status();
 
 }  // namespace gdn

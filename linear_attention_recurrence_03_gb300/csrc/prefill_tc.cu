@@ -135,7 +135,13 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 #define GDN_SEGMENT_GROWTH_PERMILLE 1220
 #endif
 constexpr int kOverlapSegments = GDN_OVERLAP_SEGMENTS;
-constexpr int kMinSegmentChunks = 8;
+// (Below two segments of this many chunks the boundary costs more than the prep it hides:
+// S = 1024 on 16 heads ran 55 us as two segments of 8 chunks and 40 us as one; S = 2048
+// 81 us as two of 16 and 66 us as one; from 64 chunks on two segments win.)
+#ifndef GDN_MIN_SEGMENT_CHUNKS
+#define GDN_MIN_SEGMENT_CHUNKS 24
+#endif
+constexpr int kMinSegmentChunks = GDN_MIN_SEGMENT_CHUNKS;
 constexpr int kSegmentGrowthPermille = GDN_SEGMENT_GROWTH_PERMILLE;
 // 1: a carry segment is launched as a programmatic dependent of the one before it, so its
 // setup overlaps that one's last chunks (the state is read after griddepcontrol.wait).

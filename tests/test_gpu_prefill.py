@@ -184,7 +184,7 @@ def test_prefill_overlapped_segments_equal_one_pass():
     crosses segments in fp32, so the result equals the one-segment run (the static
     scratch of gdn_prefill_noalloc holds this whole sequence) bit for bit, and matches the
     oracle on sampled heads."""
-    w = syn.shrink(syn.PREFILL_BF16_GQA2, B=1, Hk=4, Hv=8, S=64 * 40 - 17, state_std=0.05)
+    w = syn.shrink(syn.PREFILL_BF16_GQA2, B=1, Hk=4, Hv=8, S=64 * 56 - 17, state_std=0.05)
     x = syn.prefill_inputs(w)
     args = [x[n].to(DEV) for n in ("q", "k", "v", "g_log", "beta")]
     st0 = x["state"].to(DEV)
