@@ -61,8 +61,8 @@ typedef enum gdn_tril_algorithm {
 /*
  * gdn_prefill_workspace_bytes -- scratch (device memory) gdn_prefill needs for this
  * shape. Returns 0 when no workspace is needed, or (size_t)-1 if the shape is invalid.
- * The bf16 path with Dk = Dv = 128 (the tensor-core kernels) needs 66064 bytes per
- * (batch, value head, 64-token chunk): B * Hv * ceil(S / 64) * 66064; every other
+ * The bf16 path with Dk = Dv = 128 (the tensor-core kernels) needs 49680 bytes per
+ * (batch, value head, 64-token chunk): B * Hv * ceil(S / 64) * 49680; every other
  * shape needs none.
  */
 size_t gdn_prefill_workspace_bytes(int B, int Hk, int Hv, int S, int Dk, int Dv,
@@ -105,7 +105,7 @@ gdn_status gdn_prefill(const void* q, const void* k, const void* v,
 /*
  * gdn_prefill_varlen_workspace_bytes -- device scratch gdn_prefill_varlen needs for N
  * sequences packed into T tokens: on the bf16 Dk = Dv = 128 path (tensor cores)
- * Hv * (ceil(T / 64) + N) * 66064 bytes rounded up to 256, plus 4 * (N + 2); on every
+ * Hv * (ceil(T / 64) + N) * 49680 bytes rounded up to 256, plus 4 * (N + 2); on every
  * other path 4 * (N + 2) rounded up to 16. (size_t)-1 for an invalid shape.
  */
 size_t gdn_prefill_varlen_workspace_bytes(int N, int Hk, int Hv, int T, int Dk, int Dv,
@@ -153,10 +153,10 @@ gdn_status gdn_prefill_varlen(const void* q, const void* k, const void* v, const
  *
  * Arguments, results and errors as gdn_prefill (the caller still passes inputs, state and
  * out). On the tensor-core path (bf16, Dk = Dv = 128) the sequence is processed in segments
- * of whole 64-token chunks that fit the scratch -- 128 MiB / 66064 bytes per (batch, value
- * head, chunk) unit = 2031 units -- the state carrying over in fp32 from one segment to the
+ * of whole 64-token chunks that fit the scratch -- 128 MiB / 49680 bytes per (batch, value
+ * head, chunk) unit = 2701 units -- the state carrying over in fp32 from one segment to the
  * next, so the result equals gdn_prefill's. GDN_EUNSUPPORTED, with a message, when B * Hv
- * exceeds 2031 (not even one chunk per head fits). Every other path needs no scratch and
+ * exceeds 2701 (not even one chunk per head fits). Every other path needs no scratch and
  * runs as gdn_prefill.
  *
  * The first call on each device looks up the array's device address (with that device

@@ -158,14 +158,12 @@ constexpr int kMaxSegments = 8;
 constexpr bool kCarrySplit = GDN_CARRY_SPLIT != 0;
 
 // ---- workspace: per (batch, value head, chunk) unit, bf16 tiles of 64 rows x 64 columns
-// in the 128-byte swizzled layout, T_U | P | W[:, 0:64] | W[:, 64:128] | Q~[:, 0:64] |
-// Q~[:, 64:128] | K~[:, 0:64] | K~[:, 64:128], then the carry's decay scalars, with
-// Q~ = diag(Gamma) Q and K~ = diag(exp(gamma_last - gamma)) K. The Q~ and K~ tiles are
-// written only for the two-slice carry (latency-bound: the row decays are applied before
-// it runs); the transposed carry reads q and k itself and applies the decays in its own
-// steps, so its units carry T_U, P, W and the scalars only (half the traffic).
-constexpr uint32_t WS_TU = 0, WS_P = 8192, WS_W = 16384, WS_QT = 32768, WS_KT = 49152,
-                   WS_CS = 65536;
+// in the 128-byte swizzled layout, T_U | P | W[:, 0:64] | W[:, 64:128] | K~[:, 0:64] |
+// K~[:, 64:128], then the carry's decay scalars, with K~ = diag(exp(gamma_last - gamma)) K.
+// The K~ tiles are written only for the two-slice carry, whose chain reads them (its U
+// step then writes one tile); the transposed carry reads k itself and applies the decays
+// in its own steps. Both carries read q and apply diag(Gamma) to the rows of Q S0.
+constexpr uint32_t WS_TU = 0, WS_P = 8192, WS_W = 16384, WS_KT = 32768, WS_CS = 49152;
 
 struct CarryScalars {
     float kdec[C];  // exp(gamma_last - gamma_r)
@@ -217,23 +215,24 @@ constexpr uint32_t PT_COLS = 128;
 enum { PB_FULL = 0, PB_GRAM, PB_PREP, PB_WDONE, PB_DRAIN, PB_COUNT };
 
 // ---- carry kernel: one CTA per (NS-column slice of the state, value head, batch), NS = 64
-// or 128 (CarryCfg<NS>). Shared memory map:
+// (CarryCfg<NS>; the transposed carry shares the stage layout with NS = 128). Shared
+// memory map:
 //   stage s (two stages, one chunk each), in two copy groups:
-//     block b (Dk columns 64b..64b+63): W_b | Q~_b | K~_b (8 KB each, stride 24 KB)
-//       ([W_b; Q~_b] is one 128-row operand), then P ([K~_1; P] one operand),
+//     block b (Dk columns 64b..64b+63): W_b | Q_b | K~_b (8 KB each, stride 24 KB)
+//       ([W_b; Q_b] is one 128-row operand), then P ([K~_1; P] one operand),
 //     V slice (64 tokens x NS columns, in 64-column blocks), T_U ([T_U; -] one operand)
-//     early group (read by U~ and [W; Q~] S0, freed as soon as they complete): W, Q~, V,
+//     early group (read by U~ and [W; Q] S0, freed as soon as they complete): W, q, V,
 //     T_U; late group (read by K~^T U, P U and the state update): K~, P and the scalars
-//     (the transposed carry loads q and k into the Q~ and K~ slots)
+//     (the transposed carry loads k into the K~ slots)
 //   two U tiles (64 tokens x NS, by chunk parity), the bf16 state operand (128 x NS,
 //   64-column blocks), per-stage scalars, barriers
-// warp 0: producer; warp 2: MMA issuer (an SM sub-partition whose SIMT warps only write the
-// output); warps 4..11: SIMT; warps 1 and 3 only take part in the setup and the teardown
+// warp 0: producer; warp 1 (one thread): MMA issuer; warps 4..11: SIMT; warps 2 and 3
+// only take part in the setup and the teardown
 constexpr int CARRY_THREADS = 384;
 constexpr uint32_t BLK_STRIDE = 24576;
 constexpr uint32_t OFF_W = 0, OFF_Q = 8192, OFF_K = 16384;
 constexpr uint32_t OFF_P = 49152, OFF_V = 57344;
-static_assert(OFF_P == BLK_STRIDE + OFF_K + 8192, "[K_1; P] is one 128-row operand");
+static_assert(OFF_P == BLK_STRIDE + OFF_K + 8192, "[K~_1; P] is one 128-row operand");
 
 template <int NS>
 struct CarryCfg {
@@ -250,18 +249,21 @@ struct CarryCfg {
     static constexpr uint32_t SMEM = MISC + 64 + 1024;
     // TMEM (fp32 columns), two buffers of each kind by chunk parity:
     //   B[p]: U~ of the chunk (upper half), then, once U is formed, its state increment
-    //   A[p]: [W S0; Q~ S0], then [-; Q~ S0 + P U] (the un-scaled output)
-    static constexpr uint32_t TMB = 0, TMA = 2 * NS;
-    static constexpr uint32_t TMCOLS = 4 * NS;
+    //   A[p]: [W S0; Q S0]
+    //   C[p]: [-; P U]
+    // The output of token r is scale (Gamma_r (Q S0)_r + (P U)_r).
+    static constexpr uint32_t TMB = 0, TMA = 2 * NS, TMC = 4 * NS;
+    static constexpr uint32_t TMCOLS = 6 * NS <= 256 ? 256 : 512;
     static_assert(BAR % 8 == 0 && SCAL % 16 == 0, "barrier and copy alignment");
-    static_assert(SMEM <= 232448, "shared memory budget");
+    static_assert(NS != 64 || SMEM <= 232448, "shared memory budget");
 };
 
 // FULLE/EMPTYE: the early copy group of stage s; FULLL/EMPTYL: the late group
 enum {
     B_FULLE0 = 0, B_FULLE1, B_FULLL0, B_FULLL1, B_EMPTYE0, B_EMPTYE1, B_EMPTYL0, B_EMPTYL1,
-    B_ADONE, B_SDONE, B_CDONE, B_DRAIN, B_UREADY, B_SREADY, B_COUNT
+    B_ADONE, B_SDONE, B_CDONE, B_DRAIN, B_COUNT
 };
+static_assert(B_COUNT * 8 <= 128, "carry barrier block");
 
 // status bits
 constexpr uint32_t ST_PRODUCER = 1u, ST_MMA = 2u, ST_CARRY = 4u, ST_PREP = 8u;
@@ -284,8 +286,8 @@ struct TcArgs {
     const int* cu;
     const int* cb;
     int N;
-    // the prep writes Q~ and K~ to the workspace (for the two-slice carry)
-    int export_qk;
+    // the prep writes K~ to the workspace (for the two-slice carry)
+    int export_k;
 };
 
 __device__ __forceinline__ size_t ws_offset(int b, int h, int c, int Hv, int nch) {
@@ -417,6 +419,13 @@ __device__ __forceinline__ bool wait_hot(uint64_t* bar, uint32_t parity, volatil
             return false;
         }
     }
+}
+
+// The waits of the two-slice carry's chain (SIMT warps on the MMA groups, the issuer on the
+// late copy group) poll without a suspend hint: ~50 cycles sooner per hand-off.
+__device__ __forceinline__ bool wait_chain(uint64_t* bar, uint32_t parity,
+                                           volatile int* abort_flag, uint32_t bit) {
+    return wait_hot(bar, parity, abort_flag, bit);
 }
 
 // Lower-triangular 16x16 block index of block (i, j), i >= j.
@@ -560,7 +569,7 @@ __device__ __forceinline__ void issue_carry1(uint32_t tmem, uint32_t st, uint32_
     }
 }
 
-// carry: the state increment K^T U' over the tokens (K read M-major), into `tb`
+// carry: the state increment K~^T U over the tokens (K~ read M-major), into `tb`
 template <int NS>
 __device__ __forceinline__ void issue_carry3(uint32_t tmem, uint32_t st, uint32_t u_tile,
                                              uint32_t tb) {
@@ -572,17 +581,17 @@ __device__ __forceinline__ void issue_carry3(uint32_t tmem, uint32_t st, uint32_
         mma_bf16(tmem + tb, dadd(ak, k * 2048), dadd(bu2, k * 2048), id, k > 0);
 }
 
-// carry: [K_1 U; P U] = [K_1; P] U, accumulated onto [W S0; diag(Gamma) Q S0] in `ta`: the
-// lower half becomes the un-scaled output diag(Gamma) Q S0 + P U (the upper half is no
-// longer needed)
+// carry: [K~_1 U; P U] = [K~_1; P] U into the TMEM buffer `tc` (the upper half, over the
+// K~ block that precedes P, is not used)
 template <int NS>
 __device__ __forceinline__ void issue_carry2(uint32_t tmem, uint32_t st, uint32_t u_tile,
-                                             uint32_t ta) {
+                                             uint32_t tc) {
     constexpr uint32_t id = idesc_bf16(128, NS, false, true);
     const uint64_t ap = smem_desc_sw128(st + OFF_P - 8192, 16, 1024);
     const uint64_t bu = smem_desc_sw128(u_tile, 8192, 1024);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) mma_bf16(tmem + ta, dadd(ap, k * 32), dadd(bu, k * 2048), id, 1);
+    for (int k = 0; k < 4; ++k)
+        mma_bf16(tmem + tc, dadd(ap, k * 32), dadd(bu, k * 2048), id, k > 0);
 }
 
 // ---------------------------------------------------------------- the prep kernel
@@ -753,35 +762,6 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
             tc_fence_after();
             if (P == 0) TRACE_PREP(23);
 
-            // ---- Q~ = diag(Gamma) Q and (later, beside the diagonal solve) K~ =
-            // diag(exp(gamma_last - gamma)) K straight to the workspace; 16-byte chunk j of
-            // the two 64-column blocks, same swizzled position
-            uint8_t* wsu = a.ws + ws_offset(b, h, cl, a.Hv, nch);
-            auto export_rows = [&](int j, bool isq) {
-                const CarryScalars& cs = *reinterpret_cast<const CarryScalars*>(sm + P_CS);
-                const int blk = j >> 9, off = (j & 511) * 16, row = (j & 511) >> 3;
-                // one packed bf16 product per pair (the row factor rounded to bf16)
-                const __nv_bfloat162 f2 =
-                    __float2bfloat162_rn(isq ? sc.Gam[row] : cs.kdec[row]);
-                const uint4 x = *reinterpret_cast<const uint4*>(
-                    sm + blk * PQ_STRIDE + (isq ? PQ_Q : PQ_K) + off);
-                const uint32_t in[4] = {x.x, x.y, x.z, x.w};
-                uint32_t o[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const __nv_bfloat162 r =
-                        __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&in[e]), f2);
-                    o[e] = *reinterpret_cast<const uint32_t*>(&r);
-                }
-                *reinterpret_cast<uint4*>(wsu + (isq ? WS_QT : WS_KT) + blk * 8192 + off) =
-                    make_uint4(o[0], o[1], o[2], o[3]);
-            };
-            if (a.export_qk) {
-#pragma unroll
-                for (int it = 0; it < 4; ++it) export_rows(P + 256 * it, true);
-                bar_sync(2, 256);  // every Q chunk is read before A overwrites the Q slots
-            }
-
             // ---- P (bf16 tile) and A (fp32 blocks) from the Gram matrices: thread (wg, L)
             // takes row L of [QK^T; KK^T], columns 16 bj + 8 wg .. + 7 of every 16-block bj.
             // A warp's rows fill the two row blocks bq, bq + 1, so blocks left of bq and
@@ -852,8 +832,8 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
             // diagonal blocks (prep warps 0 and 1): forward substitution, one thread per
             // column of the block's inverse, its 16 entries in registers. The rows go in
             // lockstep, so the threads of a block read the same A entry (a broadcast);
-            // the column's zeros above its diagonal keep the full sums exact. Meanwhile
-            // warps 2..7 write K~ to the workspace (when it is exported).
+            // the column's zeros above its diagonal keep the full sums exact.
+            // Meanwhile warps 2..7 write K~ to the workspace (when it is exported).
             if (P < 64) {
                 const int i = P >> 4, cc = P & 15;
                 const float* Ad = Ablk(i, i);
@@ -873,8 +853,27 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
                 float* Td = Tb + bidx(i, i) * 16 * BS;
 #pragma unroll
                 for (int m = 0; m < 16; ++m) Td[m * BS + cc] = __uint_as_float(to_tf32(x[m]));
-            } else if (a.export_qk) {
-                for (int j = P - 64; j < 1024; j += 192) export_rows(j, false);
+            } else if (a.export_k) {
+                // meanwhile K~ = diag(exp(gamma_last - gamma)) K goes straight to the
+                // workspace: 16-byte chunk j of the two 64-column blocks, same swizzled
+                // position, one packed bf16 product per pair (the row factor rounded to bf16)
+                const CarryScalars& cs = *reinterpret_cast<const CarryScalars*>(sm + P_CS);
+                uint8_t* wsk = a.ws + ws_offset(b, h, cl, a.Hv, nch) + WS_KT;
+                for (int j = P - 64; j < 1024; j += 192) {
+                    const int blk = j >> 9, off = (j & 511) * 16, row = (j & 511) >> 3;
+                    const __nv_bfloat162 f2 = __float2bfloat162_rn(cs.kdec[row]);
+                    const uint4 x = *reinterpret_cast<const uint4*>(sm + blk * PQ_STRIDE + PQ_K + off);
+                    const uint32_t in[4] = {x.x, x.y, x.z, x.w};
+                    uint32_t o[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const __nv_bfloat162 r =
+                            __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&in[e]), f2);
+                        o[e] = *reinterpret_cast<const uint32_t*>(&r);
+                    }
+                    *reinterpret_cast<uint4*>(wsk + blk * 8192 + off) =
+                        make_uint4(o[0], o[1], o[2], o[3]);
+                }
             }
             bar_sync(2, 256);
             if (P == 0) TRACE_PREP(25);
@@ -993,22 +992,26 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
 // ---------------------------------------------------------------- the carry kernel
 
 // One CTA per (NS-column slice of the state, value head h, batch b), sequential over
-// chunks. Warp 0 streams the chunk's v slice (TMA) and the prep's tiles and scalars
-// (bulk copies) into a two-stage ring; warp 2 (one thread) issues every MMA; warps 4..11
-// (two per TMEM lane quadrant, thread = state row L, NS/2 columns) keep the fp32 state in
-// registers, form U (rows 0-63) while writing the previous chunk's output (rows 64-127),
-// and update the state. MMA order per chunk c: [W; Q~] S0, U~ of chunk c+1 if it has
-// landed, then K~^T U, U~ of chunk c+1 if not issued yet, P U.
+// chunks. Warp 0 streams the chunk's q and v slice (TMA) and the prep's tiles and
+// scalars (bulk copies) into a two-stage ring; warps 4..11 (two per TMEM lane quadrant,
+// thread = state row L, NS/2 columns) keep the fp32 state in registers, form U (rows
+// 0-63, the U warps 4, 5, 8, 9) while writing the previous chunk's output (rows 64-127, the
+// output warps 6, 7, 10, 11), and update the state; one thread of warp 1 issues every MMA.
+// MMA order per chunk c: [W; Q] S0, U~ of chunk c+1 if it has landed, then K~^T U, U~ of
+// chunk c+1 if not issued yet, P U. (Every MMA comes from the one thread: the tensor pipe
+// takes about one tcgen05.mma per 44 cycles whichever thread issues it, so a second issuer
+// only puts the off-chain MMAs in front of the chain's.)
 
 // The producer of a carry CTA (one thread): streams chunk c (token rows tbase + 64 c) into
-// the two-stage ring, in the early (W, Q~ or q, V, T_U) and late (K~ or k, P, scalars) copy
+// the two-stage ring, in the early (W, q, V, T_U) and late (K~ or k, P, scalars) copy
 // groups: the prep's tiles and scalars from the head's workspace units (from `wsh`), the V
-// slice (columns n0 .. n0 + NS - 1, tensor z = zv), and either the prep's Q~ and K~
-// (qk_ws) or q and k of the key head (tensor z = zq, both 64-column blocks).
+// slice (columns n0 .. n0 + NS - 1, tensor z = zv), q of the key head (tensor z = zq, both
+// 64-column blocks) and either the prep's K~ (kt_ws, for the two-slice carry) or k of the
+// key head (for the transposed carry, which also has chunk c + 2 prefetched into L2).
 template <int NS>
 __device__ __forceinline__ void carry_produce(uint8_t* sm, uint64_t* bar, CarryScalars* scal,
                                               const CUtensorMap* mqp, const CUtensorMap* mkp,
-                                              const CUtensorMap* mvp, bool qk_ws,
+                                              const CUtensorMap* mvp, bool kt_ws,
                                               const uint8_t* wsh, int nch, int n0, int tbase,
                                               int zq, int zv, volatile int* abort_flag) {
     using Cfg = CarryCfg<NS>;
@@ -1021,19 +1024,18 @@ __device__ __forceinline__ void carry_produce(uint8_t* sm, uint64_t* bar, CarryS
         uint8_t* st = sm + s * Cfg::STAGE;
         const uint8_t* wsc = wsh + (size_t)c * WS_UNIT;
         const int t = tbase + c * C;
-        // early group of chunk c: W, Q~ or q, V, T_U
+        // early group of chunk c: W, q, V, T_U
         if (c >= 2 && !wait_or_abort(&bar[B_EMPTYE0 + s], ((c >> 1) + 1) & 1, abort_flag,
                                      ST_PRODUCER))
             break;
         if (*abort_flag) break;
-        TRACE(c, 0);
+        TRACE(c, 19);
         uint64_t* fe = &bar[B_FULLE0 + s];
         mbar_arrive_expect_tx(fe, 4 * 8192 + Cfg::NB * 8192 + 8192);
         for (int blk = 0; blk < 2; ++blk) {
             uint8_t* sb = st + blk * BLK_STRIDE;
             bulk_g2s(sb + OFF_W, wsc + WS_W + blk * 8192, 8192, fe);
-            if (qk_ws) bulk_g2s(sb + OFF_Q, wsc + WS_QT + blk * 8192, 8192, fe);
-            else tma_load_3d(sb + OFF_Q, mqp, fe, blk * 64, t, zq);
+            tma_load_3d(sb + OFF_Q, mqp, fe, blk * 64, t, zq);
         }
         for (int blk = 0; blk < Cfg::NB; ++blk)
             tma_load_3d(st + OFF_V + blk * 8192, mvp, fe, n0 + blk * 64, t, zv);
@@ -1044,28 +1046,28 @@ __device__ __forceinline__ void carry_produce(uint8_t* sm, uint64_t* bar, CarryS
                                      ST_PRODUCER))
             break;
         uint64_t* fl = &bar[B_FULLL0 + s];
+        TRACE(c, 18);
         mbar_arrive_expect_tx(fl, 3 * 8192 + (uint32_t)sizeof(CarryScalars));
         for (int blk = 0; blk < 2; ++blk) {
             uint8_t* dk = st + blk * BLK_STRIDE + OFF_K;
-            if (qk_ws) bulk_g2s(dk, wsc + WS_KT + blk * 8192, 8192, fl);
+            if (kt_ws) bulk_g2s(dk, wsc + WS_KT + blk * 8192, 8192, fl);
             else tma_load_3d(dk, mkp, fl, blk * 64, t, zq);
         }
         bulk_g2s(st + OFF_P, wsc + WS_P, 8192, fl);
         bulk_g2s(&scal[s], wsc + WS_CS, sizeof(CarryScalars), fl);
         lastL[s] = c;
-        // chunk c + 2 goes to L2 now (only the parts of the unit that were written), for
-        // the transposed carry, whose full waves are bound by HBM bandwidth. The two-slice
-        // carry does without: the prefetches share the SM's copy engine with the chunk
-        // loads its chain waits for (a traced chunk takes about 2.6K cycles without them,
-        // 2.9K with).
-        if (!qk_ws && c + 2 < nch) {
+        // chunk c + 2 goes to L2 now, for the transposed carry, whose full waves are bound
+        // by HBM bandwidth. The two-slice carry does without: the prefetches share the
+        // SM's copy engine with the chunk loads its chain waits for (a traced chunk took
+        // about 2.6K cycles without them, 2.9K with).
+        if (!kt_ws && c + 2 < nch) {
             const int t2 = t + 2 * C;
             for (int blk = 0; blk < Cfg::NB; ++blk) tma_prefetch_l2_3d(mvp, n0 + blk * 64, t2, zv);
             for (int blk = 0; blk < 2; ++blk) {
                 tma_prefetch_l2_3d(mqp, blk * 64, t2, zq);
                 tma_prefetch_l2_3d(mkp, blk * 64, t2, zq);
             }
-            bulk_prefetch_l2(wsc + 2 * WS_UNIT, WS_QT);
+            bulk_prefetch_l2(wsc + 2 * WS_UNIT, WS_KT);
             bulk_prefetch_l2(wsc + 2 * WS_UNIT + WS_CS, sizeof(CarryScalars));
         }
     }
@@ -1079,6 +1081,12 @@ __device__ __forceinline__ void carry_produce(uint8_t* sm, uint64_t* bar, CarryS
         if (lastL[s] >= 0) mbar_wait_bounded(&bar[B_FULLL0 + s], (lastL[s] >> 1) & 1, kWaitNs);
     }
 }
+
+
+// The MMA issuer's warp. Warp 1 shares its SM sub-partition with the U warps 5 and 9,
+// which wait while [W; Q] S0 is issued; the partitions of warps 2 and 3 hold the output
+// warps, which are then writing the previous chunk.
+constexpr int kIssuerWarp = 1;
 
 template <int NS>
 __global__ void __launch_bounds__(CARRY_THREADS, 1)
@@ -1120,8 +1128,7 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
     }
 
     if (tid == 0) {
-        for (int i = 0; i < B_COUNT; ++i)
-            mbar_init(&bar[i], (i == B_UREADY || i == B_SREADY) ? 8 : 1);
+        for (int i = 0; i < B_COUNT; ++i) mbar_init(&bar[i], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -1143,9 +1150,9 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
                               wb * a.Hk + h / (a.Hv / a.Hk), wb * a.Hv + h, abort_flag);
 
         }
-    } else if (warp == 2 || warp >= 4) {
-        // ----------------------------------------- carry (warps 2, 4..11: 288 threads)
-        const bool issuer = warp == 2;
+    } else if (warp == kIssuerWarp || warp >= 4) {
+        // ----------------------------------------- carry (issuer warp, 4..11: 288 threads)
+        const bool issuer = warp == kIssuerWarp;
         const bool leader = issuer && lane == 0;
         const int q = warp & 3, hc = issuer ? 0 : (warp - 4) >> 2;
         const int L = 32 * q + lane;
@@ -1179,23 +1186,27 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
             for (int p = 0; p < NP; ++p) write_row32(s_base + 16384u * pblk(p), L, pch(p), Sr + 32 * p);
         }
 
-        // out = scale (Q~ S0 + P U) of chunk cc for token L - 64 (quadrants 2, 3)
-        auto write_out = [&](int cc) {
+        // out = scale (Gamma_r (Q S0)_r + (P U)_r) of chunk cc for token r = L - 64
+        // (quadrants 2, 3), with gsc = scale Gamma_r
+        auto write_out = [&](int cc, float gsc) {
             const int t = tbase + cc * C + (L - 64);
             const uint32_t ta = Cfg::TMA + (uint32_t)NS * (uint32_t)(cc & 1);
+            const uint32_t tcb = Cfg::TMC + (uint32_t)NS * (uint32_t)(cc & 1);
 #pragma unroll
             for (int p = 0; p < NP; ++p) {
-                float o[32];
-                tmem_ld32(tmem + lane_off + ta + 32 * p, o);
+                float o[32], pu[32];
+                tmem_ld32x2(tmem + lane_off + ta + 32 * p, tmem + lane_off + tcb + 32 * p, o, pu);
                 if (t < tend) {
                     uint4* dst = reinterpret_cast<uint4*>(gout + (size_t)t * 128 + 32 * p);
 #pragma unroll
+                    for (int j = 0; j < 32; ++j) o[j] = fmaf(gsc, o[j], a.scale * pu[j]);
+#pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         uint4 w;
-                        w.x = pack_bf16(a.scale * o[8 * j + 0], a.scale * o[8 * j + 1]);
-                        w.y = pack_bf16(a.scale * o[8 * j + 2], a.scale * o[8 * j + 3]);
-                        w.z = pack_bf16(a.scale * o[8 * j + 4], a.scale * o[8 * j + 5]);
-                        w.w = pack_bf16(a.scale * o[8 * j + 6], a.scale * o[8 * j + 7]);
+                        w.x = pack_bf16(o[8 * j + 0], o[8 * j + 1]);
+                        w.y = pack_bf16(o[8 * j + 2], o[8 * j + 3]);
+                        w.z = pack_bf16(o[8 * j + 4], o[8 * j + 5]);
+                        w.w = pack_bf16(o[8 * j + 6], o[8 * j + 7]);
                         dst[j] = w;
                     }
                 }
@@ -1203,143 +1214,194 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
         };
 
         int mmas = 0, done = 0;
-        // SIMT warp -> issuer hand-offs (mbarriers, one arrival per SIMT warp):
-        //   SREADY #c: the state tile of chunk c is written (#0: the initial state) and the
-        //              output of chunk c-2 is read out of its TMEM buffer
-        //   UREADY #c: U of chunk c is in its tile and the output of chunk c-1 is written
-        auto warp_arrive = [&](int bi) {
+        // SIMT warp -> issuer hand-offs, named barriers that also OR a failure flag over
+        // their members (bar_any), so that every member learns at once that a wait ran out:
+        //   BAR_S #c (issuer warp + 8 SIMT warps): the state tile of chunk c is written
+        //            (#0: the initial state), the output of chunk c-2 is read out of TMEM
+        //   BAR_U #c (issuer warp + the 4 U warps): U of chunk c is in its tile
+        // Each member passes every barrier of every chunk in the same order until a BAR_S
+        // reports a failure; then all of them stop there together. Every wait between the
+        // barriers is bounded (and returns at once once the abort flag is set), so no
+        // member can keep another waiting at a barrier.
+        constexpr uint32_t BAR_S = 2, BAR_U = 3;
+        auto handoff = [&]() {
             fence_proxy_async_smem();
             tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar[bi]);
         };
-        if (!issuer) warp_arrive(B_SREADY);
-        bool ok = true;
-        if (leader) {
+        bool ok = true, fail = false;
+        // A failure seen by one lane (the issuing lane, or one lane's wait) becomes the whole
+        // warp's before the next warp-collective instruction (tcgen05.ld, bar.red), so that
+        // every lane of a warp always takes the same path to those.
+        auto warp_fail = [&]() { fail = __any_sync(0xffffffffu, fail); };
+        float gsc_prev = 0.f;  // output warps: scale Gamma_r of the previous chunk's row
+        if (issuer) {
             bool u_next = false;  // U~(c+1) already issued
-            ok = wait_or_abort(&bar[B_FULLE0], 0, abort_flag, ST_MMA);
-            if (ok) {
-                tc_fence_after();
-                issue_u<NS>(tmem, sbase, Cfg::TMB);
-                mmas = 1;
+            bool stopped = false;
+            if (leader) {
+                if (wait_chain(&bar[B_FULLE0], 0, abort_flag, ST_MMA)) {
+                    tc_fence_after();
+                    issue_u<NS>(tmem, sbase, Cfg::TMB);
+                    mmas = 1;
+                } else {
+                    fail = true;
+                }
             }
-            for (int c = 0; ok && c < nch; ++c) {
+            __syncwarp();
+            for (int c = 0; c < nch; ++c) {
                 const int s = c & 1;
                 const uint32_t st = sbase + s * Cfg::STAGE;
                 const uint32_t ta = Cfg::TMA + (uint32_t)NS * (uint32_t)s;
                 const uint32_t tb = Cfg::TMB + (uint32_t)NS * (uint32_t)s;
-                // MMA1 [W; Q~] S0 once the state tile of chunk c is complete
-                if (!wait_or_abort(&bar[B_SREADY], c & 1, abort_flag, ST_MMA)) break;
-                TRACE(c, 12);
-                tc_fence_after();
-                issue_carry1<NS>(tmem, st, s_base, ta);
-                // ADONE also covers U~(c) and P U(c-1), issued earlier (U of chunk c may
-                // overwrite the U tile P U(c-2) read)
-                tc_commit(&bar[B_ADONE]);
-                tc_commit(&bar[B_EMPTYE0 + s]);  // the early group of chunk c is read
-                TRACE(c, 3);
-                // U~(c+1) now if chunk c+1 has landed (it then runs while U is formed); its
-                // buffer was last read by the state update of chunk c-1
-                u_next = c + 1 < nch &&
-                         mbar_test_wait(&bar[B_FULLE0 + (s ^ 1)], ((c + 1) >> 1) & 1);
-                if (u_next) {
-                    issue_u<NS>(tmem, sbase + (s ^ 1) * Cfg::STAGE,
-                                Cfg::TMB + (uint32_t)NS * (uint32_t)(s ^ 1));
-                    TRACE(c + 1, 5);
+                // MMA1 [W; Q] S0 once the state tile of chunk c is complete
+                if (leader) TRACE(c, 24);
+                if (bar_any(BAR_S, 288, fail)) {
+                    stopped = true;
+                    break;
                 }
+                if (leader) {
+                    TRACE(c, 12);
+                    tc_fence_after();
+                    issue_carry1<NS>(tmem, st, s_base, ta);
+                    TRACE(c, 6);
+                    // ADONE also covers U~(c) and P U(c-1), issued earlier (U of chunk c may
+                    // overwrite the U tile P U(c-2) read)
+                    tc_commit(&bar[B_ADONE]);
+                    tc_commit(&bar[B_EMPTYE0 + s]);  // the early group of chunk c is read
+                    // U~(c+1) now if chunk c+1 has landed (it then runs while U is formed);
+                    // its buffer was last read by the state update of chunk c-1
+                    u_next = c + 1 < nch &&
+                             mbar_test_wait(&bar[B_FULLE0 + (s ^ 1)], ((c + 1) >> 1) & 1);
+                    if (u_next) {
+                        issue_u<NS>(tmem, sbase + (s ^ 1) * Cfg::STAGE,
+                                    Cfg::TMB + (uint32_t)NS * (uint32_t)(s ^ 1));
+                        TRACE(c + 1, 5);
+                    }
+                }
+                __syncwarp();
                 // K~^T U once U of chunk c is formed, then P U
-                ok = wait_or_abort(&bar[B_UREADY], c & 1, abort_flag, ST_MMA) &&
-                     wait_or_abort(&bar[B_FULLL0 + s], (c >> 1) & 1, abort_flag, ST_MMA);
-                if (!ok) break;
-                TRACE(c, 14);
-                tc_fence_after();
-                const uint32_t ut = u_tile + Cfg::UT * (uint32_t)s;
-                issue_carry3<NS>(tmem, st, ut, tb);  // U~(c) is consumed
-                tc_commit(&bar[B_SDONE]);
-                TRACE(c, 9);
-                if (c + 1 < nch && !u_next) {
-                    ok = wait_or_abort(&bar[B_FULLE0 + (s ^ 1)], ((c + 1) >> 1) & 1, abort_flag,
-                                       ST_MMA);
-                    if (!ok) break;
-                    issue_u<NS>(tmem, sbase + (s ^ 1) * Cfg::STAGE,
-                                Cfg::TMB + (uint32_t)NS * (uint32_t)(s ^ 1));
-                    TRACE(c + 1, 5);
+                if (bar_any(BAR_U, 160, fail)) fail = true;
+                if (leader) TRACE(c, 7);
+                if (leader && !fail) {
+                    if (!wait_chain(&bar[B_FULLL0 + s], (c >> 1) & 1, abort_flag, ST_MMA)) {
+                        fail = true;
+                    } else {
+                        TRACE(c, 14);
+                        tc_fence_after();
+                        const uint32_t ut = u_tile + Cfg::UT * (uint32_t)s;
+                        issue_carry3<NS>(tmem, st, ut, tb);  // U~(c) is consumed
+                        tc_commit(&bar[B_SDONE]);
+                        TRACE(c, 9);
+                        if (c + 1 < nch && !u_next) {
+                            if (!wait_chain(&bar[B_FULLE0 + (s ^ 1)], ((c + 1) >> 1) & 1,
+                                            abort_flag, ST_MMA))
+                                fail = true;
+                            else
+                                issue_u<NS>(tmem, sbase + (s ^ 1) * Cfg::STAGE,
+                                            Cfg::TMB + (uint32_t)NS * (uint32_t)(s ^ 1));
+                            TRACE(c + 1, 5);
+                        }
+                        issue_carry2<NS>(tmem, st, ut, Cfg::TMC + (uint32_t)NS * (uint32_t)s);
+                        tc_commit(&bar[B_CDONE]);
+                        tc_commit(&bar[B_EMPTYL0 + s]);  // the late group of chunk c is read
+                        TRACE(c, 4);
+                        if (!fail) done = c + 1;
+                    }
                 }
-                issue_carry2<NS>(tmem, st, ut, ta);
-                tc_commit(&bar[B_CDONE]);
-                tc_commit(&bar[B_EMPTYL0 + s]);  // the late group of chunk c is read
-                TRACE(c, 4);
-                done = c + 1;
+                __syncwarp();
             }
-        } else if (!issuer) {
-            for (int c = 0; c < nch; ++c) {
+            // the SIMT warps' last BAR_S (after the state update of the last chunk)
+            if (!stopped) bar_any(BAR_S, 288, fail);
+            ok = !fail;
+        } else {
+            // the initial state tile is written: BAR_S #0
+            handoff();
+            bool stop = bar_any(BAR_S, 288, false);
+            for (int c = 0; c < nch && !stop; ++c) {
                 const int s = c & 1;
                 const uint32_t ta = Cfg::TMA + (uint32_t)NS * (uint32_t)s;
                 const uint32_t tb = Cfg::TMB + (uint32_t)NS * (uint32_t)s;
-                // Gamma_last of the chunk (late group) is read before this warp's UREADY:
-                // the stage's late group is reloaded only after P U, which follows it
-                ok = wait_or_abort(&bar[B_FULLL0 + s], (c >> 1) & 1, abort_flag, ST_CARRY);
-                if (!ok) break;
-                const float Gl = scal[s].Gl;
                 if (q >= 2) {
                     // the output of chunk c-1, once its P U is complete
                     if (c > 0) {
-                        ok = wait_or_abort(&bar[B_CDONE], (c - 1) & 1, abort_flag, ST_CARRY);
-                        if (!ok) break;
-                        tc_fence_after();
-                        write_out(c - 1);
+                        if (!wait_chain(&bar[B_CDONE], (c - 1) & 1, abort_flag, ST_CARRY)) fail = true;
+                        warp_fail();
+                        if (!fail) {
+                            tc_fence_after();
+                            write_out(c - 1, gsc_prev);
+                        }
                     }
+                    if (lane == 0 && warp == 6) TRACE(c, 17);
                 } else {
-                    ok = wait_or_abort(&bar[B_ADONE], c & 1, abort_flag, ST_CARRY);
-                    if (!ok) break;
-                    if (warp == 4 && lane == 0) TRACE(c, 13);
+                    if (!wait_chain(&bar[B_ADONE], c & 1, abort_flag, ST_CARRY)) fail = true;
+                    warp_fail();
+                    if (!fail) {
+                        if (lane == 0) TRACE(c, 30 + (warp & 1) + ((warp >> 2) - 1) * 2);
+                        tc_fence_after();
+                        // U = U~ - W S0 for token L
+                        const uint32_t ut = u_tile + Cfg::UT * (uint32_t)s;
+#pragma unroll
+                        for (int p = 0; p < NP; ++p) {
+                            float ws[32], uv[32];
+                            tmem_ld32x2(tmem + lane_off + ta + 32 * p,
+                                        tmem + lane_off + tb + 32 * p, ws, uv);
+                            uint32_t u[16];
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                u[j] = pack_bf16(uv[2 * j] - ws[2 * j],
+                                                 uv[2 * j + 1] - ws[2 * j + 1]);
+                            write_row32_packed(ut + 8192u * pblk(p), L, pch(p), u);
+                        }
+                        if (lane == 0) TRACE(c, 34 + (warp & 1) + ((warp >> 2) - 1) * 2);
+                    }
+                    handoff();
+                    if (warp == 4 && lane == 0) TRACE(c, 20);
+                    if (bar_any(BAR_U, 160, fail)) fail = true;
+                    if (warp == 4 && lane == 0) TRACE(c, 21);
+                }
+                // S1 = Gamma_last S0 + K~^T U for state row L (the late group, with the
+                // scalars, landed before K~^T U was issued and is reloaded only after P U)
+                if (!fail && !(wait_chain(&bar[B_SDONE], c & 1, abort_flag, ST_CARRY) &&
+                               wait_chain(&bar[B_FULLL0 + s], (c >> 1) & 1, abort_flag,
+                                          ST_CARRY)))
+                    fail = true;
+                warp_fail();
+                if (!fail) {
+                    if (warp == 4 && lane == 0) TRACE(c, 15);
                     tc_fence_after();
-                    // U = U~ - W S0 for token L
-                    const uint32_t ut = u_tile + Cfg::UT * (uint32_t)s;
+                    const float Gl = scal[s].Gl;
+                    if (q >= 2) gsc_prev = a.scale * scal[s].Gam[L - 64];
 #pragma unroll
                     for (int p = 0; p < NP; ++p) {
-                        float ws[32], uv[32];
-                        tmem_ld32x2(tmem + lane_off + ta + 32 * p, tmem + lane_off + tb + 32 * p,
-                                    ws, uv);
-                        uint32_t u[16];
+                        float d[32];
+                        tmem_ld32(tmem + lane_off + tb + 32 * p, d);
 #pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            u[j] = pack_bf16(uv[2 * j] - ws[2 * j], uv[2 * j + 1] - ws[2 * j + 1]);
-                        write_row32_packed(ut + 8192u * pblk(p), L, pch(p), u);
+                        for (int j = 0; j < 32; ++j)
+                            Sr[32 * p + j] = fmaf(Gl, Sr[32 * p + j], d[j]);
+                        write_row32(s_base + 16384u * pblk(p), L, pch(p), Sr + 32 * p);
                     }
+                    if (lane == 0) TRACE(c, 38 + warp - 4);
                 }
-                if (lane == 0 && (warp == 4 || warp == 6)) TRACE(c, warp == 4 ? 11 : 17);
-                warp_arrive(B_UREADY);
-                // S1 = Gamma_last S0 + K~^T U for state row L
-                ok = wait_or_abort(&bar[B_SDONE], c & 1, abort_flag, ST_CARRY);
-                if (!ok) break;
-                if (warp == 4 && lane == 0) TRACE(c, 15);
-                tc_fence_after();
-#pragma unroll
-                for (int p = 0; p < NP; ++p) {
-                    float d[32];
-                    tmem_ld32(tmem + lane_off + tb + 32 * p, d);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) Sr[32 * p + j] = fmaf(Gl, Sr[32 * p + j], d[j]);
-                    write_row32(s_base + 16384u * pblk(p), L, pch(p), Sr + 32 * p);
-                }
-                if (warp == 4 && lane == 0) TRACE(c, 16);
-                warp_arrive(B_SREADY);
-                done = c + 1;
+                handoff();
+                if (warp == 4 && lane == 0) TRACE(c, 22);
+                stop = bar_any(BAR_S, 288, fail);
+                if (warp == 4 && lane == 0) TRACE(c, 23);
+                if (!fail) done = c + 1;
             }
+            ok = !fail;
         }
         // every role of the carry group decides the epilogue together (lanes 1-31 of the
         // issuer warp only take part in this barrier)
         if ((leader || !issuer) && (!ok || done < nch) && !*abort_flag)
             record_failure(abort_flag, ST_CARRY);
         bar_sync(1, 288);
-        ok = !*abort_flag;
+        ok = __all_sync(0xffffffffu, !*abort_flag);
         if (ok && !issuer && q >= 2) {
             // the output of the last chunk
-            ok = wait_or_abort(&bar[B_CDONE], (nch - 1) & 1, abort_flag, ST_CARRY);
+            ok = __all_sync(0xffffffffu,
+                            wait_chain(&bar[B_CDONE], (nch - 1) & 1, abort_flag, ST_CARRY));
             if (ok) {
                 tc_fence_after();
-                write_out(nch - 1);
+                write_out(nch - 1, gsc_prev);
             }
         }
         if (ok && !issuer) {

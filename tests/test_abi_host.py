@@ -68,10 +68,10 @@ def test_prefill_rejects_bad_arguments(lib, kw, msg):
 
 def test_workspace_query(lib):
     assert lib.gdn_prefill_workspace_bytes(1, 3, 4, 64, 128, 128, 1) == ctypes.c_size_t(-1).value
-    # tensor-core path: 66064 bytes per (batch, value head, 64-token chunk), ragged tail
+    # tensor-core path: 49680 bytes per (batch, value head, 64-token chunk), ragged tail
     # rounded up; the fp32 and other-head-dim paths need none
-    assert lib.gdn_prefill_workspace_bytes(1, 16, 32, 8192, 128, 128, 1) == 32 * 128 * 66064
-    assert lib.gdn_prefill_workspace_bytes(2, 1, 3, 65, 128, 128, 1) == 2 * 3 * 2 * 66064
+    assert lib.gdn_prefill_workspace_bytes(1, 16, 32, 8192, 128, 128, 1) == 32 * 128 * 49680
+    assert lib.gdn_prefill_workspace_bytes(2, 1, 3, 65, 128, 128, 1) == 2 * 3 * 2 * 49680
     assert lib.gdn_prefill_workspace_bytes(1, 16, 32, 8192, 128, 128, 0) == 0
     assert lib.gdn_prefill_workspace_bytes(1, 16, 32, 8192, 64, 128, 1) == 0
 
@@ -81,11 +81,11 @@ def test_prefill_requires_its_workspace(lib):
     assert "workspace" in lib.gdn_last_error().decode()
 
 
-@pytest.mark.parametrize("B,Hv", [(1, 4096), (1, 2032), (8, 254), (2, 1024)])
+@pytest.mark.parametrize("B,Hv", [(1, 4096), (1, 2702), (2, 1351), (8, 512)])
 def test_noalloc_rejects_more_heads_than_its_scratch(lib, B, Hv):
-    """The 128 MiB scratch holds 2031 units of 66064 bytes: B * Hv = 2032 and above are
-    refused on the host, before any launch (the accepted 2031 runs in the GPU tests)."""
-    assert (128 << 20) // 66064 == 2031
+    """The 128 MiB scratch holds 2701 units of 49680 bytes: B * Hv = 2702 and above are
+    refused on the host, before any launch (the accepted 2701 runs in the GPU tests)."""
+    assert (128 << 20) // 49680 == 2701
     vp = ctypes.c_void_p
     rc = lib.gdn_prefill_noalloc(vp(16), vp(16), vp(16), vp(16), vp(16), 1.0, 1, B, 1, Hv,
                                  64, 128, 128, vp(16), 0, vp(16), None)
@@ -151,9 +151,9 @@ def test_conv1d_rejects_bad_arguments(lib, kw, msg):
 
 
 def test_varlen_workspace_query(lib):
-    # tensor-core path: Hv * (ceil(T/64) + N) units of 66064 bytes (to 256), then the
+    # tensor-core path: Hv * (ceil(T/64) + N) units of 49680 bytes (to 256), then the
     # N + 2 ints of the chunk table; fp32 / other head dims: the table alone (to 16)
-    units = 32 * (4096 // 64 + 5) * 66064
+    units = 32 * (4096 // 64 + 5) * 49680
     assert lib.gdn_prefill_varlen_workspace_bytes(5, 16, 32, 4096, 128, 128, 1) == \
         (units + 255) // 256 * 256 + 4 * 7
     assert lib.gdn_prefill_varlen_workspace_bytes(5, 2, 2, 100, 64, 64, 0) == 32

@@ -91,11 +91,11 @@ def test_noalloc_equals_prefill_on_two_calls_in_a_row(lib):
 
 
 def test_noalloc_segments_with_ragged_tail(lib):
-    """B*Hv = 1000 leaves room for two chunks per (batch, head): S = 5*64 - 17 runs as
+    """B*Hv = 1300 leaves room for two chunks per (batch, head): S = 5*64 - 17 runs as
     segments of 2, 2 and 1 chunks, the last holding the ragged tail. With a zero start the
     later segments read back the state the earlier ones wrote. Both starts, two calls each,
     equal gdn_prefill and match the oracle over the whole tensor."""
-    base = syn.shrink(syn.PREFILL_BF16_GQA2, B=5, Hk=100, Hv=200, S=5 * 64 - 17)
+    base = syn.shrink(syn.PREFILL_BF16_GQA2, B=5, Hk=130, Hv=260, S=5 * 64 - 17)
     for state_std in (None, 0.05):
         x = syn.prefill_inputs(syn.shrink(base, state_std=state_std))
         X = _device_inputs(x)
@@ -110,13 +110,13 @@ def test_noalloc_segments_with_ragged_tail(lib):
 
 
 def test_noalloc_largest_head_count(lib):
-    """B*Hv = 2031, the most (batch, head) pairs one chunk of which fits the scratch: the call
+    """B*Hv = 2701, the most (batch, head) pairs one chunk of which fits the scratch: the call
     is accepted and equals gdn_prefill; one more pair is refused."""
-    x = syn.prefill_inputs(syn.shrink(syn.PREFILL_BF16_GQA2, B=1, Hk=1, Hv=2031, S=64))
+    x = syn.prefill_inputs(syn.shrink(syn.PREFILL_BF16_GQA2, B=1, Hk=1, Hv=2701, S=64))
     X = _device_inputs(x)
     _check_same(*_run(lib, x, X, noalloc=False), *_run(lib, x, X, noalloc=True))
     rc = lib.gdn_prefill_noalloc(VP(16), VP(16), VP(16), VP(16), VP(16), 1.0,
-                                 gdn.GDN_DTYPE_BF16, 1, 1, 2032, 64, 128, 128, VP(16), 0,
+                                 gdn.GDN_DTYPE_BF16, 1, 1, 2702, 64, 128, 128, VP(16), 0,
                                  VP(16), None)
     assert rc == gdn.GDN_EUNSUPPORTED
     assert np.isfinite(x["scale"])
