@@ -74,7 +74,7 @@ uint32_t prefill_tc_take_status() {
 // Profiling aid, compiled only with -DGDN_TRACE: per-chunk SM clock stamps of the
 // pipeline events of carry CTA (0,0,0) and of the prep CTAs of head 0, batch 0, read
 // back with gdn_trace_read().
-constexpr int kTraceChunks = 64, kTraceEvents = 48;
+constexpr int kTraceChunks = 64, kTraceEvents = 64;
 __device__ unsigned long long g_trace[kTraceChunks][kTraceEvents];
 #define TRACE(c, ev)                                                                    \
     do {                                                                                \
@@ -212,7 +212,7 @@ constexpr uint32_t PT_G = 0;  // Gram [QK^T; KK^T], 64 columns
 constexpr uint32_t PT_W = 0;  // [W; -], 128 columns (the Gram matrices are read by then)
 constexpr uint32_t PT_COLS = 128;
 
-enum { PB_FULL = 0, PB_GRAM, PB_PREP, PB_WDONE, PB_DRAIN, PB_COUNT };
+enum { PB_FULL = 0, PB_GRAM, PB_WDONE, PB_DRAIN, PB_COUNT };
 
 // ---- carry kernel: one CTA per (NS-column slice of the state, value head, batch), NS = 64
 // (CarryCfg<NS>; the transposed carry shares the stage layout with NS = 128). Shared
@@ -641,6 +641,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
     }
 
     const int zq = b * a.Hk + kh, zv = b * a.Hv + h;
+    if (tid == 0) TRACE_PREP(29);
     // g and beta of the chunk are loaded first and the copies of Q and K started at
     // once, so that their latency overlaps the setup (padding tokens -- past the end of
     // the sequence -- get g = beta = 0, an exact no-op)
@@ -724,12 +725,6 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
                 tc_commit(&bar[PB_GRAM]);
                 issued = 1;
                 TRACE_PREP(21);
-                if (wait_or_abort(&bar[PB_PREP], 0, abort_flag, ST_PREP)) {
-                    tc_fence_after();
-                    issue_w(tmem, sb);
-                    tc_commit(&bar[PB_WDONE]);
-                    TRACE_PREP(22);
-                }
             } else {
                 // the copies must land before the CTA exits
                 mbar_wait_bounded(&bar[PB_FULL], 0, kWaitNs);
@@ -750,6 +745,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
         const int g8 = lane >> 2, t4 = lane & 3;
         const uint32_t lane_off = (uint32_t)(32 * q) << 16;
         const uint32_t tu = sb + P_TU, tw = sb + P_TW;
+        bool w_issued = false;  // thread P == 0 issued the W MMA
 
         // One warp polls the mbarriers; the others wait at the named barrier, which costs
         // no issue slots (the prep is bound by instruction issue, with three CTAs per SM).
@@ -941,15 +937,28 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
                 block_store(e, Tb + bidx(i, j) * 16 * BS, i, j, nt, g8, t4, sc.beta, sc.Gam, tu,
                             tw);
             }
+            fence_proxy_async_smem();  // T_U, T_W and P are read by the W MMA and copies
             bar_sync(2, 256);
-            fence_proxy_async_smem();
+            uint8_t* wsu = a.ws + ws_offset(b, h, cl, a.Hv, nch);
             if (P == 0) {
                 TRACE_PREP(27);
-                mbar_arrive(&bar[PB_PREP]);
+                // [W; P K] = [T_W; P] K, issued here as soon as T_W is complete (the
+                // Gram columns it overwrites were read before the mask barrier)
+                tc_fence_after();
+                issue_w(tmem, sb);
+                tc_commit(&bar[PB_WDONE]);
+                w_issued = true;
+                TRACE_PREP(22);
+                // T_U, P and the scalars are final: to the workspace now, under the W MMA
+                bulk_s2g(wsu + WS_TU, sb + P_TU, 8192);
+                bulk_s2g(wsu + WS_P, sb + P_P, 8192);
+                bulk_s2g(wsu + WS_CS, sb + P_CS, sizeof(CarryScalars));
+                bulk_commit();
             }
             // ---- W = T_W K from TMEM (rows 0..63: lanes 0..63) into the W staging tiles;
             // two warps per lane quadrant, one 64-column block each
             if (pw == 0) ok = wait_or_abort(&bar[PB_WDONE], 0, abort_flag, ST_PREP);
+            if (P == 0) TRACE_PREP(54);
             if (!bar_any(2, 256, !ok || *abort_flag)) {
                 tc_fence_after();
                 if (q < 2) {
@@ -965,18 +974,20 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
                 bar_sync(2, 256);
                 if (P == 0) {
                     TRACE_PREP(28);
-                    uint8_t* ws = a.ws + ws_offset(b, h, cl, a.Hv, nch);
-                    bulk_s2g(ws + WS_TU, sb + P_TU, 8192);
-                    bulk_s2g(ws + WS_P, sb + P_P, 8192);
-                    bulk_s2g(ws + WS_W, sb + PQ_Q, 8192);
-                    bulk_s2g(ws + WS_W + 8192, sb + PQ_STRIDE + PQ_Q, 8192);
-                    bulk_s2g(ws + WS_CS, sb + P_CS, sizeof(CarryScalars));
+                    bulk_s2g(wsu + WS_W, sb + PQ_Q, 8192);
+                    bulk_s2g(wsu + WS_W + 8192, sb + PQ_STRIDE + PQ_Q, 8192);
                     bulk_commit();
-                    // the CTA may exit once the tiles are read out of shared memory: the
-                    // carry, a later kernel, sees the global writes completed
-                    bulk_wait_read_all();
                 }
             }
+        }
+        if (P == 0) {
+            // the CTA may exit once the tiles are read out of shared memory: the carry, a
+            // later kernel, sees the global writes completed
+            bulk_wait_read_all();
+            TRACE_PREP(53);
+            // no MMA may be in flight when TMEM is freed
+            if (w_issued && !mbar_wait_bounded(&bar[PB_WDONE], 0, kWaitNs))
+                atomicOr(&g_tc_status, ST_PREP);
         }
     }
 
@@ -1253,7 +1264,7 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
                 const uint32_t ta = Cfg::TMA + (uint32_t)NS * (uint32_t)s;
                 const uint32_t tb = Cfg::TMB + (uint32_t)NS * (uint32_t)s;
                 // MMA1 [W; Q] S0 once the state tile of chunk c is complete
-                if (leader) TRACE(c, 24);
+                if (leader) TRACE(c, 52);
                 if (bar_any(BAR_S, 288, fail)) {
                     stopped = true;
                     break;
@@ -1354,9 +1365,9 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
                         if (lane == 0) TRACE(c, 34 + (warp & 1) + ((warp >> 2) - 1) * 2);
                     }
                     handoff();
-                    if (warp == 4 && lane == 0) TRACE(c, 20);
+                    if (warp == 4 && lane == 0) TRACE(c, 48);
                     if (bar_any(BAR_U, 160, fail)) fail = true;
-                    if (warp == 4 && lane == 0) TRACE(c, 21);
+                    if (warp == 4 && lane == 0) TRACE(c, 49);
                 }
                 // S1 = Gamma_last S0 + K~^T U for state row L (the late group, with the
                 // scalars, landed before K~^T U was issued and is reloaded only after P U)
@@ -1382,9 +1393,9 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
                     if (lane == 0) TRACE(c, 38 + warp - 4);
                 }
                 handoff();
-                if (warp == 4 && lane == 0) TRACE(c, 22);
+                if (warp == 4 && lane == 0) TRACE(c, 50);
                 stop = bar_any(BAR_S, 288, fail);
-                if (warp == 4 && lane == 0) TRACE(c, 23);
+                if (warp == 4 && lane == 0) TRACE(c, 51);
                 if (!fail) done = c + 1;
             }
             ok = !fail;
