@@ -54,6 +54,28 @@ struct Smem {
     float part[NWARP];
 };
 
+// Two fp32 FMAs in one instruction (fma.rn.f32x2): d.x = a.x b.x + c.x, d.y = a.y b.y + c.y,
+// each rounded once, exactly as two fmaf would.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;"
+        : "=l"(d)
+        : "l"(*reinterpret_cast<const unsigned long long*>(&a)),
+          "l"(*reinterpret_cast<const unsigned long long*>(&b)),
+          "l"(*reinterpret_cast<const unsigned long long*>(&c)));
+    return *reinterpret_cast<const float2*>(&d);
+}
+
+// Two fp32 products in one instruction (mul.rn.f32x2), each rounded as a * b.
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+    unsigned long long d;
+    asm("mul.rn.f32x2 %0, %1, %2;"
+        : "=l"(d)
+        : "l"(*reinterpret_cast<const unsigned long long*>(&a)),
+          "l"(*reinterpret_cast<const unsigned long long*>(&b)));
+    return *reinterpret_cast<const float2*>(&d);
+}
+
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
@@ -160,17 +182,22 @@ __global__ void __launch_bounds__(NT, 2) decode_kernel(DecodeArgs a) {
             const size_t row = (size_t)(t0 + t) * BH + (size_t)bh;  // this token's row
             // 3. per-warp partial x = S^T k^ and y = S^T q^ over this warp's rows
             {
-                float px[4] = {0.f, 0.f, 0.f, 0.f}, py[4] = {0.f, 0.f, 0.f, 0.f};
+                // column pairs (0,1), (2,3) in paired FMAs: each lane as fmaf, same order
+                float2 x01 = make_float2(0.f, 0.f), x23 = x01, y01 = x01, y23 = x01;
 #pragma unroll
                 for (int m = 0; m < ROWS; ++m) {
                     const int i = w + NWARP * m;
                     const float ki = s.kn[t][i], qi = s.qn[t][i];  // zero beyond K
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        px[c] = fmaf(ki, st[m][c], px[c]);
-                        py[c] = fmaf(qi, st[m][c], py[c]);
-                    }
+                    const float2 kk = make_float2(ki, ki), qq = make_float2(qi, qi);
+                    const float2 s01 = make_float2(st[m][0], st[m][1]);
+                    const float2 s23 = make_float2(st[m][2], st[m][3]);
+                    x01 = ffma2(kk, s01, x01);
+                    x23 = ffma2(kk, s23, x23);
+                    y01 = ffma2(qq, s01, y01);
+                    y23 = ffma2(qq, s23, y23);
                 }
+                const float px[4] = {x01.x, x01.y, x23.x, x23.y};
+                const float py[4] = {y01.x, y01.y, y23.x, y23.y};
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const int j = col_of<VEC4>(lane, c);
@@ -208,13 +235,25 @@ __global__ void __launch_bounds__(NT, 2) decode_kernel(DecodeArgs a) {
             // 6. S' = alpha S + k^ u^T in registers (rows beyond K stay zero). The next
             // token's partials overwrite s.red only after this thread's reads of s.u and
             // s.part, and its u after the next barrier.
+            {
+                const float2 u01 = make_float2(s.u[col_of<VEC4>(lane, 0)], s.u[col_of<VEC4>(lane, 1)]);
+                const float2 u23 = make_float2(s.u[col_of<VEC4>(lane, 2)], s.u[col_of<VEC4>(lane, 3)]);
+                const float2 aa = make_float2(alpha, alpha);
 #pragma unroll
-            for (int m = 0; m < ROWS; ++m) {
-                const int i = w + NWARP * m;
-                const float ki = s.kn[t][i];  // zero beyond K
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    st[m][c] = fmaf(alpha, st[m][c], ki * s.u[col_of<VEC4>(lane, c)]);
+                for (int m = 0; m < ROWS; ++m) {
+                    const int i = w + NWARP * m;
+                    const float ki = s.kn[t][i];  // zero beyond K
+                    const float2 kk = make_float2(ki, ki);
+                    // alpha S + (k_i u_j), each product rounded first, as fmaf(alpha, S, k u)
+                    const float2 n01 =
+                        ffma2(aa, make_float2(st[m][0], st[m][1]), fmul2(kk, u01));
+                    const float2 n23 =
+                        ffma2(aa, make_float2(st[m][2], st[m][3]), fmul2(kk, u23));
+                    st[m][0] = n01.x;
+                    st[m][1] = n01.y;
+                    st[m][2] = n23.x;
+                    st[m][3] = n23.y;
+                }
             }
         }
     }
@@ -421,17 +460,21 @@ __global__ void __launch_bounds__(MT, 2) decode_multi_kernel(DecodeArgs a) {
         // rows 64 rh .. 64 rh + 63); the second row half adds its partials through red
         {
             const int j = tid & (kMaxHeadDim - 1), th = (tid >> 7) & 1, rh = tid >> 8;
-            float px[4] = {0.f, 0.f, 0.f, 0.f}, py[4] = {0.f, 0.f, 0.f, 0.f};
+            // token pairs in paired fp32 FMAs (each lane rounds as fmaf)
+            float2 x01 = make_float2(0.f, 0.f), x23 = x01, y01 = x01, y23 = x01;
 #pragma unroll 4
             for (int i = 64 * rh; i < 64 * rh + 64; ++i) {
                 const float sv = s.S[i * kMaxHeadDim + j];
+                const float2 ss = make_float2(sv, sv);
                 const float4 k4 = *reinterpret_cast<const float4*>(&s.kT[i][4 * th]);
                 const float4 q4 = *reinterpret_cast<const float4*>(&s.qT[i][4 * th]);
-                px[0] = fmaf(k4.x, sv, px[0]); px[1] = fmaf(k4.y, sv, px[1]);
-                px[2] = fmaf(k4.z, sv, px[2]); px[3] = fmaf(k4.w, sv, px[3]);
-                py[0] = fmaf(q4.x, sv, py[0]); py[1] = fmaf(q4.y, sv, py[1]);
-                py[2] = fmaf(q4.z, sv, py[2]); py[3] = fmaf(q4.w, sv, py[3]);
+                x01 = ffma2(make_float2(k4.x, k4.y), ss, x01);
+                x23 = ffma2(make_float2(k4.z, k4.w), ss, x23);
+                y01 = ffma2(make_float2(q4.x, q4.y), ss, y01);
+                y23 = ffma2(make_float2(q4.z, q4.w), ss, y23);
             }
+            const float px[4] = {x01.x, x01.y, x23.x, x23.y};
+            const float py[4] = {y01.x, y01.y, y23.x, y23.y};
             if (rh == 1) {
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
@@ -501,18 +544,22 @@ __global__ void __launch_bounds__(MT, 2) decode_multi_kernel(DecodeArgs a) {
         {
             const int j = tid & (kMaxHeadDim - 1), rq = tid >> 7;
             const float Gl = s.Gam[TB - 1];
-            float u[TB];
-#pragma unroll
-            for (int t = 0; t < TB; ++t) u[t] = s.X[t][j];
+            // the token pairs (0,1), (2,3), (4,5), (6,7) in paired fp32 FMAs, the two halves
+            // added at the end
+            const float2 u01 = make_float2(s.X[0][j], s.X[1][j]);
+            const float2 u23 = make_float2(s.X[2][j], s.X[3][j]);
+            const float2 u45 = make_float2(s.X[4][j], s.X[5][j]);
+            const float2 u67 = make_float2(s.X[6][j], s.X[7][j]);
 #pragma unroll 4
             for (int i = 32 * rq; i < 32 * rq + 32; ++i) {
                 const float4 k0 = *reinterpret_cast<const float4*>(&s.kT[i][0]);
                 const float4 k1 = *reinterpret_cast<const float4*>(&s.kT[i][4]);
-                float x = Gl * s.S[i * kMaxHeadDim + j];
-                x = fmaf(k0.x, u[0], x); x = fmaf(k0.y, u[1], x);
-                x = fmaf(k0.z, u[2], x); x = fmaf(k0.w, u[3], x);
-                x = fmaf(k1.x, u[4], x); x = fmaf(k1.y, u[5], x);
-                x = fmaf(k1.z, u[6], x); x = fmaf(k1.w, u[7], x);
+                float2 acc = make_float2(Gl * s.S[i * kMaxHeadDim + j], 0.f);
+                acc = ffma2(make_float2(k0.x, k0.y), u01, acc);
+                acc = ffma2(make_float2(k0.z, k0.w), u23, acc);
+                acc = ffma2(make_float2(k1.x, k1.y), u45, acc);
+                acc = ffma2(make_float2(k1.z, k1.w), u67, acc);
+                const float x = acc.x + acc.y;
                 if (last) {
                     if (i < K && j < V) __stcs(S1 + (size_t)i * V + j, x);
                 } else {
