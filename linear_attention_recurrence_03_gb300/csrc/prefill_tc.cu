@@ -93,7 +93,25 @@ __device__ unsigned long long g_trace[kTraceChunks][kTraceEvents];
         if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (c) < kTraceChunks) \
             g_trace[(c)][(ev)] = (var);                                                 \
     } while (0)
+// Launch spans: per kernel (prep of segment j: slot 2j, its carry: 2j + 1, j < 4) the
+// earliest CTA start and the latest CTA end (globaltimer ns), read back with
+// gdn_trace_span_read().
+__device__ unsigned long long g_span[8][2];
+#define SPAN_BEGIN(slot)                                                                \
+    do {                                                                                \
+        if (threadIdx.x == 0 && (slot) < 8) atomicMin(&g_span[(slot)][0], ptx::globaltimer_ns()); \
+    } while (0)
+#define SPAN_END(slot)                                                                  \
+    do {                                                                                \
+        if (threadIdx.x == 0 && (slot) < 8) atomicMax(&g_span[(slot)][1], ptx::globaltimer_ns()); \
+    } while (0)
 #else
+#define SPAN_BEGIN(slot) \
+    do {                 \
+    } while (0)
+#define SPAN_END(slot) \
+    do {               \
+    } while (0)
 #define TCLK(var) \
     do {          \
     } while (0)
@@ -642,6 +660,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
 
     const int zq = b * a.Hk + kh, zv = b * a.Hv + h;
     if (tid == 0) TRACE_PREP(29);
+    SPAN_BEGIN(a.c0 == 0 ? 0 : 2);
     // g and beta of the chunk are loaded first and the copies of Q and K started at
     // once, so that their latency overlaps the setup (padding tokens -- past the end of
     // the sequence -- get g = beta = 0, an exact no-op)
@@ -998,6 +1017,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
         tc_fence_after();
         tmem_dealloc(tmem, PT_COLS);
     }
+    SPAN_END(a.c0 == 0 ? 0 : 2);
 }
 
 // ---------------------------------------------------------------- the carry kernel
@@ -1138,6 +1158,7 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
         return;
     }
 
+    SPAN_BEGIN(a.c0 == 0 ? 1 : 3);
     if (tid == 0) {
         for (int i = 0; i < B_COUNT; ++i) mbar_init(&bar[i], 1);
         *abort_flag = 0;
@@ -1435,6 +1456,7 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
         tc_fence_after();
         tmem_dealloc(tmem, Cfg::TMCOLS);
     }
+    SPAN_END(a.c0 == 0 ? 1 : 3);
 }
 
 // ---------------------------------------------------------------- transposed carry
@@ -2173,5 +2195,13 @@ cudaError_t launch_prefill_tc_overlapped(const PrefillArgs& a, cudaStream_t stre
 #ifdef GDN_TRACE
 extern "C" int gdn_trace_read(unsigned long long* dst) {
     return cudaMemcpyFromSymbol(dst, gdn::g_trace, sizeof(gdn::g_trace)) == cudaSuccess ? 0 : 1;
+}
+extern "C" int gdn_trace_span_reset() {
+    unsigned long long init[8][2];
+    for (int i = 0; i < 8; ++i) init[i][0] = ~0ull, init[i][1] = 0;
+    return cudaMemcpyToSymbol(gdn::g_span, init, sizeof(init)) == cudaSuccess ? 0 : 1;
+}
+extern "C" int gdn_trace_span_read(unsigned long long* dst) {
+    return cudaMemcpyFromSymbol(dst, gdn::g_span, sizeof(gdn::g_span)) == cudaSuccess ? 0 : 1;
 }
 #endif
