@@ -14,6 +14,8 @@
 //   O       = scale (diag(Gamma) Q S0 + P U)
 //   S1      = Gamma_{C-1} S0 + sum_j exp(gamma_{C-1} - gamma_j) k_j u_j^T
 // U = T Y is the same as U~ - W S0 with W = T diag(beta Gamma) K, U~ = T diag(beta) V.
+// T itself is never formed: U solves (I + A) U = Y by forward substitution over the rows,
+// U_r = Y_r - sum_{m<r} A[r,m] U_m, eight lanes per value column splitting each row's sum.
 //
 // A ragged last chunk is padded with tokens that have g = 0 and beta = 0: such a token
 // leaves the state unchanged (alpha = 1, u = 0), so padding is exact.
@@ -36,7 +38,7 @@ constexpr int CP = C + 1;  // padded row stride of the C x C tiles
 constexpr int NSP = NS + 1;
 
 struct Smem {
-    float Q[C][DKP];
+    float Q[C][DKP];    // q and k rows, zero from column Dk up to a multiple of 4
     float K[C][DKP];
     float Y[C][NSP];    // V slice, then Y = diag(beta)(V - diag(Gamma) K S0)
     float KS[C][NSP];
@@ -44,11 +46,11 @@ struct Smem {
     float U[C][NSP];
     float S[kMaxHeadDim][NSP];
     float A[C][CP];
-    float T[C][CP];
     float P[C][CP];
     float gam[C];
     float beta[C];
     float dec[C];       // exp(gamma_last - gamma_j)
+    float Gam[C];       // exp(gamma_r)
 };
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
@@ -63,6 +65,7 @@ __global__ void __launch_bounds__(NT) prefill_simt_kernel(PrefillArgs a) {
     const int tid = threadIdx.x;
     const int n0 = blockIdx.x * NS, h = blockIdx.y;
     const int Dk = a.Dk, Dv = a.Dv, S = a.S;
+    const int Dk4 = (Dk + 3) & ~3;  // the q/k rows are read in groups of four
     const int nw = min(NS, Dv - n0);
     const int kh = h / (a.Hv / a.Hk);  // value head h reads key head h // (Hv/Hk)
     // this CTA's sequence: batch b (tensor row b, tokens 0 .. S-1), or packed sequence n
@@ -97,9 +100,9 @@ __global__ void __launch_bounds__(NT) prefill_simt_kernel(PrefillArgs a) {
     for (int c0 = 0; c0 < len; c0 += C) {
         const int L = min(C, len - c0);
         __syncthreads();
-        for (int idx = tid; idx < C * Dk; idx += NT) {
-            const int r = idx / Dk, i = idx % Dk;
-            const bool live = r < L;
+        for (int idx = tid; idx < C * Dk4; idx += NT) {
+            const int r = idx / Dk4, i = idx % Dk4;
+            const bool live = r < L && i < Dk;
             s.Q[r][i] = live ? to_f32(q[(size_t)(c0 + r) * Dk + i]) : 0.f;
             s.K[r][i] = live ? to_f32(k[(size_t)(c0 + r) * Dk + i]) : 0.f;
         }
@@ -127,78 +130,97 @@ __global__ void __launch_bounds__(NT) prefill_simt_kernel(PrefillArgs a) {
         if (tid >= 32 && tid < C) s.gam[tid] += s.gam[31];
         __syncthreads();
         const float gl = s.gam[C - 1];
-        if (tid < C) s.dec[tid] = expf(gl - s.gam[tid]);
+        if (tid < C) {
+            s.dec[tid] = expf(gl - s.gam[tid]);
+            s.Gam[tid] = expf(s.gam[tid]);
+        }
 
-        // A (strictly lower, beta and decay folded in) and P (lower incl. diagonal)
+        // A (strictly lower, beta and decay folded in) and P (lower incl. diagonal); every
+        // dot product below runs as four interleaved partial sums
         {
             const int j = tid % C;
             for (int r = tid / C; r < C; r += NT / C) {
-                float kk = 0.f, qk = 0.f;
+                float kk[4] = {0.f, 0.f, 0.f, 0.f}, qk[4] = {0.f, 0.f, 0.f, 0.f};
                 if (j <= r) {
-                    for (int i = 0; i < Dk; ++i) {
-                        const float kj = s.K[j][i];
-                        kk = fmaf(s.K[r][i], kj, kk);
-                        qk = fmaf(s.Q[r][i], kj, qk);
+                    for (int i = 0; i < Dk4; i += 4) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float kj = s.K[j][i + e];
+                            kk[e] = fmaf(s.K[r][i + e], kj, kk[e]);
+                            qk[e] = fmaf(s.Q[r][i + e], kj, qk[e]);
+                        }
                     }
                 }
+                const float kks = (kk[0] + kk[1]) + (kk[2] + kk[3]);
+                const float qks = (qk[0] + qk[1]) + (qk[2] + qk[3]);
                 const float d = (j <= r) ? expf(s.gam[r] - s.gam[j]) : 0.f;
-                s.A[r][j] = (j < r) ? s.beta[r] * kk * d : 0.f;
-                s.P[r][j] = qk * d;
+                s.A[r][j] = (j < r) ? s.beta[r] * kks * d : 0.f;
+                s.P[r][j] = qks * d;
             }
         }
         // K S0 and Q S0
         for (int idx = tid; idx < C * NS; idx += NT) {
             const int r = idx / NS, n = idx % NS;
-            float ks = 0.f, qs = 0.f;
-            for (int i = 0; i < Dk; ++i) {
-                const float sv = s.S[i][n];
-                ks = fmaf(s.K[r][i], sv, ks);
-                qs = fmaf(s.Q[r][i], sv, qs);
+            float ks[4] = {0.f, 0.f, 0.f, 0.f}, qs[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int i = 0; i < Dk4; i += 4) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float sv = s.S[i + e][n];
+                    ks[e] = fmaf(s.K[r][i + e], sv, ks[e]);
+                    qs[e] = fmaf(s.Q[r][i + e], sv, qs[e]);
+                }
             }
-            s.KS[r][n] = ks;
-            s.QS[r][n] = qs;
+            s.KS[r][n] = (ks[0] + ks[1]) + (ks[2] + ks[3]);
+            s.QS[r][n] = (qs[0] + qs[1]) + (qs[2] + qs[3]);
         }
         __syncthreads();
-        // T = (I + A)^-1, one column per thread, forward substitution
-        if (tid < C) {
-            const int j = tid;
-            for (int r = 0; r < j; ++r) s.T[r][j] = 0.f;
-            s.T[j][j] = 1.f;
-            for (int r = j + 1; r < C; ++r) {
-                float acc = 0.f;
-                for (int m = j; m < r; ++m) acc = fmaf(s.A[r][m], s.T[m][j], acc);
-                s.T[r][j] = -acc;
-            }
-        }
         // Y = diag(beta) (V - diag(Gamma) K S0)
         for (int idx = tid; idx < C * NS; idx += NT) {
             const int r = idx / NS, n = idx % NS;
-            s.Y[r][n] = s.beta[r] * (s.Y[r][n] - expf(s.gam[r]) * s.KS[r][n]);
+            s.Y[r][n] = s.beta[r] * (s.Y[r][n] - s.Gam[r] * s.KS[r][n]);
         }
         __syncthreads();
-        // U = T Y
-        for (int idx = tid; idx < C * NS; idx += NT) {
-            const int r = idx / NS, n = idx % NS;
-            float acc = 0.f;
-            for (int j = 0; j <= r; ++j) acc = fmaf(s.T[r][j], s.Y[j][n], acc);
-            s.U[r][n] = acc;
+        // U = (I + A)^-1 Y, row by row: warp w takes value columns 4w .. 4w + 3, lane
+        // (column 4w + lane / 8, part lane % 8) the earlier rows part, part + 8, ...; three
+        // shuffles join the parts. A padding row has A = 0 and Y = 0, hence U = 0.
+        {
+            const int lane = tid & 31;
+            const int n = 4 * (tid >> 5) + (lane >> 3), part = lane & 7;
+            for (int r = 0; r < C; ++r) {
+                float acc = 0.f;
+                for (int m = part; m < r; m += 8) acc = fmaf(s.A[r][m], s.U[m][n], acc);
+                acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+                acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+                acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+                if (part == 0) s.U[r][n] = s.Y[r][n] - acc;
+                __syncwarp();
+            }
         }
         __syncthreads();
-        // O = scale (diag(Gamma) Q S0 + P U), written for live rows and columns
+        // O = scale (diag(Gamma) Q S0 + P U), written for live rows and columns (P is zero
+        // above the diagonal)
         for (int idx = tid; idx < C * NS; idx += NT) {
             const int r = idx / NS, n = idx % NS;
-            float pu = 0.f;
-            for (int j = 0; j <= r; ++j) pu = fmaf(s.P[r][j], s.U[j][n], pu);
-            const float o = a.scale * fmaf(expf(s.gam[r]), s.QS[r][n], pu);
+            float pu[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int j = 0; j <= r; j += 4) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) pu[e] = fmaf(s.P[r][j + e], s.U[j + e][n], pu[e]);
+            }
+            const float pus = (pu[0] + pu[1]) + (pu[2] + pu[3]);
+            const float o = a.scale * fmaf(s.Gam[r], s.QS[r][n], pus);
             if (r < L && n < nw) store_as(&out[(size_t)(c0 + r) * Dv + n0 + n], o);
         }
         // S1 = Gamma_last S0 + sum_j exp(gamma_last - gamma_j) k_j u_j^T
         const float Gl = expf(gl);
         for (int idx = tid; idx < Dk * NS; idx += NT) {
             const int i = idx / NS, n = idx % NS;
-            float acc = Gl * s.S[i][n];
-            for (int j = 0; j < C; ++j) acc = fmaf(s.dec[j] * s.K[j][i], s.U[j][n], acc);
-            s.S[i][n] = acc;
+            float acc[4] = {Gl * s.S[i][n], 0.f, 0.f, 0.f};
+            for (int j = 0; j < C; j += 4) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    acc[e] = fmaf(s.dec[j + e] * s.K[j + e][i], s.U[j + e][n], acc[e]);
+            }
+            s.S[i][n] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
         }
     }
     __syncthreads();
