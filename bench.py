@@ -39,7 +39,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # overlapped segments, dram__bytes_read.sum + dram__bytes_write.sum, one ncu capture),
 # keyed by the sha256 of the kernel source at capture time (reported only while it
 # matches).
-NCU_TRAFFIC = {"prefill_tc.cu@778822c599911449": 488020224}
+NCU_TRAFFIC = {"prefill_tc.cu@068059ef9cbacc67": 488020224}
 
 
 def parse_args():

@@ -1,5 +1,5 @@
 // prefill_tc.cu -- chunked GDN prefill on the tcgen05 tensor cores: bf16 operands, fp32
-// accumulation in tensor memory (TMEM), fp32 state master in TMEM.
+// accumulation in tensor memory (TMEM), fp32 state master in registers.
 //
 // "GDN CTE Kernel API Reference": the gated delta rule in chunk-parallel form with an
 // intra-chunk (I+A) inverse; q/k/v token-major, out head-major, state fp32 (Notes: the
@@ -21,16 +21,16 @@
 // Two kernels. Everything that does not depend on S0 (the Gram matrices, the decay
 // masks, the (I+A)^-1 solve, T_U, P and W) is independent across chunks, so it runs
 // first as a fully parallel grid ("prep", one CTA per (batch, value head, chunk)) that
-// writes bf16 operand tiles (T_U, P, W, and for the two-slice carry Q~ and K~) and the
-// decay scalars per chunk to a workspace, the tiles already in the 128-byte swizzled
-// layout the tensor cores read. The sequential part ("carry") then streams v and those
-// tiles through a two-stage ring and keeps only the S0-dependent chain per chunk, in one
-// of two forms:
+// writes bf16 operand tiles (T_U, P, W, and for the two-slice carry K~ = diag(exp(
+// gamma_last - gamma)) K) and the decay scalars per chunk to a workspace, the tiles
+// already in the 128-byte swizzled layout the tensor cores read. The sequential part
+// ("carry") then streams q, v and those tiles through a two-stage ring and keeps only the
+// S0-dependent chain per chunk, in one of two forms:
 //   carry_tc_kernel<64>: one CTA per (batch, value head, 64-column slice of the state;
 //   the slices never communicate), state rows in TMEM lanes, used while two CTAs per
-//   head fit the GPU:
+//   head fit the GPU (the Gamma scaling of the Q S0 rows is applied in its output step):
 //          [T_U;-] V              -> U~                   (M128 N64  K64)
-//          [W;Q~] S0              -> W S0, Q~ S0          (M128 N64  K128)
+//          [W;Q] S0               -> W S0, Q S0           (M128 N64  K128)
 //          [K~_1;P] U             -> P U                  (M128 N64  K64)
 //          K~^T U                 -> state increment      (M128 N64  K64)
 //   carry_t_kernel: one CTA per (batch, value head), the chain transposed (state columns
