@@ -18,11 +18,10 @@
 // Cross-warp sums go through shared memory in a fixed order, so results are bitwise
 // reproducible and do not depend on the grid ("LNC1 is byte-identical", Notes).
 //
-// Multi-token form (T consecutive steps of the same rows in one call; an extension, not
-// on the pages): the state stays in registers across the T tokens, so its 2 x 64 KB of
-// HBM traffic is paid once per call; token t's inputs sit at offset t * BH rows. Up to
-// four tokens run one after another on the register state; more are taken in blocks of
-// eight in chunk form (derived from the same step):
+// Multi-token form (T >= 2 consecutive steps of the same rows in one call; an extension,
+// not on the pages): the state stays on chip across the T tokens, so its 2 x 64 KB of HBM
+// traffic is paid once per call; token t's inputs sit at offset t * BH rows. The tokens
+// are taken in blocks of eight in chunk form (derived from the same step):
 // with gamma_t = g_1 + ... + g_t (from the block start), Gamma_t = exp(gamma_t) and
 // D[t][i] = exp(gamma_t - gamma_i) (i <= t, never above 1),
 //   X[t] = S0^T k^_t, Y[t] = S0^T q^_t            (one pass over the old state, all t)
@@ -32,18 +31,21 @@
 //   S_last = Gamma_last S0 + sum_t D[last][t] k^_t u_t^T   (one update pass)
 // instead of one reduction, solve and update per token.
 #include "internal.h"
+#include "sm100_ptx.cuh"
 
 namespace gdn {
 namespace {
+
+using namespace ptx;
 
 constexpr int NT = 256;
 constexpr int NWARP = NT / 32;
 constexpr int ROWS = kMaxHeadDim / NWARP;  // 16 state rows per warp at most
 
-// TG: tokens whose inputs are staged together (1 for a single step, NWARP otherwise)
-template <int TG>
+// The single step stages one token's inputs (TG = 1; the loops over tokens below run once)
+constexpr int TG = 1;
 struct Smem {
-    // inputs of up to TG tokens: q^, k^ (normalised in place), v, z
+    // inputs of the token: q^, k^ (normalised in place), v, z
     float qn[TG][kMaxHeadDim];
     float kn[TG][kMaxHeadDim];
     float v[TG][kMaxHeadDim];
@@ -92,9 +94,9 @@ __device__ __forceinline__ int col_of(int lane, int c) {
     return VEC4 ? 4 * lane + c : lane + 32 * c;
 }
 
-template <bool VEC4, int TG>
+template <bool VEC4>
 __global__ void __launch_bounds__(NT, 2) decode_kernel(DecodeArgs a) {
-    __shared__ Smem<TG> s;
+    __shared__ Smem s;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int bh = blockIdx.x, h = bh % a.H;
     const int K = a.K, V = a.V;
@@ -128,9 +130,8 @@ __global__ void __launch_bounds__(NT, 2) decode_kernel(DecodeArgs a) {
         }
     }
 
-    // 2. the inputs of TG tokens at a time, staged in shared memory and turned into q^, k^,
-    // k^.q^, beta and alpha (none of it depends on the state); each token then needs two
-    // barriers
+    // 2. the token's inputs, staged in shared memory and turned into q^, k^, k^.q^, beta and
+    // alpha (none of it depends on the state); the step then needs two barriers
     for (int t0 = 0; t0 < a.T; t0 += TG) {
         const int nt = min(TG, a.T - t0);
         if (t0 > 0) __syncthreads();  // the previous group's inputs are read
@@ -278,314 +279,590 @@ __global__ void __launch_bounds__(NT, 2) decode_kernel(DecodeArgs a) {
 
 // ---------------------------------------------------------------- several tokens
 
-// The chunk form (more than four tokens per call), blocks of TB tokens. One CTA of
-// MT = 512 threads per row; the 64 KB state sits in shared memory (one bulk copy, started
-// first, so its latency overlaps the staging of the inputs, the norms and the small Gram
-// products), which leaves the registers free for two CTAs per SM. k^ and q^ are stored
-// token-minor ([row][token]), so that a thread's four tokens of a row are one 16-byte
-// broadcast load in both passes over the state.
+// The chunk form (two or more tokens per call), in blocks of TB = 8 tokens (the last block
+// padded with zero tokens: beta = g = 0 and zero q, k, v, which add exact zeros). The two
+// passes over the state run on the tensor cores through mma.sync m16n8k8 (tf32 operands,
+// fp32 accumulate). One CTA of eight warps per row. The state lives in registers for the
+// whole call as S^T, laid out as the accumulator of the update product: warp w holds value
+// columns j = 16 w .. 16 w + 15 (the product's 16 rows) over all 128 key rows i (16 tiles
+// of 8). The same registers are the A operand of the reductions X^T = S^T K and
+// Y^T = S^T Q when the key index is taken in the order (k-slot c <-> i = 8 s + 2 c,
+// slot c + 4 <-> i = 8 s + 2 c + 1) within tile s, which the B operands follow, so no state
+// element ever moves between threads, and the state is read and written once per call.
+//
+// Per block, with the header's notation (rows of K, Q, V: the block's tokens):
+//   X^T = S0^T K_raw, Y^T = S0^T Q_raw                   (k, q as read: bf16 values)
+//   R = diag(beta) (V - diag(Gamma / |k|) X)               (|k|, |q|: the l2 norms)
+//   (I + A) U = R,  A[t][i] = beta_t D[t][i] (k^_t . k^_i)  (i < t)
+//   O = (diag(Gamma / |q|) Y + P U) / sqrt(K),  P[t][i] = D[t][i] (k^_i . q^_t)  (i <= t)
+//   S_last = Gamma_last S0 + K_raw^T diag(D[last][t] / |k_t|) U
+// The 8 x 8 Gram products come from one warp's m16n8k8 products; the solve, O and U_d run
+// in fp32 on every lane for its two value columns (the quad's four lanes hold the eight
+// tokens of a column and share them by shuffles).
+// Precision: k and q enter the products as their bf16 values (exact in tf32), the norms as
+// scalars afterwards; the state and U_d enter as two tf32 terms (the leading 11 bits and
+// the next 11: within 2^-21 relative of the fp32 value); the increment is added to the fp32
+// state with fmaf.
 constexpr int TB = 8;
-constexpr int MT = 512;
+constexpr int MT = 256;
 constexpr int MW = MT / 32;
+constexpr int KP = kMaxHeadDim + 8;  // row stride of the token-major q and k tiles
+constexpr uint32_t kTf32Mask = 0xffffe000u;
+
+struct MultiSmem {
+    float qr[TB][KP];  // q of the block's tokens as read (bf16 values), token-major
+    float kr[TB][KP];  // k likewise
+    float v[TB][kMaxHeadDim];
+    float z[TB][kMaxHeadDim];
+    float KK[TB][TB];  // kr_t . kr_i
+    float QK[TB][TB];  // qr_t . kr_i
+    float A[TB][TB];   // beta_t D[t][i] (k^_t . k^_i), i < t
+    float P[TB][TB];   // D[t][i] (k^_i . q^_t), i <= t
+    float beta[TB], gam[TB], Gam[TB], dlast[TB], invq[TB], invk[TB];
+    float braw[TB], araw[TB];  // b and a of the block's tokens as read
+    float hconst[2];           // A_log and dt_bias of the row's head
+    float part[MW][TB];        // per-warp sums of o_t^2
+};
+
+// the tf32 value of x's leading 11 significant bits, and of the next 11 of the remainder
+// (x - hi is exact in fp32)
+__device__ __forceinline__ uint32_t tf32_hi(float x) { return __float_as_uint(x) & kTf32Mask; }
+__device__ __forceinline__ uint32_t tf32_lo(float x, uint32_t hi) {
+    return __float_as_uint(x - __uint_as_float(hi)) & kTf32Mask;
+}
+
+// d += a b: one m16n8k8 product, tf32 operands (every operand is passed with its low 13 bits
+// clear), fp32 accumulate. Fragments (g = lane / 4, c = lane % 4): a = A[g][c], A[g+8][c],
+// A[g][c+4], A[g+8][c+4]; b = B[c][g], B[c+4][g]; d = D[g][2c], D[g][2c+1], D[g+8][2c],
+// D[g+8][2c+1].
+__device__ __forceinline__ void mma8(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                     uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// An accumulator fragment (rows g, g + 8; columns 2c, 2c + 1) as the A operand of a product
+// over those columns, in the permuted k order (slot c <-> column 2c, slot c + 4 <-> 2c + 1),
+// split into its two tf32 terms.
+__device__ __forceinline__ void acc_as_a(const float (&d)[4], uint32_t (&hi)[4], uint32_t (&lo)[4]) {
+    const float x[4] = {d[0], d[2], d[1], d[3]};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        hi[e] = tf32_hi(x[e]);
+        lo[e] = tf32_lo(x[e], hi[e]);
+    }
+}
+
+// Eight consecutive bf16 elements e0 .. e0 + 7 of a row of n as floats (zero beyond n): one
+// 16-byte load when `vec` (the row is 16-byte aligned) and all eight are in the row.
+__device__ __forceinline__ void load8(const __nv_bfloat16* row, int n, int e0, bool vec,
+                                      float (&x)[8]) {
+    if (vec && e0 + 8 <= n) {
+        const uint4 w = __ldcs(reinterpret_cast<const uint4*>(row + e0));
+        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            x[2 * e] = __uint_as_float(u[e] << 16);
+            x[2 * e + 1] = __uint_as_float(u[e] & 0xffff0000u);
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = e0 + e < n ? __bfloat162float(row[e0 + e]) : 0.f;
+    }
+}
+
+// Eight bf16 elements (16 bytes of shared memory) as floats.
+__device__ __forceinline__ void bf16x8_to_float(const __nv_bfloat16* p, float (&x)[8]) {
+    const uint4 w = *reinterpret_cast<const uint4*>(p);
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        x[2 * e] = __uint_as_float(u[e] << 16);
+        x[2 * e + 1] = __uint_as_float(u[e] & 0xffff0000u);
+    }
+}
+
+__device__ __forceinline__ void zero8(float (&x)[8]) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = 0.f;
+}
+
+// Dynamic shared memory of the pipelined form (1024-byte aligned): the state of the CTA's
+// next row as four tensor-copy boxes of 32 value columns x 128 key rows with the 128-byte
+// swizzle (the 16-byte chunk c of key row i sits at chunk c ^ (i mod 8), so the fragment
+// loads out of it hit 32 distinct banks), and the q, k, v, z rows of its next block of
+// tokens (one box each). Both copies fill zeros outside K x V and beyond the last token.
+struct MultiPipe {
+    float S[4][kMaxHeadDim][32];
+    __nv_bfloat16 in[4][TB][kMaxHeadDim];  // q, k, v, z
+    uint64_t bar[2];                       // 0: the state landed, 1: the inputs landed
+};
+constexpr uint32_t kStateBytes = sizeof(float) * 4 * kMaxHeadDim * 32;
+constexpr uint32_t kInputBytes = sizeof(__nv_bfloat16) * 4 * TB * kMaxHeadDim;
 constexpr uint64_t kDecodeWaitNs = 2000000000ull;
 
 // Status bit of a bounded wait of this file that ran out (decode_take_status).
 __device__ uint32_t g_decode_status = 0;
 
-struct MultiSmem {
-    float S[kMaxHeadDim * kMaxHeadDim];  // the state, row-major [K][V] (row stride 128)
-    float kT[kMaxHeadDim][TB];           // k^ token-minor (zero rows for padding tokens)
-    float qT[kMaxHeadDim][TB];           // q^ token-minor
-    float v[TB][kMaxHeadDim];
-    float z[TB][kMaxHeadDim];
-    float X[TB][kMaxHeadDim];            // S0^T k^_t (partials summed), then u_t
-    float Y[TB][kMaxHeadDim];            // S0^T q^_t, then the un-normalised o_t
-    float red[2][2 * TB][kMaxHeadDim];   // the second row half's partial sums
-    float A[TB][TB];                     // beta_t D[t][i] (k^_t . k^_i), i < t
-    float P[TB][TB];                     // D[t][i] (k^_i . q^_t), i <= t
-    float kk[TB][TB], kq[TB][TB];
-    float gam[TB], Gam[TB], dlast[TB], beta[TB], g[TB], inv[2][TB];
-    float ssq[TB][kMaxHeadDim / 32];
-    unsigned long long bar;
-    int failed;
-};
+#ifdef GDN_TRACE
+// Profiling aid, compiled only with -DGDN_TRACE: SM clock stamps of the phases of the
+// first four rows of the multi-token CTAs 0 and 1, per warp (gdn_decode_trace_read).
+__device__ unsigned long long g_dtrace[2][4][16][8];
+#define DTR(ev)                                                                        \
+    do {                                                                               \
+        if (blockIdx.x < 2 && rit < 4 && lane == 0) g_dtrace[blockIdx.x][rit][ev][w] = clock64(); \
+    } while (0)
+#else
+#define DTR(ev) \
+    do {        \
+    } while (0)
+#endif
 
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ uint64_t globaltimer() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Waits (at most kDecodeWaitNs) for phase 0 of the mbarrier at `bar`; false if it ran out.
-__device__ __forceinline__ bool wait_phase0(uint32_t bar) {
-    const uint64_t t_start = globaltimer();
-    while (true) {
-        uint32_t ok;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(ok)
-            : "r"(bar)
-            : "memory");
-        if (ok) return true;
-        if (globaltimer() - t_start > kDecodeWaitNs) return false;
-    }
-}
-
-template <bool FULL>  // FULL: K = V = 128 (one bulk copy of the state)
-__global__ void __launch_bounds__(MT, 2) decode_multi_kernel(DecodeArgs a) {
-    extern __shared__ __align__(128) uint8_t smraw[];
-    MultiSmem& s = *reinterpret_cast<MultiSmem*>(smraw);
+// PIPE: persistent CTAs (two per SM), each taking rows blockIdx.x, blockIdx.x + gridDim.x,
+// ...: the next row's state and the next block's inputs are copied into shared memory by
+// the tensor-copy engine while the current block computes (maps ms: the state as
+// [BH][K][V] fp32, mq .. mz: the inputs as [T][BH][K or V] bf16; needs K, V multiples of
+// 8). Otherwise one CTA per row, the state read straight into registers (any K, V <= 128).
+// FULL: K = V = 128.
+template <bool PIPE, bool FULL>
+__global__ void __launch_bounds__(MT, 2)
+    decode_multi_kernel(const __grid_constant__ CUtensorMap ms,
+                        const __grid_constant__ CUtensorMap mq,
+                        const __grid_constant__ CUtensorMap mk,
+                        const __grid_constant__ CUtensorMap mv,
+                        const __grid_constant__ CUtensorMap mz, DecodeArgs a) {
+    __shared__ __align__(16) MultiSmem s;
+    extern __shared__ __align__(1024) uint8_t dsm_raw[];
+    MultiPipe& pp = *reinterpret_cast<MultiPipe*>(
+        dsm_raw + ((1024u - (smem_u32(dsm_raw) & 1023u)) & 1023u));
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    const int bh = blockIdx.x, h = bh % a.H;
-    const int K = a.K, V = a.V;
-    const float* S0 = a.state_in + (size_t)bh * K * V;
-    float* S1 = a.state_out + (size_t)bh * K * V;
+    const int g = lane >> 2, c = lane & 3;
+    const int K = FULL ? kMaxHeadDim : a.K, V = FULL ? kMaxHeadDim : a.V;
+    const int j0 = 16 * w;  // this warp's value columns j0 .. j0 + 15
     const size_t BH = (size_t)a.BH;
+    const int G = PIPE ? (int)gridDim.x : a.BH;  // row stride of this CTA's rows
     const float rsK = 1.f / sqrtf((float)K);
-    const uint32_t bar = smem_addr(&s.bar);
+    // norm weights of this thread's two columns
+    const float nw0 = j0 + g < V ? a.norm_weight[j0 + g] : 0.f;
+    const float nw1 = j0 + g + 8 < V ? a.norm_weight[j0 + g + 8] : 0.f;
+    const bool vec_qk = (K % 8) == 0;  // rows of q, k (v, z) start 16-byte aligned
+    const bool vec_vz = (V % 8) == 0;
 
-    // 0. the state: one bulk copy (K = V = 128), else plain loads with zero padding
-    if (FULL) {
+    // copies of the pipelined form (one thread each): the state of row r, and the inputs
+    // of the block of row r starting at token t0
+    auto issue_state = [&](int r) {
+        mbar_arrive_expect_tx(&pp.bar[0], kStateBytes);
+        for (int b = 0; b < 4; ++b) tma_load_3d(&pp.S[b][0][0], &ms, &pp.bar[0], 32 * b, 0, r);
+    };
+    auto issue_inputs = [&](int r, int t0) {
+        mbar_arrive_expect_tx(&pp.bar[1], kInputBytes);
+        tma_load_3d(&pp.in[0][0][0], &mq, &pp.bar[1], 0, r, t0);
+        tma_load_3d(&pp.in[1][0][0], &mk, &pp.bar[1], 0, r, t0);
+        tma_load_3d(&pp.in[2][0][0], &mv, &pp.bar[1], 0, r, t0);
+        tma_load_3d(&pp.in[3][0][0], &mz, &pp.bar[1], 0, r, t0);
+    };
+    // raw b and a of token `lane` of the block (r, t0), and on lanes 8, 9 A_log and dt_bias
+    // of the row's head (warp 1), loaded a block ahead and carried to the block's start
+    float nb = 0.f, na = 0.f;
+    auto load_gates = [&](int r, int t0) {
+        nb = na = 0.f;
+        if (lane < TB && t0 + lane < a.T) {
+            const size_t row = (size_t)(t0 + lane) * BH + (size_t)r;
+            nb = __bfloat162float(a.b[row]);
+            na = __bfloat162float(a.a[row]);
+        } else if (lane == TB || lane == TB + 1) {
+            nb = (lane == TB ? a.A_log : a.dt_bias)[r % a.H];
+        }
+    };
+    uint32_t ph_state = 0, ph_in = 0;
+    bool state_pending = false, in_pending = false, failed = false;
+    if (PIPE) {
         if (tid == 0) {
-            s.failed = 0;
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
-            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
-                         "r"(65536u)
-                         : "memory");
-            asm volatile(
-                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], "
-                "%2, [%3];" ::"r"(smem_addr(s.S)),
-                "l"(reinterpret_cast<uint64_t>(S0)), "r"(65536u), "r"(bar)
-                : "memory");
+            mbar_init(&pp.bar[0], 1);
+            mbar_init(&pp.bar[1], 1);
+            fence_mbar_init();
         }
-    } else {
-        for (int e = tid; e < kMaxHeadDim * kMaxHeadDim; e += MT) {
-            const int i = e / kMaxHeadDim, j = e % kMaxHeadDim;
-            s.S[e] = (i < K && j < V) ? __ldcs(S0 + (size_t)i * V + j) : 0.f;
+        __syncthreads();
+        if (tid == 0) {
+            issue_state(blockIdx.x);
+            issue_inputs(blockIdx.x, 0);
         }
-        if (tid == 0) s.failed = 0;
+        if (w == 1) load_gates(blockIdx.x, 0);
+        state_pending = in_pending = true;
     }
 
-    for (int t0 = 0; t0 < a.T; t0 += TB) {
-        const int nt = min(TB, a.T - t0);  // real tokens of this block
-        const bool last = t0 + TB >= a.T;
-        __syncthreads();  // (the mbarrier is initialised; the previous block is done)
-        // 1. inputs of the block (padding tokens: zero rows, beta = 0, g = 0)
-        for (int e = tid; e < TB * kMaxHeadDim; e += MT) {
-            const int t = e / kMaxHeadDim, i = e % kMaxHeadDim;
-            const size_t row = (size_t)(t0 + t) * BH + (size_t)bh;
-            const bool real = t < nt;
-            s.qT[i][t] = (real && i < K) ? __bfloat162float(a.q[row * K + i]) : 0.f;
-            s.kT[i][t] = (real && i < K) ? __bfloat162float(a.k[row * K + i]) : 0.f;
-            s.v[t][i] = (real && i < V) ? __bfloat162float(a.v[row * V + i]) : 0.f;
-            s.z[t][i] = (real && i < V) ? __bfloat162float(a.z[row * V + i]) : 0.f;
-        }
-        if (tid < TB) {
-            const size_t row = (size_t)(t0 + tid) * BH + (size_t)bh;
-            const bool real = tid < nt;
-            s.beta[tid] = real ? sigmoid_f(__bfloat162float(a.b[row])) : 0.f;
-            s.g[tid] = real ? -expf(a.A_log[h]) *
-                                  softplus_f(__bfloat162float(a.a[row]) + a.dt_bias[h])
-                            : 0.f;
-        }
-        __syncthreads();
-        // 2. the l2 norms (warp j: token j / 2, q or k), the decay prefix (one thread)
-        if (w < 2 * TB) {
-            const int t = w >> 1;
-            float acc = 0.f;
+    int rit = 0;
+    for (int r = blockIdx.x; r < a.BH && !failed; r += G, ++rit) {
+        const int h = r % a.H;
+        // the state as S^T fragments: st[s][e] = S[i][j] with i = 8 s + 2 c + (e & 1),
+        // j = j0 + g + 8 (e >> 1) (zero outside K x V)
+        float st[16][4];
+        if (!PIPE) {
+            const float* S0 = a.state_in + (size_t)r * K * V;
 #pragma unroll
-            for (int i = lane; i < kMaxHeadDim; i += 32) {
-                const float x = (w & 1) ? s.kT[i][t] : s.qT[i][t];
-                acc = fmaf(x, x, acc);
-            }
-            acc = warp_sum(acc);
-            if (lane == 0) s.inv[w & 1][t] = 1.f / sqrtf(acc + kEpsL2);
-        }
-        if (tid == MT - 1) {
-            float gm = 0.f;
+            for (int s8 = 0; s8 < 16; ++s8) {
 #pragma unroll
-            for (int t = 0; t < TB; ++t) {
-                gm += s.g[t];
-                s.gam[t] = gm;
-                s.Gam[t] = expf(gm);
-            }
-#pragma unroll
-            for (int t = 0; t < TB; ++t) s.dlast[t] = expf(gm - s.gam[t]);
-        }
-        __syncthreads();
-        for (int e = tid; e < TB * kMaxHeadDim; e += MT) {
-            const int i = e / TB, t = e % TB;
-            s.qT[i][t] *= s.inv[0][t];
-            s.kT[i][t] *= s.inv[1][t];
-        }
-        __syncthreads();
-        // 3. the small Gram products k^_t . k^_i and k^_i . q^_t (i <= t): four adjacent
-        // threads per product, thread `part` taking rows part, part + 4, ... (so a warp's
-        // loads fall in distinct banks), joined by two shuffles
-        {
-            const int part = tid & 3, pr = tid >> 2;  // pr: 0..127
-            const int kind = pr >> 6, t = (pr >> 3) & 7, i = pr & 7;
-            float acc = 0.f;
-            if (i <= t) {
-#pragma unroll 8
-                for (int e = part; e < kMaxHeadDim; e += 4)
-                    acc = fmaf(s.kT[e][i], kind ? s.qT[e][t] : s.kT[e][t], acc);
-            }
-            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-            acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-            if (part == 0 && i <= t) {
-                if (kind) s.kq[t][i] = acc;
-                else s.kk[t][i] = acc;
-            }
-        }
-        // the state has landed (first block); a copy that never lands is waited for once
-        // more before the CTA leaves
-        if (FULL && t0 == 0 && !wait_phase0(bar)) {
-            atomicOr(&g_decode_status, 1u);
-            s.failed = 1;
-        }
-        __syncthreads();
-        if (s.failed) {
-            if (tid == 0) wait_phase0(bar);
-            return;
-        }
-        // 4. X[t] = S0^T k^_t and Y[t] = S0^T q^_t: thread (column j, tokens 4 th .. 4 th + 3,
-        // rows 64 rh .. 64 rh + 63); the second row half adds its partials through red
-        {
-            const int j = tid & (kMaxHeadDim - 1), th = (tid >> 7) & 1, rh = tid >> 8;
-            // token pairs in paired fp32 FMAs (each lane rounds as fmaf)
-            float2 x01 = make_float2(0.f, 0.f), x23 = x01, y01 = x01, y23 = x01;
-#pragma unroll 4
-            for (int i = 64 * rh; i < 64 * rh + 64; ++i) {
-                const float sv = s.S[i * kMaxHeadDim + j];
-                const float2 ss = make_float2(sv, sv);
-                const float4 k4 = *reinterpret_cast<const float4*>(&s.kT[i][4 * th]);
-                const float4 q4 = *reinterpret_cast<const float4*>(&s.qT[i][4 * th]);
-                x01 = ffma2(make_float2(k4.x, k4.y), ss, x01);
-                x23 = ffma2(make_float2(k4.z, k4.w), ss, x23);
-                y01 = ffma2(make_float2(q4.x, q4.y), ss, y01);
-                y23 = ffma2(make_float2(q4.z, q4.w), ss, y23);
-            }
-            const float px[4] = {x01.x, x01.y, x23.x, x23.y};
-            const float py[4] = {y01.x, y01.y, y23.x, y23.y};
-            if (rh == 1) {
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    s.red[0][4 * th + r][j] = px[r];
-                    s.red[1][4 * th + r][j] = py[r];
-                }
-            }
-            __syncthreads();
-            if (rh == 0) {
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    s.X[4 * th + r][j] = px[r] + s.red[0][4 * th + r][j];
-                    s.Y[4 * th + r][j] = py[r] + s.red[1][4 * th + r][j];
+                for (int e = 0; e < 4; ++e) {
+                    const int i = 8 * s8 + 2 * c + (e & 1), j = j0 + g + 8 * (e >> 1);
+                    st[s8][e] = (i < K && j < V) ? __ldcs(S0 + (size_t)i * V + j) : 0.f;
                 }
             }
         }
-        // the coefficients of the solve and of the outputs
-        if (tid >= MT - TB * TB) {
-            const int e = tid - (MT - TB * TB), t = e / TB, i = e % TB;
-            const float d = (i <= t) ? expf(s.gam[t] - s.gam[i]) : 0.f;
-            s.A[t][i] = (i < t) ? s.beta[t] * d * s.kk[t][i] : 0.f;
-            s.P[t][i] = (i <= t) ? d * s.kq[t][i] : 0.f;
-        }
-        __syncthreads();
-        // 5. column j: the solve for u_t, then o_t (u into X, o into Y), and the partial
-        // sums of o_t^2 per warp
-        if (tid < kMaxHeadDim) {
-            const int j = tid;
-            float u[TB], o[TB];
+        for (int t0 = 0; t0 < a.T; t0 += TB) {
+            const int nt = min(TB, a.T - t0);  // real tokens of this block
+            if (PIPE) {
+                // this block's gates (read a block ahead) and copies; one barrier also
+                // orders the previous block's reads of the tiles before they are rewritten
+                DTR(0);
+                if (w == 1 && lane < TB) {
+                    s.braw[lane] = nb;
+                    s.araw[lane] = na;
+                }
+                if (w == 1 && (lane == TB || lane == TB + 1)) s.hconst[lane - TB] = nb;
+                bool ok = mbar_wait_bounded(&pp.bar[1], ph_in, kDecodeWaitNs);
+                if (t0 == 0) ok = ok && mbar_wait_bounded(&pp.bar[0], ph_state, kDecodeWaitNs);
+                if (!__syncthreads_and(ok)) {
+                    failed = true;
+                    break;
+                }
+                DTR(1);
+                ph_in ^= 1;
+                in_pending = false;
+                if (t0 == 0) {
+                    ph_state ^= 1;
+                    state_pending = false;
+                    // element (i, j) of box j / 32 at row i, chunk ((j % 32) / 4) ^ (i % 8);
+                    // i % 8 = 2 c + (e & 1) for every tile
+                    const float* box = &pp.S[w >> 1][0][0];
 #pragma unroll
-            for (int t = 0; t < TB; ++t) {
-                float r = (j < V) ? s.beta[t] * (s.v[t][j] - s.Gam[t] * s.X[t][j]) : 0.f;
+                    for (int e = 0; e < 4; ++e) {
+                        const int e0 = e & 1, ch = (4 * (w & 1) + 2 * (e >> 1) + (g >> 2)) ^ (2 * c + e0);
+                        const float* src = box + (2 * c + e0) * 32 + 4 * ch + (g & 3);
 #pragma unroll
-                for (int i = 0; i < t; ++i) r = fmaf(-s.A[t][i], u[i], r);
-                u[t] = r;
-                float y = s.Gam[t] * s.Y[t][j];
-#pragma unroll
-                for (int i = 0; i <= t; ++i) y = fmaf(s.P[t][i], u[i], y);
-                o[t] = (j < V) ? y * rsK : 0.f;
+                        for (int s8 = 0; s8 < 16; ++s8) st[s8][e] = src[256 * s8];
+                    }
+                }
+            } else if (t0 > 0) {
+                __syncthreads();  // the previous block's tiles are read
             }
-#pragma unroll
-            for (int t = 0; t < TB; ++t) {
-                s.X[t][j] = u[t] * s.dlast[t];  // the update pass needs D[last][t] u_t
-                s.Y[t][j] = o[t];
-                const float sq = warp_sum(o[t] * o[t]);
-                if (lane == 0) s.ssq[t][w] = sq;
-            }
-        }
-        __syncthreads();
-        // 6. RMSNormGated of each real token
-        for (int e = tid; e < nt * kMaxHeadDim; e += MT) {
-            const int t = e / kMaxHeadDim, j = e % kMaxHeadDim;
-            if (j >= V) continue;
-            float ms = 0.f;
-#pragma unroll
-            for (int ww = 0; ww < kMaxHeadDim / 32; ++ww) ms += s.ssq[t][ww];
-            ms /= (float)V;
-            const float zj = s.z[t][j];
-            const float y = s.Y[t][j] * (1.f / sqrtf(ms + kEpsRms)) * a.norm_weight[j] *
-                            (zj * sigmoid_f(zj));
-            const size_t row = (size_t)(t0 + t) * BH + (size_t)bh;
-            a.out[row * V + j] = __float2bfloat16_rn(y);
-        }
-        // 7. S_last = Gamma_last S0 + sum_t D[last][t] k^_t u_t^T: thread (column j, rows
-        // 32 rq .. 32 rq + 31); written to global memory after the last block, else back
-        // to shared memory for the next one (a padding token adds exact zeros)
-        {
-            const int j = tid & (kMaxHeadDim - 1), rq = tid >> 7;
-            const float Gl = s.Gam[TB - 1];
-            // the token pairs (0,1), (2,3), (4,5), (6,7) in paired fp32 FMAs, the two halves
-            // added at the end
-            const float2 u01 = make_float2(s.X[0][j], s.X[1][j]);
-            const float2 u23 = make_float2(s.X[2][j], s.X[3][j]);
-            const float2 u45 = make_float2(s.X[4][j], s.X[5][j]);
-            const float2 u67 = make_float2(s.X[6][j], s.X[7][j]);
-#pragma unroll 4
-            for (int i = 32 * rq; i < 32 * rq + 32; ++i) {
-                const float4 k0 = *reinterpret_cast<const float4*>(&s.kT[i][0]);
-                const float4 k1 = *reinterpret_cast<const float4*>(&s.kT[i][4]);
-                float2 acc = make_float2(Gl * s.S[i * kMaxHeadDim + j], 0.f);
-                acc = ffma2(make_float2(k0.x, k0.y), u01, acc);
-                acc = ffma2(make_float2(k0.z, k0.w), u23, acc);
-                acc = ffma2(make_float2(k1.x, k1.y), u45, acc);
-                acc = ffma2(make_float2(k1.z, k1.w), u67, acc);
-                const float x = acc.x + acc.y;
-                if (last) {
-                    if (i < K && j < V) __stcs(S1 + (size_t)i * V + j, x);
+            // 1. inputs: 16 x 8 elements per input row, the 32 rows (q, k, v, z of 8
+            // tokens) in two rounds; q and k with their squared norms (16 lanes per row)
+            {
+                const int rr = tid >> 4, p = tid & 15, t = rr & 7;
+                const bool isk = rr >= 8;
+                float x[8];
+                if (PIPE) {
+                    bf16x8_to_float(&pp.in[isk ? 1 : 0][t][8 * p], x);
+                } else if (t < nt) {
+                    const size_t row = (size_t)(t0 + t) * BH + (size_t)r;
+                    load8((isk ? a.k : a.q) + row * K, K, 8 * p, vec_qk, x);
                 } else {
-                    s.S[i * kMaxHeadDim + j] = x;
+                    zero8(x);
+                }
+                float ss = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+#pragma unroll
+                for (int off = 8; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+                if (p == 0) (isk ? s.invk : s.invq)[t] = 1.f / sqrtf(ss + kEpsL2);
+                float* dst = isk ? &s.kr[t][8 * p] : &s.qr[t][8 * p];
+                *reinterpret_cast<float4*>(dst) = make_float4(x[0], x[1], x[2], x[3]);
+                *reinterpret_cast<float4*>(dst + 4) = make_float4(x[4], x[5], x[6], x[7]);
+            }
+            {
+                const int rr = (tid >> 4) + 16, p = tid & 15, t = rr & 7;
+                const bool isz = rr >= 24;
+                float x[8];
+                if (PIPE) {
+                    bf16x8_to_float(&pp.in[isz ? 3 : 2][t][8 * p], x);
+                } else if (t < nt) {
+                    const size_t row = (size_t)(t0 + t) * BH + (size_t)r;
+                    load8((isz ? a.z : a.v) + row * V, V, 8 * p, vec_vz, x);
+                } else {
+                    zero8(x);
+                }
+                float* dst = isz ? &s.z[t][8 * p] : &s.v[t][8 * p];
+                *reinterpret_cast<float4*>(dst) = make_float4(x[0], x[1], x[2], x[3]);
+                *reinterpret_cast<float4*>(dst + 4) = make_float4(x[4], x[5], x[6], x[7]);
+            }
+            // gates of token t on lane t of warp 1, the decay prefix gamma_t over the block
+            if (w == 1) {
+                const int t = lane & 7;
+                float bt = 0.f, gt = 0.f;
+                if (lane < TB && t < nt) {
+                    float braw, araw, alog, dtb;
+                    if (PIPE) {
+                        braw = s.braw[t];
+                        araw = s.araw[t];
+                        alog = s.hconst[0];
+                        dtb = s.hconst[1];
+                    } else {
+                        const size_t row = (size_t)(t0 + t) * BH + (size_t)r;
+                        braw = __bfloat162float(a.b[row]);
+                        araw = __bfloat162float(a.a[row]);
+                        alog = a.A_log[h];
+                        dtb = a.dt_bias[h];
+                    }
+                    bt = sigmoid_f(braw);
+                    gt = -expf(alog) * softplus_f(araw + dtb);
+                }
+                float gm = gt;
+#pragma unroll
+                for (int off = 1; off < TB; off <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, gm, off);
+                    if (t >= off) gm += y;
+                }
+                const float glast = __shfl_sync(0xffffffffu, gm, TB - 1);
+                if (lane < TB) {
+                    s.beta[t] = bt;
+                    s.gam[t] = gm;
+                    s.Gam[t] = expf(gm);
+                    s.dlast[t] = expf(glast - gm);
+                }
+            }
+            DTR(2);
+            __syncthreads();
+            DTR(3);
+            if (PIPE) {
+                // the staged state and inputs are read: the next copies go out now
+                int nr = r, nt0 = t0 + TB;
+                if (nt0 >= a.T) nr = r + G, nt0 = 0;
+                if (t0 == 0 && r + G < a.BH) {
+                    if (tid == 32) issue_state(r + G);
+                    state_pending = true;
+                }
+                if (nr < a.BH) {
+                    if (tid == 32) issue_inputs(nr, nt0);
+                    if (w == 1) load_gates(nr, nt0);
+                    in_pending = true;
+                }
+            }
+            // 2. warp 0: the Gram products [K_raw; Q_raw] K_raw^T (m16n8k8 over the keys, four
+            // partial sums), then the coefficients A and P (zero outside their triangles)
+            if (w == 0) {
+                float d[4][4] = {};
+#pragma unroll
+                for (int s8 = 0; s8 < 16; ++s8) {
+                    const float2 ka = *reinterpret_cast<const float2*>(&s.kr[g][8 * s8 + 2 * c]);
+                    const float2 qa = *reinterpret_cast<const float2*>(&s.qr[g][8 * s8 + 2 * c]);
+                    const uint32_t af[4] = {__float_as_uint(ka.x), __float_as_uint(qa.x),
+                                            __float_as_uint(ka.y), __float_as_uint(qa.y)};
+                    mma8(d[s8 & 3], af, __float_as_uint(ka.x), __float_as_uint(ka.y));
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) d[0][e] = (d[0][e] + d[1][e]) + (d[2][e] + d[3][e]);
+                s.KK[g][2 * c] = d[0][0];
+                s.KK[g][2 * c + 1] = d[0][1];
+                s.QK[g][2 * c] = d[0][2];
+                s.QK[g][2 * c + 1] = d[0][3];
+                __syncwarp();
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int t = lane >> 2, i = 2 * c + e;
+                    const float D = i <= t ? expf(s.gam[t] - s.gam[i]) : 0.f;
+                    s.A[t][i] = i < t ? s.beta[t] * D * (s.invk[t] * s.invk[i]) * s.KK[t][i] : 0.f;
+                    s.P[t][i] = D * (s.invk[i] * s.invq[t]) * s.QK[t][i];
+                }
+            }
+
+            DTR(4);
+            // 3. X^T = S0^T K_raw and Y^T = S0^T Q_raw for this warp's 16 columns (x[e], y[e]:
+            // column j0 + g + 8 (e >> 1), token 2c + (e & 1))
+            float x[4] = {0.f, 0.f, 0.f, 0.f}, y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int s8 = 0; s8 < 16; ++s8) {
+                uint32_t ah[4], al[4];
+                acc_as_a(st[s8], ah, al);
+                const float2 kb = *reinterpret_cast<const float2*>(&s.kr[g][8 * s8 + 2 * c]);
+                const float2 qb = *reinterpret_cast<const float2*>(&s.qr[g][8 * s8 + 2 * c]);
+                const uint32_t k0 = __float_as_uint(kb.x), k1 = __float_as_uint(kb.y);
+                const uint32_t q0 = __float_as_uint(qb.x), q1 = __float_as_uint(qb.y);
+                mma8(x, al, k0, k1);
+                mma8(y, al, q0, q1);
+                mma8(x, ah, k0, k1);
+                mma8(y, ah, q0, q1);
+            }
+            DTR(5);
+            __syncthreads();  // A, P and the scalars are written
+            DTR(6);
+
+            // 4. R^T (r[e]: column j0 + g + 8 (e >> 1), token 2c + (e & 1)); each lane gathers
+            // the eight tokens of its two columns from its quad and solves (I + A) U = R by
+            // forward substitution in fp32 (u0: column j0 + g, u1: column j0 + g + 8), then
+            // forms its own tokens' outputs o = Gamma / |q| Y + P U (before the 1 / sqrt(K))
+            // and U_d = D[last][t] / |k_t| u_t for the state update
+            float ud[4], o[4];
+            {
+                float r[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int t = 2 * c + (e & 1), j = j0 + g + 8 * (e >> 1);
+                    r[e] = s.beta[t] * (s.v[t][j] - s.Gam[t] * (s.invk[t] * x[e]));
+                }
+                float u0[TB], u1[TB];
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const int src = (lane & ~3) | cc;
+                    u0[2 * cc] = __shfl_sync(0xffffffffu, r[0], src);
+                    u0[2 * cc + 1] = __shfl_sync(0xffffffffu, r[1], src);
+                    u1[2 * cc] = __shfl_sync(0xffffffffu, r[2], src);
+                    u1[2 * cc + 1] = __shfl_sync(0xffffffffu, r[3], src);
+                }
+#pragma unroll
+                for (int t = 1; t < TB; ++t) {
+#pragma unroll
+                    for (int i = 0; i < t; ++i) {
+                        const float at = s.A[t][i];
+                        u0[t] = fmaf(-at, u0[i], u0[t]);
+                        u1[t] = fmaf(-at, u1[i], u1[t]);
+                    }
+                }
+#pragma unroll
+                for (int e0 = 0; e0 < 2; ++e0) {
+                    const int t = 2 * c + e0;
+                    float o0 = 0.f, o1 = 0.f;
+#pragma unroll
+                    for (int i = 0; i < TB; ++i) {
+                        const float pt = s.P[t][i];
+                        o0 = fmaf(pt, u0[i], o0);
+                        o1 = fmaf(pt, u1[i], o1);
+                    }
+                    const float gy = s.Gam[t] * s.invq[t];
+                    o[e0] = fmaf(gy, y[e0], o0);
+                    o[2 + e0] = fmaf(gy, y[2 + e0], o1);
+                    // u_t of this lane's token t = 2c + e0 (selects, no dynamic register index)
+                    float a0 = u0[e0], a1 = u1[e0];
+#pragma unroll
+                    for (int cc = 1; cc < 4; ++cc) {
+                        if (c == cc) {
+                            a0 = u0[2 * cc + e0];
+                            a1 = u1[2 * cc + e0];
+                        }
+                    }
+                    const float sc = s.dlast[t] * s.invk[t];
+                    ud[e0] = sc * a0;
+                    ud[2 + e0] = sc * a1;
+                }
+            }
+            // 5. o / sqrt(K); RMSNormGated per token over the V columns (the columns beyond V
+            // hold zeros)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[e] *= rsK;
+            {
+                float s0 = fmaf(o[0], o[0], o[2] * o[2]), s1 = fmaf(o[1], o[1], o[3] * o[3]);
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    s0 += __shfl_xor_sync(0xffffffffu, s0, off);
+                    s1 += __shfl_xor_sync(0xffffffffu, s1, off);
+                }
+                if (g == 0) {
+                    s.part[w][2 * c] = s0;
+                    s.part[w][2 * c + 1] = s1;
+                }
+            }
+            DTR(7);
+            __syncthreads();
+            DTR(8);
+            {
+                float m0 = 0.f, m1 = 0.f;
+#pragma unroll
+                for (int ww = 0; ww < MW; ++ww) {
+                    m0 += s.part[ww][2 * c];
+                    m1 += s.part[ww][2 * c + 1];
+                }
+                const float rstd[2] = {1.f / sqrtf(m0 / (float)V + kEpsRms),
+                                       1.f / sqrtf(m1 / (float)V + kEpsRms)};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int t = 2 * c + (e & 1), j = j0 + g + 8 * (e >> 1);
+                    if (t < nt && j < V) {
+                        const float zj = s.z[t][j];
+                        const float yv = o[e] * rstd[e & 1] * ((e >> 1) ? nw1 : nw0) *
+                                         (zj * sigmoid_f(zj));
+                        const size_t row = (size_t)(t0 + t) * BH + (size_t)r;
+                        a.out[row * V + j] = __float2bfloat16_rn(yv);
+                    }
+                }
+            }
+            DTR(9);
+            // 6. S^T <- Gamma_last S^T + U_d^T K_raw, tile by tile (B: k of tokens 2c, 2c + 1)
+            {
+                uint32_t uh[4], ul[4];
+                acc_as_a(ud, uh, ul);
+                const float Gl = s.Gam[TB - 1];
+#pragma unroll
+                for (int s8 = 0; s8 < 16; ++s8) {
+                    const uint32_t b0 = __float_as_uint(s.kr[2 * c][8 * s8 + g]);
+                    const uint32_t b1 = __float_as_uint(s.kr[2 * c + 1][8 * s8 + g]);
+                    float d[4] = {0.f, 0.f, 0.f, 0.f};
+                    mma8(d, ul, b0, b1);
+                    mma8(d, uh, b0, b1);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) st[s8][e] = fmaf(Gl, st[s8][e], d[e]);
                 }
             }
         }
+        DTR(10);
+        if (failed) break;
+        // the state, written once
+        float* S1 = a.state_out + (size_t)r * K * V;
+#pragma unroll
+        for (int s8 = 0; s8 < 16; ++s8) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int i = 8 * s8 + 2 * c + (e & 1), j = j0 + g + 8 * (e >> 1);
+                if (i < K && j < V) __stcs(S1 + (size_t)i * V + j, st[s8][e]);
+            }
+        }
+        DTR(11);
+    }
+    if (PIPE && failed && tid == 0) {
+        // a copy gave up: the copies still in flight land before the CTA leaves
+        atomicOr(&g_decode_status, 1u);
+        if (state_pending) mbar_wait_bounded(&pp.bar[0], ph_state, kDecodeWaitNs);
+        if (in_pending) mbar_wait_bounded(&pp.bar[1], ph_in, kDecodeWaitNs);
     }
 }
 
-template <bool FULL>
-cudaError_t launch_multi(const DecodeArgs& a, cudaStream_t stream) {
-    static cudaError_t attr = [] {
-        // shared memory above the default 48 KB, and the largest carveout so that two CTAs
-        // fit an SM
-        cudaError_t e = cudaFuncSetAttribute(decode_multi_kernel<FULL>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)sizeof(MultiSmem));
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(decode_multi_kernel<FULL>,
-                                     cudaFuncAttributePreferredSharedMemoryCarveout,
-                                     (int)cudaSharedmemCarveoutMaxShared);
-        return e;
-    }();
+// 3-D tensor map over [d2][d1][d0] (d0 contiguous) with a box of b0 x b1 x b2
+bool encode_map(CUtensorMap* m, CUtensorMapDataType type, int esize, const void* base,
+                uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1, uint32_t b2,
+                CUtensorMapSwizzle swz) {
+    auto fn = tensor_map_encoder();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {d0 * esize, d0 * d1 * esize};
+    cuuint32_t box[3] = {b0, b1, b2};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, type, 3, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool PIPE, bool FULL>
+cudaError_t launch_multi(const DecodeArgs& a, int sms, cudaStream_t stream) {
+    CUtensorMap ms{}, mq{}, mk{}, mv{}, mz{};
+    if constexpr (!PIPE) {
+        decode_multi_kernel<false, FULL><<<a.BH, MT, 0, stream>>>(ms, mq, mk, mv, mz, a);
+        return cudaGetLastError();
+    }
+    constexpr auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const uint64_t T = (uint64_t)a.T, BH = (uint64_t)a.BH, K = (uint64_t)a.K, V = (uint64_t)a.V;
+    if (!encode_map(&ms, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.state_in, V, K, BH, 32,
+                    kMaxHeadDim, 1, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_map(&mq, BF, 2, a.q, K, BH, T, kMaxHeadDim, 1, TB, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_map(&mk, BF, 2, a.k, K, BH, T, kMaxHeadDim, 1, TB, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_map(&mv, BF, 2, a.v, V, BH, T, kMaxHeadDim, 1, TB, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_map(&mz, BF, 2, a.z, V, BH, T, kMaxHeadDim, 1, TB, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    constexpr int smem = (int)sizeof(MultiPipe) + 1024;  // + alignment slack
+    static cudaError_t attr = cudaFuncSetAttribute(decode_multi_kernel<true, FULL>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (attr != cudaSuccess) return attr;
-    decode_multi_kernel<FULL><<<a.BH, MT, sizeof(MultiSmem), stream>>>(a);
+    const int grid = min(a.BH, 2 * max(sms, 1));
+    decode_multi_kernel<true, FULL><<<grid, MT, smem, stream>>>(ms, mq, mk, mv, mz, a);
     return cudaGetLastError();
 }
 
@@ -593,9 +870,6 @@ cudaError_t launch_multi(const DecodeArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_decode(const DecodeArgs& args, cudaStream_t stream) {
     if (args.BH == 0 || args.T == 0) return cudaSuccess;
-    // two CTAs per SM are resident (launch bounds): rows that far ahead are prefetched, in
-    // the single step, where it was measured to help (the multi-token form, whose CTAs stay
-    // T times as long, measured the same with and without it)
     constexpr int kMaxDevices = 64;
     static int sms_of[kMaxDevices] = {};
     int dev = 0, sms = 0;
@@ -603,24 +877,22 @@ cudaError_t launch_decode(const DecodeArgs& args, cudaStream_t stream) {
         if (sms_of[dev] == 0) cudaDeviceGetAttribute(&sms_of[dev], cudaDevAttrMultiProcessorCount, dev);
         sms = sms_of[dev];
     }
-    DecodeArgs a = args;
-    a.pf_rows = a.T == 1 ? 2 * sms : 0;
-    // More than kPerTokenMaxT tokens: the chunk form (blocks of eight). Up to that, the
-    // token loop, which measured faster there (T = 2: 0.212 against 0.242 ms, T = 4: 0.309
-    // against 0.332 ms at BH = 8192; T = 8: 0.608 against 0.512 ms); a single step stages
-    // one token's inputs (the smaller footprint keeps the streaming step at its bandwidth),
-    // several tokens NWARP at a time.
-    constexpr int kPerTokenMaxT = 4;
-    if (a.T > kPerTokenMaxT)
-        return (a.K == kMaxHeadDim && a.V == kMaxHeadDim) ? launch_multi<true>(a, stream)
-                                                          : launch_multi<false>(a, stream);
-    if (a.V == kMaxHeadDim) {
-        if (a.T == 1) decode_kernel<true, 1><<<a.BH, NT, 0, stream>>>(a);
-        else decode_kernel<true, NWARP><<<a.BH, NT, 0, stream>>>(a);
-    } else {
-        if (a.T == 1) decode_kernel<false, 1><<<a.BH, NT, 0, stream>>>(a);
-        else decode_kernel<false, NWARP><<<a.BH, NT, 0, stream>>>(a);
+    // Two or more tokens: the chunk form (blocks of eight), pipelined when K and V are
+    // multiples of 8 (the tensor copies' 16-byte rows). Measured at BH = 8192 against
+    // the single step's register loop run token after token: T = 2 0.213 against 0.212 ms,
+    // T = 3 0.214 against 0.284, T = 4 0.214 against 0.318.
+    if (args.T > 1) {
+        if (args.K == kMaxHeadDim && args.V == kMaxHeadDim)
+            return launch_multi<true, true>(args, sms, stream);
+        if (args.K % 8 == 0 && args.V % 8 == 0) return launch_multi<true, false>(args, sms, stream);
+        return launch_multi<false, false>(args, sms, stream);
     }
+    // the single step: two CTAs per SM are resident (launch bounds), and the state of the
+    // rows that far ahead is prefetched into L2
+    DecodeArgs a = args;
+    a.pf_rows = 2 * sms;
+    if (a.V == kMaxHeadDim) decode_kernel<true><<<a.BH, NT, 0, stream>>>(a);
+    else decode_kernel<false><<<a.BH, NT, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
@@ -635,3 +907,9 @@ uint32_t decode_take_status() {
 }
 
 }  // namespace gdn
+
+#ifdef GDN_TRACE
+extern "C" int gdn_decode_trace_read(unsigned long long* dst) {
+    return cudaMemcpyFromSymbol(dst, gdn::g_dtrace, sizeof(gdn::g_dtrace)) == cudaSuccess ? 0 : 1;
+}
+#endif

@@ -4,6 +4,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <cstddef>
 #include <cstdint>
@@ -119,6 +120,9 @@ cudaError_t launch_tril_inverse(const float* A, float* T, int n, int algorithm,
 
 // Fused decode step, T tokens in a row (the state read and written once).
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+// cuTensorMapEncodeTiled from the driver (nullptr when the driver has none).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 // Device status word of each translation unit that has bounded waits: returns the
 // bits set since the last call and clears them (the stream must be synchronised).

@@ -1897,7 +1897,9 @@ __global__ void __launch_bounds__(1024) varlen_setup_kernel(const int* cu, int N
 
 // ---------------------------------------------------------------- host side
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+}  // namespace
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
     std::call_once(once, [] {
@@ -1911,9 +1913,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+namespace {
+
 // 3-D bf16 map over [z][y][x] = [heads][S][128], box 64 x 64 x 1, 128-byte swizzle.
 bool encode_3d(CUtensorMap* m, const void* base, int S, int heads) {
-    auto fn = encode_fn();
+    auto fn = tensor_map_encoder();
     if (!fn) return false;
     cuuint64_t dims[3] = {128, (cuuint64_t)S, (cuuint64_t)heads};
     cuuint64_t strides[2] = {128 * 2, (cuuint64_t)S * 128 * 2};

@@ -113,6 +113,23 @@ def test_decode_multi_matches_oracle(K, V, T):
     assert rel(to_np(st), s_ref) <= TOL_BF16["state"]
 
 
+@pytest.mark.parametrize("K,V,T", [(64, 96, 11), (128, 128, 9), (100, 128, 10), (8, 16, 3)])
+def test_decode_multi_many_rows(K, V, T):
+    """400 rows, more than two per SM: a CTA takes several rows in turn, with the next
+    row's state and the next block's inputs copied in while it computes (K, V multiples
+    of 8; K = 100 takes the one-row-per-CTA form). Two blocks of tokens where T > 8. Every
+    row and token against the chained oracle; in place equals out of place bit for bit."""
+    w = syn.DecodeWorkload("t", B=100, num_k_heads=2, num_v_heads=4, K=K, V=V)
+    x = syn.decode_multi_inputs(w, T)
+    y1, s1 = _gpu_multi(x)
+    y2, s2 = _gpu_multi(x, in_place=True)
+    assert torch.equal(y1, y2) and torch.equal(s1, s2)
+    y_ref, s_ref = oracle.decode_multi(*(x[n] for n in MULTI_NAMES), x["num_v_heads"])
+    for t in range(T):
+        assert rel(to_np(y1[t]), y_ref[t]) <= TOL_BF16["out"], f"token {t}"
+    assert rel(to_np(s1), s_ref) <= TOL_BF16["state"]
+
+
 def test_decode_multi_one_token_is_the_step():
     """T = 1 is gdn_decode_step bit for bit; T = 0 leaves everything untouched."""
     w = syn.DecodeWorkload("t", B=4, num_k_heads=2, num_v_heads=8, K=128, V=128)
