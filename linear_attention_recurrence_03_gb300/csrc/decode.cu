@@ -401,7 +401,14 @@ struct MultiPipe {
 };
 constexpr uint32_t kStateBytes = sizeof(float) * 4 * kMaxHeadDim * 32;
 constexpr uint32_t kInputBytes = sizeof(__nv_bfloat16) * 4 * TB * kMaxHeadDim;
+// Limit of the bounded waits. GDN_TEST_STALL (a test-only build, never the library's
+// default) shortens it to 5 ms and has each pipelined CTA never copy in the inputs of its
+// second block, so that a test can see the wait run out and the status word report it.
+#ifdef GDN_TEST_STALL
+constexpr uint64_t kDecodeWaitNs = 5000000ull;
+#else
 constexpr uint64_t kDecodeWaitNs = 2000000000ull;
+#endif
 
 // Status bit of a bounded wait of this file that ran out (decode_take_status).
 __device__ uint32_t g_decode_status = 0;
@@ -634,7 +641,12 @@ __global__ void __launch_bounds__(MT, 2)
                     state_pending = true;
                 }
                 if (nr < a.BH) {
-                    if (tid == 32) issue_inputs(nr, nt0);
+#ifdef GDN_TEST_STALL
+                    const bool skip = r == (int)blockIdx.x && t0 == 0;  // the second block
+#else
+                    constexpr bool skip = false;
+#endif
+                    if (tid == 32 && !skip) issue_inputs(nr, nt0);
                     if (w == 1) load_gates(nr, nt0);
                     in_pending = true;
                 }

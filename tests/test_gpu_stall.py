@@ -56,3 +56,35 @@ def test_bounded_wait_runs_out_then_library_recovers():
     o_ref, s_ref = oracle_prefill_all(x)
     assert rel(to_np(o), o_ref) <= TOL_BF16["out"]
     assert rel(to_np(s), s_ref) <= TOL_BF16["state"]
+
+
+def test_decode_multi_wait_runs_out_then_library_recovers():
+    """The same for the multi-token decode: in the GDN_TEST_STALL build each pipelined CTA
+    never copies in the inputs of its second block of eight tokens, so with T = 16 its
+    bounded wait for them runs out (5 ms): the call reports GDN_ETIMEOUT, and the normal
+    library then runs the same call with a clean status and parity with the chained
+    oracle."""
+    ensure_built()
+    stall = _stall_library()
+    import ctypes
+    import oracle
+    names = ("q", "k", "v", "b", "a", "A_log", "dt_bias", "z", "norm_weight", "state")
+    w = syn.DecodeWorkload("t", B=1, num_k_heads=2, num_v_heads=4, K=128, V=128)
+    x = syn.decode_multi_inputs(w, 16)
+    d = [x[n].to(DEV) for n in names]
+    vp = ctypes.c_void_p
+    so = torch.empty_like(d[-1])
+    out = torch.empty((16, w.BH, w.V), dtype=torch.bfloat16, device=DEV)
+    stream = vp(torch.cuda.current_stream().cuda_stream)
+    rc = stall.gdn_decode_multi(*(vp(t.data_ptr()) for t in d), vp(so.data_ptr()),
+                                vp(out.data_ptr()), 16, w.BH, w.num_v_heads, 128, 128, stream)
+    assert rc == gdn.GDN_OK  # enqueued: the failure is found on the device
+    assert stall.gdn_get_device_status(stream) == gdn.GDN_ETIMEOUT
+    assert "bounded wait" in stall.gdn_last_error().decode()
+    assert stall.gdn_get_device_status(stream) == gdn.GDN_OK
+    y, st = gdn.gdn_decode_multi(*d, w.num_v_heads)
+    assert gdn.gdn_get_device_status() == gdn.GDN_OK
+    y_ref, s_ref = oracle.decode_multi(*(x[n] for n in names), w.num_v_heads)
+    for t in range(16):
+        assert rel(to_np(y[t].cpu()), y_ref[t]) <= TOL_BF16["out"], f"token {t}"
+    assert rel(to_np(st.cpu()), s_ref) <= TOL_BF16["state"]
