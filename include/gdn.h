@@ -207,9 +207,13 @@ gdn_status gdn_decode_step(const void* q, const void* k, const void* v, const vo
 
 /*
  * gdn_decode_multi -- T consecutive fused decode tokens of the same BH rows in one call:
- * token t applies exactly the gdn_decode_step formulas to the state left by token t-1.
+ * token t applies the gdn_decode_step formulas to the state left by token t-1.
  * Not on the pages (an extension of the "GDN TKG Kernel API Reference" step): the state
  * is read once and written once, so its HBM traffic is shared by the T tokens.
+ * For T >= 2 the tokens run in the equivalent chunk form (blocks of eight), so results
+ * agree with T single steps up to rounding, not bit for bit. The state products use
+ * two-term tf32 splits, within 2^-21 of fp32; the solve and the state update are fp32.
+ * T == 1 is gdn_decode_step bit for bit.
  *
  *   q, k         device, [T, BH, K] bf16 raw (token-major: token t's rows at t * BH).
  *   v, z         device, [T, BH, V] bf16.
