@@ -38,9 +38,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic of one layer prefill call (the four launches of prefill_tc.cu's two
 # overlapped segments, dram__bytes_read.sum + dram__bytes_write.sum, one ncu capture),
 # keyed by the sha256 of the kernel source at capture time (reported only while it
-# matches). Captured on 068059ef9cbacc67; 2b92b37d52fc85e1 differs from it only in the
-# host-side tensor-map encoder, now shared with decode.cu (no kernel changed).
-NCU_TRAFFIC = {"prefill_tc.cu@2b92b37d52fc85e1": 488020224}
+# matches).
+NCU_TRAFFIC = {"prefill_tc.cu@07004b0165fb774e": 488759552}
 
 
 def parse_args():

@@ -306,6 +306,9 @@ struct TcArgs {
     int N;
     // the prep writes K~ to the workspace (for the two-slice carry)
     int export_k;
+    // the carry is a programmatic dependent of the prep that wrote its workspace: its
+    // producer waits for that grid (griddepcontrol.wait) before the first copy
+    int ws_wait;
 };
 
 __device__ __forceinline__ size_t ws_offset(int b, int h, int c, int Hv, int nch) {
@@ -695,6 +698,9 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = misc[0];
+    // a carry launched as a programmatic dependent of this grid may start its setup once
+    // every prep CTA has begun (it waits for the grid's end before reading the workspace)
+    if (tid == 0) grid_dep_launch_dependents();
 
     if (warp == 0) {
         // -------------------------------------------- decay tables, MMA issue
@@ -1042,10 +1048,11 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
 template <int NS>
 __device__ __forceinline__ void carry_produce(uint8_t* sm, uint64_t* bar, CarryScalars* scal,
                                               const CUtensorMap* mqp, const CUtensorMap* mkp,
-                                              const CUtensorMap* mvp, bool kt_ws,
+                                              const CUtensorMap* mvp, bool kt_ws, bool ws_wait,
                                               const uint8_t* wsh, int nch, int n0, int tbase,
                                               int zq, int zv, volatile int* abort_flag) {
     using Cfg = CarryCfg<NS>;
+    if (ws_wait) grid_dep_wait();  // the prep before this grid wrote the workspace
     int lastE[2] = {-1, -1}, lastL[2] = {-1, -1};  // last chunk of each group in each stage
     for (int c = 0; c < nch; ++c) {
         const int s = c & 1;
@@ -1177,7 +1184,7 @@ __global__ void __launch_bounds__(CARRY_THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------- loads (one thread)
         if (lane == 0) {
-            carry_produce<NS>(sm, bar, scal, &mq, &mk, &mv, true,
+            carry_produce<NS>(sm, bar, scal, &mq, &mk, &mv, true, a.ws_wait != 0,
                               a.ws + ws_offset(wb, h, u0, a.Hv, a.nseg), nch, n0, tbase,
                               wb * a.Hk + h / (a.Hv / a.Hk), wb * a.Hv + h, abort_flag);
 
@@ -1590,7 +1597,7 @@ __global__ void __launch_bounds__(CARRY_T_THREADS, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            carry_produce<128>(sm, bar, scal, &mq, &mk, &mv, false,
+            carry_produce<128>(sm, bar, scal, &mq, &mk, &mv, false, a.ws_wait != 0,
                                a.ws + ws_offset(wb, h, u0, a.Hv, a.nseg), nch, 0, tbase,
                                wb * a.Hk + h / (a.Hv / a.Hk), zo, abort_flag);
         }
@@ -1966,15 +1973,21 @@ struct SegmentLaunch {
     const PrefillArgs* a;
     int sms;
 
-    TcArgs args(int c0, int nseg, uint8_t* ws) const {
+    TcArgs args(int c0, int nseg, uint8_t* ws, bool ws_wait = false) const {
         const int sin = (c0 > 0 || a->state_is_input) ? 1 : 0;
         return TcArgs{a->g,     a->beta, a->scale, a->B, a->Hk,  a->Hv,
                       a->S,     c0,      nseg,     a->state, sin,
                       static_cast<__nv_bfloat16*>(a->out), ws, a->cu_seqlens, a->table, a->N,
-                      split() ? 1 : 0};
+                      split() ? 1 : 0, ws_wait ? 1 : 0};
     }
     // sequences of the carry grid: the batch, or the variable-length batch's sequences
     int rows() const { return a->cu_seqlens ? a->N : a->B; }
+    // A one-segment call's carry runs as a programmatic dependent of its prep (same stream)
+    // when it is the two-slice carry: the B=2 Hk=4 Hv=8 S=1024 call took 37.5 us against
+    // 39.6. The transposed carry (256 CTAs of the B=8 S=4096 call) and the overlapped
+    // schedule's first carry measured slower that way (499 against 482 us; 235.5 against
+    // 223.2 us for the layer call), so they follow their prep as plain stream successors.
+    bool prep_pdl() const { return split(); }
     // two carry CTAs per head (64-column state slices) while that still fits the GPU in
     // one wave, else one transposed CTA per head
     bool split() const { return kCarrySplit && 2 * rows() * a->Hv <= sms; }
@@ -1984,17 +1997,20 @@ struct SegmentLaunch {
             mq, mk, args(c0, nseg, ws));
         return cudaGetLastError();
     }
-    // pdl: launched as a programmatic dependent of the previous kernel in `st` (the carry
-    // of the segment before), which lets its setup run before that one ends
-    cudaError_t carry(int c0, int nseg, uint8_t* ws, cudaStream_t st, bool pdl = false) const {
+    // pdl: launched as a programmatic dependent of the previous kernel in `st`, which lets
+    // its setup run before that one ends: the carry of the segment before (which wrote the
+    // state), or with after_prep the prep that wrote its workspace (the producer then waits
+    // for that grid before its first copy)
+    cudaError_t carry(int c0, int nseg, uint8_t* ws, cudaStream_t st, bool pdl = false,
+                      bool after_prep = false) const {
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cudaLaunchConfig_t cfg = {};
         cfg.stream = st;
         cfg.attrs = attr;
-        cfg.numAttrs = pdl ? 1 : 0;
-        const TcArgs ta = args(c0, nseg, ws);
+        cfg.numAttrs = (pdl || after_prep) ? 1 : 0;
+        const TcArgs ta = args(c0, nseg, ws, after_prep);
         if (split()) {
             cfg.gridDim = dim3(2, a->Hv, rows());
             cfg.blockDim = dim3(CARRY_THREADS);
@@ -2111,7 +2127,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, int c0, int nseg, cudaStream
     e = L.prep(c0, nseg, ws, stream);
     if (e != cudaSuccess) return e;
     *launched = 1;
-    e = L.carry(c0, nseg, ws, stream);
+    e = L.carry(c0, nseg, ws, stream, false, L.prep_pdl());
     if (e == cudaSuccess) *launched = 2;
     return e;
 }
@@ -2136,7 +2152,7 @@ cudaError_t launch_prefill_tc_varlen(const PrefillArgs& a, cudaStream_t stream, 
     e = L.prep(0, nmax, ws, stream);
     if (e != cudaSuccess) return e;
     *launched = 2;
-    e = L.carry(0, nmax, ws, stream);
+    e = L.carry(0, nmax, ws, stream, false, L.prep_pdl());
     if (e == cudaSuccess) *launched = 3;
     return e;
 }
@@ -2161,7 +2177,7 @@ cudaError_t launch_prefill_tc_overlapped(const PrefillArgs& a, cudaStream_t stre
         e = L.prep(0, nch, ws, stream);
         if (e != cudaSuccess) return e;
         *launched = 1;
-        e = L.carry(0, nch, ws, stream);
+        e = L.carry(0, nch, ws, stream, false, L.prep_pdl());
         if (e == cudaSuccess) *launched = 2;
         return e;
     }
@@ -2174,18 +2190,30 @@ cudaError_t launch_prefill_tc_overlapped(const PrefillArgs& a, cudaStream_t stre
     if (e == cudaSuccess) e = cudaStreamWaitEvent(o->carry, o->fork, 0);
     if (e != cudaSuccess) return e;
     // prep of segment j+1 overlaps the carry of segment j; each carry waits for its prep
-    // (a wait takes the event's latest record at the time it is enqueued)
+    // (a wait takes the event's latest record at the time it is enqueued). The first
+    // segment's prep runs on the carry stream, right before its carry (no event between
+    // them: 223 us per layer call against 237 with this prep on the prep stream), and the
+    // other preps start once it is done; the carries of the later segments are programmatic
+    // dependents of the carry before them and wait for their prep's event.
     cudaError_t le = cudaSuccess;
     for (int j = 0, c0 = 0; j < g && le == cudaSuccess; c0 += sizes[j], ++j) {
         const int n = sizes[j];
         uint8_t* wsj = ws + (size_t)a.B * (size_t)a.Hv * (size_t)c0 * WS_UNIT;
-        le = L.prep(c0, n, wsj, o->prep);
-        if (le != cudaSuccess) break;
-        ++*launched;
-        le = cudaEventRecord(o->prepped, o->prep);
-        if (le == cudaSuccess) le = cudaStreamWaitEvent(o->carry, o->prepped, 0);
-        // segments after the first are programmatic dependents of the carry before them
-        if (le == cudaSuccess) le = L.carry(c0, n, wsj, o->carry, kCarryPdl && j > 0);
+        if (j == 0) {
+            le = L.prep(c0, n, wsj, o->carry);
+            if (le != cudaSuccess) break;
+            ++*launched;
+            le = cudaEventRecord(o->fork, o->carry);
+            if (le == cudaSuccess) le = cudaStreamWaitEvent(o->prep, o->fork, 0);
+            if (le == cudaSuccess) le = L.carry(c0, n, wsj, o->carry);
+        } else {
+            le = L.prep(c0, n, wsj, o->prep);
+            if (le != cudaSuccess) break;
+            ++*launched;
+            le = cudaEventRecord(o->prepped, o->prep);
+            if (le == cudaSuccess) le = cudaStreamWaitEvent(o->carry, o->prepped, 0);
+            if (le == cudaSuccess) le = L.carry(c0, n, wsj, o->carry, kCarryPdl);
+        }
         if (le == cudaSuccess) ++*launched;
     }
     // join, also after a failed launch, so that no work is left outside the caller's stream
