@@ -33,9 +33,9 @@ namespace {
 constexpr int C = 64;      // chunk length
 constexpr int NS = 32;     // state columns per CTA
 constexpr int NT = 256;    // threads per CTA
-constexpr int DKP = 129;   // padded row stride (floats) of the q/k tiles
-constexpr int CP = C + 1;  // padded row stride of the C x C tiles
-constexpr int NSP = NS + 1;
+constexpr int DKP = 132;    // row stride (floats) of the q/k tiles: 16-byte rows
+constexpr int CP = C + 1;   // padded row stride of the C x C tiles
+constexpr int NSP = NS + 4; // row stride of the 32-column tiles: 16-byte rows
 
 struct Smem {
     float Q[C][DKP];    // q and k rows, zero from column Dk up to a multiple of 4
@@ -100,14 +100,15 @@ __global__ void __launch_bounds__(NT) prefill_simt_kernel(PrefillArgs a) {
     for (int c0 = 0; c0 < len; c0 += C) {
         const int L = min(C, len - c0);
         __syncthreads();
-        for (int idx = tid; idx < C * Dk4; idx += NT) {
-            const int r = idx / Dk4, i = idx % Dk4;
-            const bool live = r < L && i < Dk;
-            s.Q[r][i] = live ? to_f32(q[(size_t)(c0 + r) * Dk + i]) : 0.f;
-            s.K[r][i] = live ? to_f32(k[(size_t)(c0 + r) * Dk + i]) : 0.f;
+        for (int r = tid >> 6; r < C; r += NT >> 6) {
+            for (int i = tid & 63; i < Dk4; i += 64) {
+                const bool live = r < L && i < Dk;
+                s.Q[r][i] = live ? to_f32(q[(size_t)(c0 + r) * Dk + i]) : 0.f;
+                s.K[r][i] = live ? to_f32(k[(size_t)(c0 + r) * Dk + i]) : 0.f;
+            }
         }
-        for (int idx = tid; idx < C * NS; idx += NT) {
-            const int r = idx / NS, n = idx % NS;
+        for (int r = tid >> 5; r < C; r += NT >> 5) {
+            const int n = tid & 31;
             s.Y[r][n] = (r < L && n < nw) ? to_f32(v[(size_t)(c0 + r) * Dv + n0 + n]) : 0.f;
         }
         if (tid < C) {
@@ -143,12 +144,17 @@ __global__ void __launch_bounds__(NT) prefill_simt_kernel(PrefillArgs a) {
                 float kk[4] = {0.f, 0.f, 0.f, 0.f}, qk[4] = {0.f, 0.f, 0.f, 0.f};
                 if (j <= r) {
                     for (int i = 0; i < Dk4; i += 4) {
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float kj = s.K[j][i + e];
-                            kk[e] = fmaf(s.K[r][i + e], kj, kk[e]);
-                            qk[e] = fmaf(s.Q[r][i + e], kj, qk[e]);
-                        }
+                        const float4 kj = *reinterpret_cast<const float4*>(&s.K[j][i]);
+                        const float4 kr = *reinterpret_cast<const float4*>(&s.K[r][i]);
+                        const float4 qr = *reinterpret_cast<const float4*>(&s.Q[r][i]);
+                        kk[0] = fmaf(kr.x, kj.x, kk[0]);
+                        kk[1] = fmaf(kr.y, kj.y, kk[1]);
+                        kk[2] = fmaf(kr.z, kj.z, kk[2]);
+                        kk[3] = fmaf(kr.w, kj.w, kk[3]);
+                        qk[0] = fmaf(qr.x, kj.x, qk[0]);
+                        qk[1] = fmaf(qr.y, kj.y, qk[1]);
+                        qk[2] = fmaf(qr.z, kj.z, qk[2]);
+                        qk[3] = fmaf(qr.w, kj.w, qk[3]);
                     }
                 }
                 const float kks = (kk[0] + kk[1]) + (kk[2] + kk[3]);
@@ -158,20 +164,42 @@ __global__ void __launch_bounds__(NT) prefill_simt_kernel(PrefillArgs a) {
                 s.P[r][j] = qks * d;
             }
         }
-        // K S0 and Q S0
-        for (int idx = tid; idx < C * NS; idx += NT) {
-            const int r = idx / NS, n = idx % NS;
-            float ks[4] = {0.f, 0.f, 0.f, 0.f}, qs[4] = {0.f, 0.f, 0.f, 0.f};
+        // K S0 and Q S0: thread = rows rb, rb + 32 and columns cb .. cb + 3, over four keys
+        // at a time (16-byte loads of the q/k rows and of four state rows)
+        {
+            const int rb = tid >> 3, cb = 4 * (tid & 7);
+            float ks[2][4] = {}, qs[2][4] = {};
             for (int i = 0; i < Dk4; i += 4) {
+                float sv[4][4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float sv = s.S[i + e][n];
-                    ks[e] = fmaf(s.K[r][i + e], sv, ks[e]);
-                    qs[e] = fmaf(s.Q[r][i + e], sv, qs[e]);
+                    const float4 x = *reinterpret_cast<const float4*>(&s.S[i + e][cb]);
+                    sv[e][0] = x.x, sv[e][1] = x.y, sv[e][2] = x.z, sv[e][3] = x.w;
+                }
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int r = rb + 32 * hh;
+                    const float4 kr = *reinterpret_cast<const float4*>(&s.K[r][i]);
+                    const float4 qr = *reinterpret_cast<const float4*>(&s.Q[r][i]);
+                    const float kv[4] = {kr.x, kr.y, kr.z, kr.w}, qv[4] = {qr.x, qr.y, qr.z, qr.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            ks[hh][c] = fmaf(kv[e], sv[e][c], ks[hh][c]);
+                            qs[hh][c] = fmaf(qv[e], sv[e][c], qs[hh][c]);
+                        }
+                    }
                 }
             }
-            s.KS[r][n] = (ks[0] + ks[1]) + (ks[2] + ks[3]);
-            s.QS[r][n] = (qs[0] + qs[1]) + (qs[2] + qs[3]);
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    s.KS[rb + 32 * hh][cb + c] = ks[hh][c];
+                    s.QS[rb + 32 * hh][cb + c] = qs[hh][c];
+                }
+            }
         }
         __syncthreads();
         // Y = diag(beta) (V - diag(Gamma) K S0)
@@ -197,30 +225,64 @@ __global__ void __launch_bounds__(NT) prefill_simt_kernel(PrefillArgs a) {
             }
         }
         __syncthreads();
-        // O = scale (diag(Gamma) Q S0 + P U), written for live rows and columns (P is zero
-        // above the diagonal)
-        for (int idx = tid; idx < C * NS; idx += NT) {
-            const int r = idx / NS, n = idx % NS;
-            float pu[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int j = 0; j <= r; j += 4) {
+        // O = scale (diag(Gamma) Q S0 + P U), written for live rows and columns: thread =
+        // rows rb, rb + 32 and columns cb .. cb + 3 (P is zero above the diagonal, so the
+        // sum runs to the later row's diagonal for both)
+        {
+            const int rb = tid >> 3, cb = 4 * (tid & 7);
+            float pu[2][4] = {};
+            for (int j = 0; j <= rb + 32; ++j) {
+                const float4 u = *reinterpret_cast<const float4*>(&s.U[j][cb]);
+                const float uv[4] = {u.x, u.y, u.z, u.w};
+                const float p0 = s.P[rb][j], p1 = s.P[rb + 32][j];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) pu[e] = fmaf(s.P[r][j + e], s.U[j + e][n], pu[e]);
+                for (int c = 0; c < 4; ++c) {
+                    pu[0][c] = fmaf(p0, uv[c], pu[0][c]);
+                    pu[1][c] = fmaf(p1, uv[c], pu[1][c]);
+                }
             }
-            const float pus = (pu[0] + pu[1]) + (pu[2] + pu[3]);
-            const float o = a.scale * fmaf(s.Gam[r], s.QS[r][n], pus);
-            if (r < L && n < nw) store_as(&out[(size_t)(c0 + r) * Dv + n0 + n], o);
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int r = rb + 32 * hh;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int n = cb + c;
+                    const float o = a.scale * fmaf(s.Gam[r], s.QS[r][n], pu[hh][c]);
+                    if (r < L && n < nw) store_as(&out[(size_t)(c0 + r) * Dv + n0 + n], o);
+                }
+            }
         }
-        // S1 = Gamma_last S0 + sum_j exp(gamma_last - gamma_j) k_j u_j^T
-        const float Gl = expf(gl);
-        for (int idx = tid; idx < Dk * NS; idx += NT) {
-            const int i = idx / NS, n = idx % NS;
-            float acc[4] = {Gl * s.S[i][n], 0.f, 0.f, 0.f};
-            for (int j = 0; j < C; j += 4) {
+        // S1 = Gamma_last S0 + sum_j exp(gamma_last - gamma_j) k_j u_j^T: thread = state rows
+        // ib + 32 m (m < 4) and columns cb .. cb + 3 (rows from Dk on stay zero)
+        {
+            const float Gl = expf(gl);
+            const int ib = tid >> 3, cb = 4 * (tid & 7);
+            float acc[4][4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    acc[e] = fmaf(s.dec[j + e] * s.K[j + e][i], s.U[j + e][n], acc[e]);
+            for (int m = 0; m < 4; ++m) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) acc[m][c] = Gl * s.S[ib + 32 * m][cb + c];
             }
-            s.S[i][n] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+            for (int j = 0; j < C; ++j) {
+                const float4 u = *reinterpret_cast<const float4*>(&s.U[j][cb]);
+                const float uv[4] = {u.x, u.y, u.z, u.w};
+                const float d = s.dec[j];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const int i = ib + 32 * m;
+                    const float kd = i < Dk4 ? d * s.K[j][i] : 0.f;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) acc[m][c] = fmaf(kd, uv[c], acc[m][c]);
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int i = ib + 32 * m;
+                if (i < Dk) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) s.S[i][cb + c] = acc[m][c];
+                }
+            }
         }
     }
     __syncthreads();
